@@ -1,0 +1,433 @@
+#!/usr/bin/env python3
+"""Throughput of the fused FGP step on the 3D TV dual, one JSON line.
+
+Workload (default): the 512^3 fp32 volume, 20 outer iterations x 10 FGP steps
+with p and r warm-started across outers, t reset to 1 at each outer, fresh
+noise in b at each outer, lambda 0.02.  One bench step is one outer
+iteration: tvfgp_run (10 FGP steps) + tvfgp_primal (z of p).
+
+Metric: Gvoxel-updates per second (voxels x FGP steps / s), with ms per FGP
+step beside it, and the HBM roofline fraction of the step kernel from the
+13-volume traffic model of the page "TV solver: the FGP step on the GPU"
+(section "Variants": read b, r(3), p(3); write p(3), r(3) = 52 bytes per
+voxel and step).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+Under torchrun with N > 1 each rank runs an independent replica (the step
+needs no exchange between replicas): weak scaling, max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "ms per FGP step and Gvoxel/s at 512³ fp32; % of GB300 HBM roofline"
+UNIT = "Gvoxel/s"
+BYTES_PER_VOXEL_STEP = 52        # 13 fp32 volumes per FGP step
+BYTES_PER_VOXEL_PRIMAL = 20      # read b, dual(3); write z
+# page "TV solver: the FGP step on the GPU", section "At 512³": the fused
+# kernel on an RTX 5070, 12.607 ms per FGP step at 512^3
+PAGE_FUSED_512_MS = 12.607
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100, help="timed bench steps (outer iterations)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default="c4", help="c1..c5 (default c4: 512^3)")
+    ap.add_argument("--variant", default="auto", choices=["auto", "fused", "scalar", "zmarch"])
+    ap.add_argument("--eager", action="store_true", help="launch eagerly instead of graph replay")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (independent replicas)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(world):
+    if world <= 1:
+        return None
+    import torch
+    import torch.distributed as dist
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    import torch
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "200"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = []
+        for line in self.file.read().splitlines():
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) != 8:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:]))
+            except ValueError:
+                continue
+        os.unlink(self.file.name)
+        inside = [r for r in rows if t0 - 0.1 <= r[0] <= t1 + 0.1] or rows
+        if not inside:
+            return None
+        reasons = sorted({n for r in inside for n, v in zip(self.NAMES, r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+def gpu_id_for(torch, dev) -> str | None:
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        return vis.split(",")[0] if vis else None
+
+
+# ---------------------------------------------------------------------------
+# roofline inputs
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for fn in ("fgp_kernels.cuh", "zmarch_tma.cuh", "tvfgp.cu"):
+        with open(os.path.join(ROOT, "fgp_dual_stencil_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_name: str, nvox: int):
+    """DRAM bytes per launch of the step kernel from the committed ncu
+    summary, scaled to this volume; None when the kernel source changed since
+    the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(kernel_name)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return float(ent["dram_bytes_per_voxel"]) * nvox
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def gpu_arm(args, world, rank, local_rank, dist):
+    import numpy as np
+    import torch
+    from fgp_dual_stencil_gb300 import synth
+    from fgp_dual_stencil_gb300 import tvfgp as T
+
+    w = synth.WORKLOADS[args.workload]
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    N, K, W = w.nvox, args.steps, args.warmup
+    n_b = max(1, min(w.outers, W + K))
+
+    base = synth.phantom(w)
+    b_host = [torch.from_numpy(synth.make_b(w, k, base)).pin_memory() for k in range(n_b)]
+    b_dev = [x.to(dev) for x in b_host]
+    shape = (3, w.nz, w.ny, w.nx)
+    p = torch.zeros(shape, device=dev)
+    r = torch.zeros(shape, device=dev)
+    z = torch.empty((w.nz, w.ny, w.nx), device=dev)
+    h = T.Tvfgp(w.nx, w.ny, w.nz, args.variant, graph=not args.eager)
+    stream = torch.cuda.current_stream(dev)
+
+    def outer(b):
+        h.run(b, p, r, w.lam, w.steps, w.t0, stream)
+        h.primal(b, p, w.lam, z, stream)
+
+    for j in range(W):
+        outer(b_dev[j % n_b])
+    if h.check(stream) != T.TVFGP_OK:
+        raise RuntimeError("device error word set during warm-up")
+    variant_used = h.last_variant
+    launches0 = h.launch_count
+
+    sampler = ClockSampler(gpu_id_for(torch, dev)) if not args.no_clocks else None
+    if sampler is not None:
+        time.sleep(0.6)                       # let the sampler start before the timed region
+    ev_start = torch.cuda.Event(enable_timing=True)
+    ev_end = torch.cuda.Event(enable_timing=True)
+    ev_run = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    ev_start.record(stream)
+    for j in range(K):
+        b = b_dev[(W + j) % n_b]
+        ev_run[j][0].record(stream)
+        h.run(b, p, r, w.lam, w.steps, w.t0, stream)
+        ev_run[j][1].record(stream)
+        h.primal(b, p, w.lam, z, stream)
+    ev_end.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    barrier(dist)
+    clocks = sampler.stop(t_wall0, t_wall1) if sampler is not None else None
+    if h.check(stream) != T.TVFGP_OK:
+        raise RuntimeError("device error word set during the timed region")
+    launches = h.launch_count - launches0
+
+    elapsed_ms = max_over_ranks(dist, ev_start.elapsed_time(ev_end))
+    run_ms = max_over_ranks(dist, sum(a.elapsed_time(b_) for a, b_ in ev_run))
+    fgp_launch_s = run_ms / 1e3 / (K * w.steps)
+
+    value = world * N * w.steps * K / (elapsed_ms / 1e3) / 1e9
+    peak, peak_kind = hbm_peak()
+    achieved = BYTES_PER_VOXEL_STEP * N / fgp_launch_s / 1e9
+    kname = {T.TVFGP_VARIANT_FUSED: "fgp_step_fused4", T.TVFGP_VARIANT_SCALAR: "fgp_step_scalar",
+             T.TVFGP_VARIANT_ZMARCH_TMA: "fgp_step_zmarch_tma"}.get(variant_used, "?")
+    traffic = ncu_traffic(kname, N)
+
+    # end to end: pinned host b in, z out, every step, through the public API
+    e2e = None
+    if not args.no_e2e:
+        z_host = torch.empty((w.nz, w.ny, w.nx), dtype=torch.float32).pin_memory()
+        b_in = torch.empty_like(b_dev[0])
+        Ke = K
+        barrier(dist)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for j in range(Ke):
+            b_in.copy_(b_host[j % n_b], non_blocking=True)
+            h.run(b_in, p, r, w.lam, w.steps, w.t0, stream)
+            h.primal(b_in, p, w.lam, z, stream)
+            z_host.copy_(z, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        e2e_s = max_over_ranks(dist, time.perf_counter() - t0)
+        barrier(dist)
+        e2e = {"value": round(world * N * w.steps * Ke / e2e_s / 1e9, 3), "unit": UNIT,
+               "h2d_bytes_per_step": 4 * N, "d2h_bytes_per_step": 4 * N,
+               "ms_per_step": round(e2e_s * 1e3 / Ke, 4)}
+        if h.check(stream) != T.TVFGP_OK:
+            raise RuntimeError("device error word set during the end-to-end run")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, base)
+
+    h.close()
+    names = {T.TVFGP_VARIANT_FUSED: "fused", T.TVFGP_VARIANT_SCALAR: "scalar",
+             T.TVFGP_VARIANT_ZMARCH_TMA: "zmarch"}
+    out = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(elapsed_ms / K, 4),
+        "ms_per_fgp_step": round(elapsed_ms / K / w.steps, 4),
+        "ms_per_fgp_launch": round(fgp_launch_s * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": round(value / (N / (PAGE_FUSED_512_MS / 1e3) / 1e9), 3)
+        if args.workload == "c4" else None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": "%dx%dx%d fp32 TV-dual FGP, %d outers x %d steps, warm p/r, t0=1 per outer, "
+                        "lambda %g; one bench step = one outer (%d FGP steps + primal)"
+                        % (w.nx, w.ny, w.nz, w.outers, w.steps, w.lam, w.steps),
+            "nx": w.nx, "ny": w.ny, "nz": w.nz, "fgp_steps_per_bench_step": w.steps,
+            "variant": names.get(variant_used, str(variant_used)),
+            "launch": "eager" if args.eager else "cuda_graph",
+            "l2": "inputs larger than L2 (%.1f GB of live buffers vs 126 MB L2)" % (11 * 4 * N / 1e9)
+            if 4 * N > 129e6 else "working set fits in L2: GB/s is not an HBM figure",
+            "parallelism": "replicas" if world > 1 else "single_gpu",
+            "vs_baseline_ref": "RTX 5070 fused kernel, 12.607 ms per FGP step at 512^3 (page figure; "
+                               "other hardware, context only)",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": kname,
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs, copy burst)" % peak_kind
+            if peak_kind == "measured" else "fallback 6.8 TB/s",
+            "traffic": None if traffic is None else round(traffic),
+            "algorithmic_bytes_per_launch": BYTES_PER_VOXEL_STEP * N,
+        },
+        "gpu_launches": launches,
+        "e2e": e2e,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    return out
+
+
+def cpu_baseline(w, base):
+    """The CPU oracle, as it stands, on a bounded sample of the workload: one
+    outer iteration (w.steps FGP steps + primal) on the full volume, all host
+    cores."""
+    import numpy as np
+    import oracle
+    from fgp_dual_stencil_gb300 import synth
+    b = synth.make_b(w, 0, base)
+    p = np.zeros((3,) + b.shape, np.float32)
+    r = np.zeros_like(p)
+    t0 = time.perf_counter()
+    oracle.fgp_run(b, p, r, w.lam, w.steps, w.t0)
+    oracle.primal(b, p, w.lam)
+    dt = time.perf_counter() - t0
+    return {"value": round(w.nvox * w.steps / dt / 1e9, 4), "unit": UNIT, "cores": oracle.get_threads(),
+            "kind": "oracle",
+            "sample": "one outer iteration (%d FGP steps + primal) on the full %dx%dx%d volume, %.1f s"
+                      % (w.steps, w.nx, w.ny, w.nz, dt)}
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the CPU oracle on the same workload
+# ---------------------------------------------------------------------------
+
+def reference_arm(args, world, rank):
+    import numpy as np
+    import oracle
+    from fgp_dual_stencil_gb300 import synth
+
+    w = synth.WORKLOADS[args.workload]
+    K, W = args.steps, args.warmup
+    nzs = min(w.nz, 32)                       # bounded sample: a z-slab of the volume
+    n_b = max(1, min(w.outers, W + K))
+    base = synth.phantom(w)
+    slabs = [np.ascontiguousarray(synth.make_b(w, k, base)[:nzs]) for k in range(n_b)]
+    p = np.zeros((3,) + slabs[0].shape, np.float32)
+    r = np.zeros_like(p)
+
+    def outer(b):
+        oracle.fgp_run(b, p, r, w.lam, w.steps, w.t0)
+        oracle.primal(b, p, w.lam)
+
+    for j in range(W):
+        outer(slabs[j % n_b])
+    t0 = time.perf_counter()
+    for j in range(K):
+        outer(slabs[(W + j) % n_b])
+    dt = time.perf_counter() - t0
+    nvox = w.nx * w.ny * nzs
+    value = nvox * w.steps * K / dt / 1e9
+    sample = ("each step: one outer iteration (%d FGP steps + primal) on a %dx%dx%d z-slab of the "
+              "%dx%dx%d volume" % (w.steps, w.nx, w.ny, nzs, w.nx, w.ny, w.nz))
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(dt * 1e3 / K, 3),
+        "ms_per_fgp_step": round(dt * 1e3 / K / w.steps * (w.nz / nzs), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "%dx%dx%d fp32 TV-dual FGP, %d outers x %d steps, lambda %g (oracle on a "
+                               "z-slab sample)" % (w.nx, w.ny, w.nz, w.outers, w.steps, w.lam),
+                   "nx": w.nx, "ny": w.ny, "nz": w.nz, "sample_nz": nzs},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": oracle.get_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    args = parse_args()
+    world, rank, local_rank = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(reference_arm(args, world, rank)), flush=True)
+        return 0
+    dist = dist_init(world)
+    out = gpu_arm(args, world, rank, local_rank, dist)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,412 @@
+// Kernels of the FGP step on the 3D isotropic TV dual (sm_103a).
+//
+// The step (page "TV solver: the FGP step on the GPU", section "What one step
+// does"): z(j) = max(b(j) - lambda L(r)(j), 0) with L(r)(j) = sum_a r_a(j) -
+// r_a(j - e_a); g_a = z(i) - z(i + e_a); q = r(i) + g/(12 lambda);
+// p' = q / max(1, |q|); r(i) = p' + m (p' - p(i)); p(i) = p'.  Boundaries:
+// r_a(-1) = 0, and g_a = 0 where i + e_a leaves the volume.
+//
+// Every kernel here evaluates exactly the same fp32 expressions in the same
+// order (explicit __f*_rn intrinsics, so no multiply-add is ever contracted),
+// which makes all variants bitwise identical to each other and to a CPU
+// evaluation of the same canonical order:
+//   L   = ((r0(j) - r0(j-ex)) + (r1(j) - r1(j-ey))) + (r2(j) - r2(j-ez))
+//   z   = max(b - lambda*L, 0)
+//   q_a = r_a + g_a*s,  s = 1/(12 lambda) rounded to float once
+//   |q| = sqrt((q0*q0 + q1*q1) + q2*q2);  p'_a = q_a / max(1, |q|)
+//   r_a = p'_a + m*(p'_a - p_a)
+// Dividing by max(1,|q|) equals q itself when |q| <= 1, so the division is
+// only issued when |q| > 1 (IEEE x/1 == x).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tvfgp {
+
+// Arguments of one FGP step.  Volumes are fp32, x fastest; dual fields are
+// planar [3][N] (component a at a*N + i).
+struct StepArgs {
+    const float *b;
+    float *p;
+    const float *rs;   // r read by this step
+    float *rd;         // r written by this step (distinct buffer: neighbours still read rs)
+    float lam;
+    float s;           // 1/(12 lambda) rounded once to float
+    float m;           // momentum weight of this step
+    int nx, ny, nz;
+    long long N;       // nx*ny*nz
+};
+
+struct PrimalArgs {
+    const float *b;
+    const float *d;    // dual field [3][N]
+    float *z;
+    float lam;
+    int nx, ny, nz;
+    long long N;
+};
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kErrTimeout = 5;   // value written to the device error word
+
+// ---------------------------------------------------------------------------
+// scalar pieces of the step (the single definition every kernel uses)
+// ---------------------------------------------------------------------------
+
+// z = max(b - lambda * ((d0 + d1) + d2), 0)
+__device__ __forceinline__ float zval(float b, float lam, float d0, float d1, float d2)
+{
+    const float L = __fadd_rn(__fadd_rn(d0, d1), d2);
+    return fmaxf(__fsub_rn(b, __fmul_rn(lam, L)), 0.0f);
+}
+
+// q = r + g*s, projection onto the unit ball, extrapolation.  Writes p' into
+// (p0,p1,p2) and the new r into (r0,r1,r2).
+__device__ __forceinline__ void dual_update(float &r0, float &r1, float &r2,
+                                            float g0, float g1, float g2,
+                                            float &p0, float &p1, float &p2,
+                                            float s, float m)
+{
+    float q0 = __fadd_rn(r0, __fmul_rn(g0, s));
+    float q1 = __fadd_rn(r1, __fmul_rn(g1, s));
+    float q2 = __fadd_rn(r2, __fmul_rn(g2, s));
+    const float nn = __fadd_rn(__fadd_rn(__fmul_rn(q0, q0), __fmul_rn(q1, q1)), __fmul_rn(q2, q2));
+    const float n = __fsqrt_rn(nn);
+    if (n > 1.0f) {
+        q0 = __fdiv_rn(q0, n);
+        q1 = __fdiv_rn(q1, n);
+        q2 = __fdiv_rn(q2, n);
+    }
+    r0 = __fadd_rn(q0, __fmul_rn(m, __fsub_rn(q0, p0)));
+    r1 = __fadd_rn(q1, __fmul_rn(m, __fsub_rn(q1, p1)));
+    r2 = __fadd_rn(q2, __fmul_rn(m, __fsub_rn(q2, p2)));
+    p0 = q0;
+    p1 = q1;
+    p2 = q2;
+}
+
+// ---------------------------------------------------------------------------
+// memory helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float4 ld_ro4(const float *p)      // read-only for the kernel
+{
+    return __ldg(reinterpret_cast<const float4 *>(p));
+}
+__device__ __forceinline__ float4 ld_once4(const float *p)    // read once, then overwritten
+{
+    return __ldcs(reinterpret_cast<const float4 *>(p));
+}
+__device__ __forceinline__ void st4(float *p, float4 v)
+{
+    *reinterpret_cast<float4 *>(p) = v;
+}
+__device__ __forceinline__ float4 f4zero()
+{
+    return make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// z at four consecutive x voxels from their b and r, the r0 of the voxel left
+// of the first one, and r1, r2 of the lower neighbours in y and z.
+__device__ __forceinline__ float4 zquad(float4 B, float4 R0, float4 R1, float4 R2, float r0left,
+                                        float4 R1lo, float4 R2lo, float lam)
+{
+    float4 z;
+    z.x = zval(B.x, lam, __fsub_rn(R0.x, r0left), __fsub_rn(R1.x, R1lo.x), __fsub_rn(R2.x, R2lo.x));
+    z.y = zval(B.y, lam, __fsub_rn(R0.y, R0.x), __fsub_rn(R1.y, R1lo.y), __fsub_rn(R2.y, R2lo.y));
+    z.z = zval(B.z, lam, __fsub_rn(R0.z, R0.y), __fsub_rn(R1.z, R1lo.z), __fsub_rn(R2.z, R2lo.z));
+    z.w = zval(B.w, lam, __fsub_rn(R0.w, R0.z), __fsub_rn(R1.w, R1lo.w), __fsub_rn(R2.w, R2lo.w));
+    return z;
+}
+
+// ---------------------------------------------------------------------------
+// FUSED: one kernel per step, float4 along x, z carried along z in registers
+// ---------------------------------------------------------------------------
+//
+// Block (32, BY): a warp is 32 consecutive x-quads (128 voxels) of one row
+// (y, z); the block stacks BY rows in y.  Each thread walks ZC planes in z.
+// At plane z it needs z(i), z(i+ex), z(i+ey), z(i+ez) for its 4 voxels:
+//   z(i)     was computed at the previous plane as that plane's z(i+ez);
+//   z(i+ex)  is the neighbour lane's z(i) (shuffle; lane 31 computes it);
+//   z(i+ey)  is recomputed from row y+1 (whose r1 lower neighbour is the
+//            thread's own r1, and whose r2 lower neighbour was loaded at the
+//            previous plane);
+//   z(i+ez)  is recomputed from the next plane's own data, which is the
+//            prefetch of the next iteration.
+// The voxel's own p loads are issued first in every iteration, then the
+// next plane's own b and r, then row y+1: no barrier exists in this kernel.
+// Requirements: nx % 4 == 0 and 16-byte aligned b, p, rs, rd.
+template <int BY, int ZC>
+__global__ void __launch_bounds__(32 * BY, 2) fgp_step_fused4(const StepArgs a)
+{
+    const int lane = threadIdx.x;
+    const int x0 = (blockIdx.x * 32 + lane) * 4;
+    const int y = blockIdx.y * BY + threadIdx.y;
+    const int nx = a.nx, ny = a.ny, nz = a.nz;
+    if (y >= ny) return;                         // whole warp: y is warp-uniform
+    const int zb = blockIdx.z * ZC;
+    const int ze = min(zb + ZC, nz);
+    const bool xin = x0 < nx;
+    const bool hasY = (y + 1 < ny);              // warp-uniform
+    const int sz = nx * ny;
+    const float lam = a.lam, s = a.s, m = a.m;
+
+    const float *__restrict__ b = a.b;
+    const float *__restrict__ r0 = a.rs;
+    const float *__restrict__ r1 = a.rs + a.N;
+    const float *__restrict__ r2 = a.rs + 2 * a.N;
+    float *__restrict__ p0 = a.p;
+    float *__restrict__ p1 = a.p + a.N;
+    float *__restrict__ p2 = a.p + 2 * a.N;
+    float *__restrict__ o0 = a.rd;
+    float *__restrict__ o1 = a.rd + a.N;
+    float *__restrict__ o2 = a.rd + 2 * a.N;
+
+    int z = zb;
+    int i = x0 + nx * (y + ny * z);
+
+    // prologue: own r at plane zb and z(i) there
+    float4 R0c = f4zero(), R1c = f4zero(), R2c = f4zero(), Zc;
+    {
+        float4 Bc = f4zero(), R1lo = f4zero(), R2lo = f4zero();
+        if (xin) {
+            Bc = ld_ro4(b + i);
+            R0c = ld_ro4(r0 + i);
+            R1c = ld_ro4(r1 + i);
+            R2c = ld_ro4(r2 + i);
+            if (y > 0) R1lo = ld_ro4(r1 + i - nx);
+            if (z > 0) R2lo = ld_ro4(r2 + i - sz);
+        }
+        float left = __shfl_up_sync(kFull, R0c.w, 1);
+        if (lane == 0) left = (x0 > 0) ? __ldg(r0 + i - 1) : 0.0f;
+        Zc = zquad(Bc, R0c, R1c, R2c, left, R1lo, R2lo, lam);
+    }
+    // r2 of row y+1 one plane below (the z-lower neighbour of z(i+ey))
+    float4 R2yp = f4zero();
+    if (xin && hasY && z > 0) R2yp = ld_ro4(r2 + i + nx - sz);
+
+    for (; z < ze; ++z, i += sz) {
+        const bool hasZ = (z + 1 < nz);          // block-uniform
+
+        // (1) the voxel's own p, first
+        float4 P0 = f4zero(), P1 = f4zero(), P2 = f4zero();
+        if (xin) {
+            P0 = ld_once4(p0 + i);
+            P1 = ld_once4(p1 + i);
+            P2 = ld_once4(p2 + i);
+        }
+        // (2) the next plane's own b, r (and r1 of its y-lower row)
+        float4 Bn = f4zero(), R0n = f4zero(), R1n = f4zero(), R2n = f4zero(), R1lon = f4zero();
+        if (xin && hasZ) {
+            Bn = ld_ro4(b + i + sz);
+            R0n = ld_ro4(r0 + i + sz);
+            R1n = ld_ro4(r1 + i + sz);
+            R2n = ld_ro4(r2 + i + sz);
+            if (y > 0) R1lon = ld_ro4(r1 + i + sz - nx);
+        }
+        // (3) row y+1 of this plane
+        float4 By = f4zero(), R0y = f4zero(), R1y = f4zero(), R2y = f4zero();
+        if (xin && hasY) {
+            By = ld_ro4(b + i + nx);
+            R0y = ld_ro4(r0 + i + nx);
+            R1y = ld_ro4(r1 + i + nx);
+            R2y = ld_ro4(r2 + i + nx);
+        }
+
+        // z(i+ey)
+        float4 ZY = f4zero();
+        if (hasY) {
+            float left = __shfl_up_sync(kFull, R0y.w, 1);
+            if (lane == 0) left = (x0 > 0) ? __ldg(r0 + i + nx - 1) : 0.0f;
+            ZY = zquad(By, R0y, R1y, R2y, left, R1c, R2yp, lam);
+        }
+        // z(i+ez)
+        float4 ZZ = f4zero();
+        if (hasZ) {
+            float left = __shfl_up_sync(kFull, R0n.w, 1);
+            if (lane == 0) left = (x0 > 0) ? __ldg(r0 + i + sz - 1) : 0.0f;
+            ZZ = zquad(Bn, R0n, R1n, R2n, left, R1lon, R2c, lam);
+        }
+        // z(i+ex) of the last voxel: the next lane's first z
+        float zx = __shfl_down_sync(kFull, Zc.x, 1);
+        if (lane == 31 && x0 + 4 < nx) {
+            const int j = i + 4;
+            const float d0 = __fsub_rn(__ldg(r0 + j), R0c.w);
+            const float d1 = __fsub_rn(__ldg(r1 + j), y > 0 ? __ldg(r1 + j - nx) : 0.0f);
+            const float d2 = __fsub_rn(__ldg(r2 + j), z > 0 ? __ldg(r2 + j - sz) : 0.0f);
+            zx = zval(__ldg(b + j), lam, d0, d1, d2);
+        }
+
+        if (xin) {
+            const float gx3 = (x0 + 3 < nx - 1) ? __fsub_rn(Zc.w, zx) : 0.0f;
+            float4 G1 = f4zero(), G2 = f4zero();
+            if (hasY) {
+                G1.x = __fsub_rn(Zc.x, ZY.x); G1.y = __fsub_rn(Zc.y, ZY.y);
+                G1.z = __fsub_rn(Zc.z, ZY.z); G1.w = __fsub_rn(Zc.w, ZY.w);
+            }
+            if (hasZ) {
+                G2.x = __fsub_rn(Zc.x, ZZ.x); G2.y = __fsub_rn(Zc.y, ZZ.y);
+                G2.z = __fsub_rn(Zc.z, ZZ.z); G2.w = __fsub_rn(Zc.w, ZZ.w);
+            }
+            float4 N0 = R0c, N1 = R1c, N2 = R2c;
+            dual_update(N0.x, N1.x, N2.x, __fsub_rn(Zc.x, Zc.y), G1.x, G2.x, P0.x, P1.x, P2.x, s, m);
+            dual_update(N0.y, N1.y, N2.y, __fsub_rn(Zc.y, Zc.z), G1.y, G2.y, P0.y, P1.y, P2.y, s, m);
+            dual_update(N0.z, N1.z, N2.z, __fsub_rn(Zc.z, Zc.w), G1.z, G2.z, P0.z, P1.z, P2.z, s, m);
+            dual_update(N0.w, N1.w, N2.w, gx3, G1.w, G2.w, P0.w, P1.w, P2.w, s, m);
+            st4(p0 + i, P0);
+            st4(p1 + i, P1);
+            st4(p2 + i, P2);
+            st4(o0 + i, N0);
+            st4(o1 + i, N1);
+            st4(o2 + i, N2);
+        }
+
+        R0c = R0n;
+        R1c = R1n;
+        R2c = R2n;
+        Zc = ZZ;
+        R2yp = R2y;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// SCALAR: one voxel per thread, any shape and alignment
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float zpoint(const float *__restrict__ b, const float *__restrict__ r0,
+                                        const float *__restrict__ r1, const float *__restrict__ r2,
+                                        int x, int y, int z, long long j, int nx, long long sz,
+                                        float lam)
+{
+    const float d0 = __fsub_rn(__ldg(r0 + j), x > 0 ? __ldg(r0 + j - 1) : 0.0f);
+    const float d1 = __fsub_rn(__ldg(r1 + j), y > 0 ? __ldg(r1 + j - nx) : 0.0f);
+    const float d2 = __fsub_rn(__ldg(r2 + j), z > 0 ? __ldg(r2 + j - sz) : 0.0f);
+    return zval(__ldg(b + j), lam, d0, d1, d2);
+}
+
+__global__ void __launch_bounds__(256) fgp_step_scalar(const StepArgs a)
+{
+    const int x = blockIdx.x * 32 + threadIdx.x;
+    const int y = blockIdx.y * 8 + threadIdx.y;
+    const int z = blockIdx.z;
+    const int nx = a.nx, ny = a.ny, nz = a.nz;
+    if (x >= nx || y >= ny) return;
+    const long long sz = (long long)nx * ny;
+    const long long i = x + (long long)nx * y + sz * z;
+    const float *r0 = a.rs, *r1 = a.rs + a.N, *r2 = a.rs + 2 * a.N;
+
+    // the voxel's own p and r first
+    float P0 = __ldcs(a.p + i), P1 = __ldcs(a.p + a.N + i), P2 = __ldcs(a.p + 2 * a.N + i);
+    float R0 = __ldg(r0 + i), R1 = __ldg(r1 + i), R2 = __ldg(r2 + i);
+
+    const float zc = zpoint(a.b, r0, r1, r2, x, y, z, i, nx, sz, a.lam);
+    const float g0 = (x < nx - 1) ? __fsub_rn(zc, zpoint(a.b, r0, r1, r2, x + 1, y, z, i + 1, nx, sz, a.lam)) : 0.0f;
+    const float g1 = (y < ny - 1) ? __fsub_rn(zc, zpoint(a.b, r0, r1, r2, x, y + 1, z, i + nx, nx, sz, a.lam)) : 0.0f;
+    const float g2 = (z < nz - 1) ? __fsub_rn(zc, zpoint(a.b, r0, r1, r2, x, y, z + 1, i + sz, nx, sz, a.lam)) : 0.0f;
+    dual_update(R0, R1, R2, g0, g1, g2, P0, P1, P2, a.s, a.m);
+    a.p[i] = P0;
+    a.p[a.N + i] = P1;
+    a.p[2 * a.N + i] = P2;
+    a.rd[i] = R0;
+    a.rd[a.N + i] = R1;
+    a.rd[2 * a.N + i] = R2;
+}
+
+// ---------------------------------------------------------------------------
+// primal z = max(b - lambda L(dual), 0)
+// ---------------------------------------------------------------------------
+
+template <int BY>
+__global__ void __launch_bounds__(32 * BY) primal_vec4(const PrimalArgs a)
+{
+    const int lane = threadIdx.x;
+    const int x0 = (blockIdx.x * 32 + lane) * 4;
+    const int y = blockIdx.y * BY + threadIdx.y;
+    const int z = blockIdx.z;
+    const int nx = a.nx, ny = a.ny;
+    if (y >= ny) return;
+    const bool xin = x0 < nx;
+    const int sz = nx * ny;
+    const int i = x0 + nx * (y + ny * z);
+    const float *d0 = a.d, *d1 = a.d + a.N, *d2 = a.d + 2 * a.N;
+    float4 B = f4zero(), D0 = f4zero(), D1 = f4zero(), D2 = f4zero(), D1lo = f4zero(), D2lo = f4zero();
+    if (xin) {
+        B = ld_ro4(a.b + i);
+        D0 = ld_ro4(d0 + i);
+        D1 = ld_ro4(d1 + i);
+        D2 = ld_ro4(d2 + i);
+        if (y > 0) D1lo = ld_ro4(d1 + i - nx);
+        if (z > 0) D2lo = ld_ro4(d2 + i - sz);
+    }
+    float left = __shfl_up_sync(kFull, D0.w, 1);
+    if (lane == 0) left = (x0 > 0) ? __ldg(d0 + i - 1) : 0.0f;
+    const float4 Z = zquad(B, D0, D1, D2, left, D1lo, D2lo, a.lam);
+    if (xin) st4(a.z + i, Z);
+}
+
+__global__ void __launch_bounds__(256) primal_scalar(const PrimalArgs a)
+{
+    const int x = blockIdx.x * 32 + threadIdx.x;
+    const int y = blockIdx.y * 8 + threadIdx.y;
+    const int z = blockIdx.z;
+    const int nx = a.nx, ny = a.ny;
+    if (x >= nx || y >= ny) return;
+    const long long sz = (long long)nx * ny;
+    const long long i = x + (long long)nx * y + sz * z;
+    a.z[i] = zpoint(a.b, a.d, a.d + a.N, a.d + 2 * a.N, x, y, z, i, nx, sz, a.lam);
+}
+
+// ---------------------------------------------------------------------------
+// bounded waits
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Poll the barrier phase with a bounded number of polls (with a short sleep
+// between them).  Returns false when the limit is reached.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int max_polls)
+{
+    for (int k = 0; k < max_polls; ++k) {
+        if (mbar_test(bar, parity)) return true;
+        __nanosleep(32);
+    }
+    return false;
+}
+
+// Test hook: wait on a barrier that nobody arrives at, give up after
+// `polls` polls, record the timeout in the error word and return.
+__global__ void timeout_probe(int *err, int polls)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const bool ok = mbar_wait_bounded(&bar, 0, polls);
+    if (!ok && threadIdx.x == 0) atomicExch(err, kErrTimeout);
+}
+
+}  // namespace tvfgp

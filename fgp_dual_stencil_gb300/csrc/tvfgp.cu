@@ -1,0 +1,553 @@
+// C-ABI of the FGP step library (declarations and contract: include/tvfgp.h).
+//
+// Host side: argument checks, the FISTA momentum schedule in double, the
+// ping-pong of r between the caller's buffer and the handle's scratch
+// buffer, eager launches back to back with no host synchronisation, and a
+// CUDA graph of the whole nsteps loop that is re-parameterised in place when
+// the buffers, lambda or t0 change (page "TV solver: the FGP step on the
+// GPU", sections "Variants" and "What made the difference").
+#include "tvfgp.h"
+#include "fgp_kernels.cuh"
+#include "zmarch_tma.cuh"
+
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <new>
+#include <vector>
+
+using namespace tvfgp;
+
+namespace {
+
+constexpr int kMagic = 0x74766670;   // "tvfp"
+constexpr int kVersion = 10000;      // 1.0.0
+
+// launch shapes of the vector kernels
+constexpr int kFusedBY = 8;
+constexpr int kFusedZC = 8;
+constexpr int kPrimalBY = 8;
+
+// The default vector variant chosen by AUTO.
+constexpr int kAutoVariant = TVFGP_VARIANT_FUSED;
+
+struct LaunchCfg {
+    const void *func;
+    dim3 grid;
+    dim3 block;
+    size_t smem;
+};
+
+struct GraphEntry {
+    int nsteps = -1;
+    int variant = -1;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    std::vector<cudaGraphNode_t> knodes;
+    cudaGraphNode_t cnode = nullptr;
+    // parameters the instantiated graph currently holds
+    const float *b = nullptr;
+    float *p = nullptr, *r = nullptr;
+    float lam = 0.f;
+    double t0 = 0.0;
+    unsigned long long use = 0;
+};
+
+constexpr int kGraphSlots = 4;
+
+}  // namespace
+
+struct tvfgp_handle {
+    int magic;
+    int nx, ny, nz;
+    long long N;
+    int variant;
+    int graph_on;
+    int last_variant;
+    long long launches;
+    float *scratch;
+    int *d_err;
+    ZmarchPlan zplan;
+    GraphEntry graphs[kGraphSlots];
+    unsigned long long graph_clock;
+};
+
+namespace {
+
+int from_cuda(cudaError_t e)
+{
+    if (e == cudaSuccess) return TVFGP_OK;
+    return e == cudaErrorMemoryAllocation ? TVFGP_ERR_OOM : TVFGP_ERR_CUDA;
+}
+
+bool valid(const tvfgp_handle *h) { return h != nullptr && h->magic == kMagic; }
+
+int check_ptr(const void *p)
+{
+    if (p == nullptr) return TVFGP_ERR_ARG;
+    if (reinterpret_cast<uintptr_t>(p) & 3u) return TVFGP_ERR_ALIGN;
+    return TVFGP_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+int check_lambda(float lam)
+{
+    if (!std::isfinite(lam) || !(lam > 0.0f)) return TVFGP_ERR_ARG;
+    const double s = 1.0 / (12.0 * static_cast<double>(lam));
+    const float sf = static_cast<float>(s);
+    if (!std::isfinite(sf) || !(sf > 0.0f)) return TVFGP_ERR_ARG;
+    return TVFGP_OK;
+}
+
+// s = 1/(12 lambda), evaluated in double and rounded once to float.
+float step_of(float lam) { return static_cast<float>(1.0 / (12.0 * static_cast<double>(lam))); }
+
+int resolve_variant(const tvfgp_handle *h, int requested, bool vec_ok)
+{
+    int v = requested == TVFGP_VARIANT_AUTO ? kAutoVariant : requested;
+    if (v == TVFGP_VARIANT_FUSED || v == TVFGP_VARIANT_ZMARCH_TMA) {
+        if (!vec_ok) return TVFGP_VARIANT_SCALAR;
+    }
+    return v;
+}
+
+StepArgs make_args(const tvfgp_handle *h, const float *b, float *p, const float *rs, float *rd,
+                   float lam, float m)
+{
+    StepArgs a;
+    a.b = b;
+    a.p = p;
+    a.rs = rs;
+    a.rd = rd;
+    a.lam = lam;
+    a.s = step_of(lam);
+    a.m = m;
+    a.nx = h->nx;
+    a.ny = h->ny;
+    a.nz = h->nz;
+    a.N = h->N;
+    return a;
+}
+
+LaunchCfg step_cfg(const tvfgp_handle *h, int variant)
+{
+    LaunchCfg c;
+    c.smem = 0;
+    if (variant == TVFGP_VARIANT_FUSED) {
+        c.func = reinterpret_cast<const void *>(&fgp_step_fused4<kFusedBY, kFusedZC>);
+        c.block = dim3(32, kFusedBY, 1);
+        c.grid = dim3((h->nx / 4 + 31) / 32, (h->ny + kFusedBY - 1) / kFusedBY,
+                      (h->nz + kFusedZC - 1) / kFusedZC);
+    } else if (variant == TVFGP_VARIANT_ZMARCH_TMA) {
+        c.func = zmarch_kernel();
+        c.block = dim3(zmarch_threads(), 1, 1);
+        c.grid = zmarch_grid(h->zplan);
+        c.smem = zmarch_smem_bytes();
+    } else {
+        c.func = reinterpret_cast<const void *>(&fgp_step_scalar);
+        c.block = dim3(32, 8, 1);
+        c.grid = dim3((h->nx + 31) / 32, (h->ny + 7) / 8, h->nz);
+    }
+    return c;
+}
+
+// Kernel-argument storage for one launch of either kernel family.
+struct KArgs {
+    StepArgs a;
+    ZmarchArgs za;
+    void *ptrs[1];
+};
+
+void fill_kargs(const tvfgp_handle *h, int variant, const StepArgs &a, KArgs &k)
+{
+    k.a = a;
+    if (variant == TVFGP_VARIANT_ZMARCH_TMA) {
+        zmarch_fill(h->zplan, a, h->d_err, k.za);
+        k.ptrs[0] = &k.za;
+    } else {
+        k.ptrs[0] = &k.a;
+    }
+}
+
+int launch_step(tvfgp_handle *h, int variant, const StepArgs &a, cudaStream_t st)
+{
+    const LaunchCfg c = step_cfg(h, variant);
+    KArgs k;
+    fill_kargs(h, variant, a, k);
+    cudaError_t e = cudaLaunchKernel(c.func, c.grid, c.block, k.ptrs, c.smem, st);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return from_cuda(e);
+    }
+    h->launches += 1;
+    h->last_variant = variant;
+    return TVFGP_OK;
+}
+
+void destroy_graph(GraphEntry &g)
+{
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+    if (g.graph) cudaGraphDestroy(g.graph);
+    g = GraphEntry();
+}
+
+// Kernel-node parameters of step k of a run.
+void step_node_params(tvfgp_handle *h, int variant, const float *b, float *p, float *r, float lam,
+                      const std::vector<double> &m, int k, KArgs &ka, cudaKernelNodeParams &kp)
+{
+    const bool even = (k % 2) == 0;
+    const StepArgs a = make_args(h, b, p, even ? r : h->scratch, even ? h->scratch : r, lam,
+                                 static_cast<float>(m[k]));
+    fill_kargs(h, variant, a, ka);
+    const LaunchCfg c = step_cfg(h, variant);
+    kp.func = const_cast<void *>(c.func);
+    kp.gridDim = c.grid;
+    kp.blockDim = c.block;
+    kp.sharedMemBytes = static_cast<unsigned>(c.smem);
+    kp.kernelParams = ka.ptrs;
+    kp.extra = nullptr;
+}
+
+int build_graph(tvfgp_handle *h, GraphEntry &g, int variant, const float *b, float *p, float *r,
+                float lam, int nsteps, double t0, const std::vector<double> &m)
+{
+    destroy_graph(g);
+    cudaError_t e = cudaGraphCreate(&g.graph, 0);
+    if (e != cudaSuccess) return from_cuda(e);
+    cudaGraphNode_t prev = nullptr;
+    g.knodes.resize(nsteps);
+    for (int k = 0; k < nsteps; ++k) {
+        KArgs ka;
+        cudaKernelNodeParams kp;
+        step_node_params(h, variant, b, p, r, lam, m, k, ka, kp);
+        e = cudaGraphAddKernelNode(&g.knodes[k], g.graph, prev ? &prev : nullptr, prev ? 1 : 0, &kp);
+        if (e != cudaSuccess) break;
+        prev = g.knodes[k];
+    }
+    if (e == cudaSuccess && (nsteps % 2) == 1)
+        e = cudaGraphAddMemcpyNode1D(&g.cnode, g.graph, &prev, 1, r, h->scratch,
+                                     sizeof(float) * 3 * static_cast<size_t>(h->N),
+                                     cudaMemcpyDeviceToDevice);
+    if (e == cudaSuccess) e = cudaGraphInstantiate(&g.exec, g.graph, 0);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        destroy_graph(g);
+        return from_cuda(e);
+    }
+    g.nsteps = nsteps;
+    g.variant = variant;
+    g.b = b;
+    g.p = p;
+    g.r = r;
+    g.lam = lam;
+    g.t0 = t0;
+    return TVFGP_OK;
+}
+
+int update_graph(tvfgp_handle *h, GraphEntry &g, const float *b, float *p, float *r, float lam,
+                 double t0, const std::vector<double> &m)
+{
+    cudaError_t e = cudaSuccess;
+    for (int k = 0; k < g.nsteps && e == cudaSuccess; ++k) {
+        KArgs ka;
+        cudaKernelNodeParams kp;
+        step_node_params(h, g.variant, b, p, r, lam, m, k, ka, kp);
+        e = cudaGraphExecKernelNodeSetParams(g.exec, g.knodes[k], &kp);
+    }
+    if (e == cudaSuccess && g.cnode)
+        e = cudaGraphExecMemcpyNodeSetParams1D(g.exec, g.cnode, r, h->scratch,
+                                               sizeof(float) * 3 * static_cast<size_t>(h->N),
+                                               cudaMemcpyDeviceToDevice);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return from_cuda(e);
+    }
+    g.b = b;
+    g.p = p;
+    g.r = r;
+    g.lam = lam;
+    g.t0 = t0;
+    return TVFGP_OK;
+}
+
+int run_graph(tvfgp_handle *h, int variant, const float *b, float *p, float *r, float lam,
+              int nsteps, double t0, const std::vector<double> &m, cudaStream_t st)
+{
+    GraphEntry *g = nullptr;
+    for (auto &e : h->graphs)
+        if (e.exec && e.nsteps == nsteps && e.variant == variant) g = &e;
+    int rc = TVFGP_OK;
+    if (g == nullptr) {
+        GraphEntry *victim = &h->graphs[0];
+        for (auto &e : h->graphs)
+            if (!e.exec || e.use < victim->use) victim = &e;
+        g = victim;
+        rc = build_graph(h, *g, variant, b, p, r, lam, nsteps, t0, m);
+    } else if (g->b != b || g->p != p || g->r != r || g->lam != lam || g->t0 != t0) {
+        rc = update_graph(h, *g, b, p, r, lam, t0, m);
+    }
+    if (rc != TVFGP_OK) return rc;
+    g->use = ++h->graph_clock;
+    cudaError_t e = cudaGraphLaunch(g->exec, st);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return from_cuda(e);
+    }
+    h->launches += nsteps;
+    h->last_variant = variant;
+    return TVFGP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tvfgp_version(void) { return kVersion; }
+
+const char *tvfgp_strerror(int code)
+{
+    switch (code) {
+    case TVFGP_OK: return "ok";
+    case TVFGP_ERR_ARG: return "invalid argument";
+    case TVFGP_ERR_ALIGN: return "pointer not 4-byte aligned";
+    case TVFGP_ERR_CUDA: return "CUDA error";
+    case TVFGP_ERR_OOM: return "out of memory";
+    case TVFGP_ERR_TIMEOUT: return "a bounded device-side wait timed out";
+    case TVFGP_ERR_UNSUPPORTED: return "variant not supported for this shape or alignment";
+    default: return "unknown status code";
+    }
+}
+
+int tvfgp_momentum(double t0, int nsteps, double *m, double *t_final)
+{
+    if (nsteps < 0 || !std::isfinite(t0) || t0 < 1.0) return TVFGP_ERR_ARG;
+    double t = t0;
+    for (int k = 0; k < nsteps; ++k) {
+        const double tn = (1.0 + std::sqrt(1.0 + 4.0 * t * t)) / 2.0;
+        if (m) m[k] = (t - 1.0) / tn;
+        t = tn;
+    }
+    if (t_final) *t_final = t;
+    return TVFGP_OK;
+}
+
+int tvfgp_create_ex(int nx, int ny, int nz, int variant, unsigned flags, tvfgp_t *out)
+{
+    if (out == nullptr) return TVFGP_ERR_ARG;
+    *out = nullptr;
+    if (nx < 1 || ny < 1 || nz < 1 || nx > 65535 || ny > 65535 || nz > 65535) return TVFGP_ERR_ARG;
+    if (static_cast<long long>(nx) * ny * (static_cast<long long>(nz) + 1) > INT_MAX) return TVFGP_ERR_ARG;
+    if (variant < TVFGP_VARIANT_AUTO || variant > TVFGP_VARIANT_ZMARCH_TMA || flags != 0)
+        return TVFGP_ERR_ARG;
+    if (variant == TVFGP_VARIANT_ZMARCH_TMA && !zmarch_supported(nx, ny, nz))
+        return TVFGP_ERR_UNSUPPORTED;
+    tvfgp_handle *h = new (std::nothrow) tvfgp_handle();
+    if (h == nullptr) return TVFGP_ERR_OOM;
+    h->magic = kMagic;
+    h->nx = nx;
+    h->ny = ny;
+    h->nz = nz;
+    h->N = static_cast<long long>(nx) * ny * nz;
+    h->variant = variant;
+    h->graph_on = 0;
+    h->last_variant = -1;
+    h->launches = 0;
+    h->graph_clock = 0;
+    h->scratch = nullptr;
+    h->d_err = nullptr;
+    cudaError_t e = cudaMalloc(&h->scratch, sizeof(float) * 3 * static_cast<size_t>(h->N));
+    if (e == cudaSuccess) e = cudaMalloc(&h->d_err, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(int));
+    if (e == cudaSuccess) {
+        const int rc = zmarch_plan(nx, ny, nz, &h->zplan);
+        if (rc != TVFGP_OK) e = cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(h->scratch);
+        cudaFree(h->d_err);
+        h->magic = 0;
+        delete h;
+        return from_cuda(e);
+    }
+    *out = h;
+    return TVFGP_OK;
+}
+
+int tvfgp_create(int nx, int ny, int nz, tvfgp_t *out)
+{
+    return tvfgp_create_ex(nx, ny, nz, TVFGP_VARIANT_AUTO, 0u, out);
+}
+
+int tvfgp_destroy(tvfgp_t h)
+{
+    if (h == nullptr) return TVFGP_OK;
+    if (!valid(h)) return TVFGP_ERR_ARG;
+    for (auto &g : h->graphs) destroy_graph(g);
+    cudaFree(h->scratch);
+    cudaFree(h->d_err);
+    h->magic = 0;
+    delete h;
+    return TVFGP_OK;
+}
+
+int tvfgp_set_variant(tvfgp_t h, int variant)
+{
+    if (!valid(h) || variant < TVFGP_VARIANT_AUTO || variant > TVFGP_VARIANT_ZMARCH_TMA)
+        return TVFGP_ERR_ARG;
+    if (variant == TVFGP_VARIANT_ZMARCH_TMA && !zmarch_supported(h->nx, h->ny, h->nz))
+        return TVFGP_ERR_UNSUPPORTED;
+    h->variant = variant;
+    return TVFGP_OK;
+}
+
+int tvfgp_set_graph(tvfgp_t h, int enable)
+{
+    if (!valid(h)) return TVFGP_ERR_ARG;
+    h->graph_on = enable != 0;
+    return TVFGP_OK;
+}
+
+int tvfgp_last_variant(tvfgp_t h) { return valid(h) ? h->last_variant : -1; }
+
+long long tvfgp_launch_count(tvfgp_t h) { return valid(h) ? h->launches : -1; }
+
+int tvfgp_step(tvfgp_t h, const float *b, float *p, const float *r_src, float *r_dst, float lambda,
+               float m, tvfgp_stream_t stream)
+{
+    if (!valid(h)) return TVFGP_ERR_ARG;
+    int rc;
+    if ((rc = check_ptr(b)) || (rc = check_ptr(p)) || (rc = check_ptr(r_src)) || (rc = check_ptr(r_dst)))
+        return rc;
+    if ((rc = check_lambda(lambda))) return rc;
+    if (!std::isfinite(m)) return TVFGP_ERR_ARG;
+    const size_t v = sizeof(float) * static_cast<size_t>(h->N);
+    if (overlap(b, v, p, 3 * v) || overlap(b, v, r_src, 3 * v) || overlap(b, v, r_dst, 3 * v) ||
+        overlap(p, 3 * v, r_src, 3 * v) || overlap(p, 3 * v, r_dst, 3 * v) ||
+        overlap(r_src, 3 * v, r_dst, 3 * v))
+        return TVFGP_ERR_ARG;
+    const bool vec_ok = (h->nx % 4 == 0) && aligned16(b) && aligned16(p) && aligned16(r_src) &&
+                        aligned16(r_dst);
+    const int variant = resolve_variant(h, h->variant, vec_ok);
+    return launch_step(h, variant, make_args(h, b, p, r_src, r_dst, lambda, m),
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+int tvfgp_run(tvfgp_t h, const float *b, float *p, float *r, float lambda, int nsteps, double t0,
+              tvfgp_stream_t stream, double *t_final)
+{
+    if (!valid(h)) return TVFGP_ERR_ARG;
+    int rc;
+    if ((rc = check_ptr(b)) || (rc = check_ptr(p)) || (rc = check_ptr(r))) return rc;
+    if ((rc = check_lambda(lambda))) return rc;
+    if (nsteps < 0 || !std::isfinite(t0) || t0 < 1.0) return TVFGP_ERR_ARG;
+    const size_t v = sizeof(float) * static_cast<size_t>(h->N);
+    if (overlap(b, v, p, 3 * v) || overlap(b, v, r, 3 * v) || overlap(p, 3 * v, r, 3 * v) ||
+        overlap(b, v, h->scratch, 3 * v) || overlap(p, 3 * v, h->scratch, 3 * v) ||
+        overlap(r, 3 * v, h->scratch, 3 * v))
+        return TVFGP_ERR_ARG;
+    std::vector<double> m(static_cast<size_t>(nsteps));
+    double tf = t0;
+    tvfgp_momentum(t0, nsteps, m.data(), &tf);
+    if (nsteps == 0) {
+        if (t_final) *t_final = tf;
+        return TVFGP_OK;
+    }
+    const bool vec_ok = (h->nx % 4 == 0) && aligned16(b) && aligned16(p) && aligned16(r);
+    const int variant = resolve_variant(h, h->variant, vec_ok);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (h->graph_on) {
+        rc = run_graph(h, variant, b, p, r, lambda, nsteps, t0, m, st);
+    } else {
+        for (int k = 0; k < nsteps && rc == TVFGP_OK; ++k) {
+            const bool even = (k % 2) == 0;
+            rc = launch_step(h, variant,
+                             make_args(h, b, p, even ? r : h->scratch, even ? h->scratch : r, lambda,
+                                       static_cast<float>(m[k])),
+                             st);
+        }
+        if (rc == TVFGP_OK && (nsteps % 2) == 1) {
+            cudaError_t e = cudaMemcpyAsync(r, h->scratch, 3 * v, cudaMemcpyDeviceToDevice, st);
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                rc = from_cuda(e);
+            }
+        }
+    }
+    if (rc == TVFGP_OK && t_final) *t_final = tf;
+    return rc;
+}
+
+int tvfgp_primal(tvfgp_t h, const float *b, const float *dual, float lambda, float *z,
+                 tvfgp_stream_t stream)
+{
+    if (!valid(h)) return TVFGP_ERR_ARG;
+    int rc;
+    if ((rc = check_ptr(b)) || (rc = check_ptr(dual)) || (rc = check_ptr(z))) return rc;
+    if ((rc = check_lambda(lambda))) return rc;
+    const size_t v = sizeof(float) * static_cast<size_t>(h->N);
+    if (overlap(z, v, b, v) || overlap(z, v, dual, 3 * v)) return TVFGP_ERR_ARG;
+    PrimalArgs a;
+    a.b = b;
+    a.d = dual;
+    a.z = z;
+    a.lam = lambda;
+    a.nx = h->nx;
+    a.ny = h->ny;
+    a.nz = h->nz;
+    a.N = h->N;
+    const bool vec_ok = (h->nx % 4 == 0) && aligned16(b) && aligned16(dual) && aligned16(z);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (vec_ok) {
+        dim3 grid((h->nx / 4 + 31) / 32, (h->ny + kPrimalBY - 1) / kPrimalBY, h->nz);
+        primal_vec4<kPrimalBY><<<grid, dim3(32, kPrimalBY, 1), 0, st>>>(a);
+    } else {
+        dim3 grid((h->nx + 31) / 32, (h->ny + 7) / 8, h->nz);
+        primal_scalar<<<grid, dim3(32, 8, 1), 0, st>>>(a);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return from_cuda(e);
+    h->launches += 1;
+    return TVFGP_OK;
+}
+
+int tvfgp_check(tvfgp_t h, tvfgp_stream_t stream)
+{
+    if (!valid(h)) return TVFGP_ERR_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return from_cuda(e);
+    }
+    int flag = 0;
+    e = cudaMemcpy(&flag, h->d_err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && flag != 0) e = cudaMemset(h->d_err, 0, sizeof(int));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return from_cuda(e);
+    }
+    return flag != 0 ? TVFGP_ERR_TIMEOUT : TVFGP_OK;
+}
+
+int tvfgp_debug_timeout_probe(tvfgp_t h, int spins, tvfgp_stream_t stream)
+{
+    if (!valid(h) || spins < 1 || spins > (1 << 24)) return TVFGP_ERR_ARG;
+    timeout_probe<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(h->d_err, spins);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return from_cuda(e);
+    h->launches += 1;
+    return TVFGP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,259 @@
+"""Python binding of libtvfgp.so (C ABI in include/tvfgp.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of the library.  Functions keep the C names.  Buffers are torch CUDA
+float32 contiguous tensors (or raw device addresses as ints): a scalar volume
+has nx*ny*nz elements (shape (nz, ny, nx) by convention), a dual field 3x that
+(shape (3, nz, ny, nx)).  ``stream`` is a torch.cuda.Stream, a raw
+cudaStream_t as int, or None for torch's current stream.
+
+If libtvfgp.so has not been built, importing this module raises ImportError:
+there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtvfgp.so")
+
+TVFGP_OK = 0
+TVFGP_ERR_ARG = 1
+TVFGP_ERR_ALIGN = 2
+TVFGP_ERR_CUDA = 3
+TVFGP_ERR_OOM = 4
+TVFGP_ERR_TIMEOUT = 5
+TVFGP_ERR_UNSUPPORTED = 6
+
+TVFGP_VARIANT_AUTO = 0
+TVFGP_VARIANT_FUSED = 1
+TVFGP_VARIANT_SCALAR = 2
+TVFGP_VARIANT_ZMARCH_TMA = 3
+
+VARIANTS = {"auto": TVFGP_VARIANT_AUTO, "fused": TVFGP_VARIANT_FUSED,
+            "scalar": TVFGP_VARIANT_SCALAR, "zmarch": TVFGP_VARIANT_ZMARCH_TMA}
+
+
+class TvfgpError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s failed: %s (status %d)" % (where, strerror(code), code))
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libtvfgp.so is not built (%s); run `python -m "
+                          "fgp_dual_stencil_gb300._build` or __graft_entry__.build()" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    i, u, d, f, vp, ll = (ctypes.c_int, ctypes.c_uint, ctypes.c_double, ctypes.c_float,
+                          ctypes.c_void_p, ctypes.c_longlong)
+    sig = {
+        "tvfgp_create": ([i, i, i, ctypes.POINTER(vp)], i),
+        "tvfgp_create_ex": ([i, i, i, i, u, ctypes.POINTER(vp)], i),
+        "tvfgp_destroy": ([vp], i),
+        "tvfgp_set_variant": ([vp, i], i),
+        "tvfgp_set_graph": ([vp, i], i),
+        "tvfgp_run": ([vp, vp, vp, vp, f, i, d, vp, ctypes.POINTER(d)], i),
+        "tvfgp_step": ([vp, vp, vp, vp, vp, f, f, vp], i),
+        "tvfgp_primal": ([vp, vp, vp, f, vp, vp], i),
+        "tvfgp_momentum": ([d, i, ctypes.POINTER(d), ctypes.POINTER(d)], i),
+        "tvfgp_check": ([vp, vp], i),
+        "tvfgp_last_variant": ([vp], i),
+        "tvfgp_launch_count": ([vp], ll),
+        "tvfgp_debug_timeout_probe": ([vp, i, vp], i),
+        "tvfgp_strerror": ([i], ctypes.c_char_p),
+        "tvfgp_version": ([], i),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+_lib = _load()
+
+
+def _ok(code: int, where: str) -> None:
+    if code != TVFGP_OK:
+        raise TvfgpError(code, where)
+
+
+def _addr(x, n: int | None, name: str):
+    """Device address of a torch tensor (checked) or a raw int address."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    import torch
+    if not isinstance(x, torch.Tensor):
+        raise TypeError("%s must be a torch tensor or an int address" % name)
+    if not x.is_cuda or x.dtype != torch.float32 or not x.is_contiguous():
+        raise ValueError("%s must be a contiguous float32 CUDA tensor" % name)
+    if n is not None and x.numel() != n:
+        raise ValueError("%s has %d elements, expected %d" % (name, x.numel(), n))
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def strerror(code: int) -> str:
+    return _lib.tvfgp_strerror(int(code)).decode()
+
+
+def tvfgp_version() -> int:
+    return int(_lib.tvfgp_version())
+
+
+def tvfgp_strerror(code: int) -> str:
+    return strerror(code)
+
+
+def tvfgp_momentum(t0: float, nsteps: int):
+    """(list of m_k, t after the last step), computed by the library's host code."""
+    m = (ctypes.c_double * max(int(nsteps), 1))()
+    tf = ctypes.c_double(0.0)
+    _ok(_lib.tvfgp_momentum(float(t0), int(nsteps), m, ctypes.byref(tf)), "tvfgp_momentum")
+    return [m[k] for k in range(int(nsteps))], tf.value
+
+
+def tvfgp_create(nx: int, ny: int, nz: int, variant: int | str = TVFGP_VARIANT_AUTO,
+                 flags: int = 0) -> int:
+    """Create a handle (an opaque int) for an nx x ny x nz volume."""
+    if isinstance(variant, str):
+        variant = VARIANTS[variant]
+    h = ctypes.c_void_p()
+    _ok(_lib.tvfgp_create_ex(int(nx), int(ny), int(nz), int(variant), int(flags), ctypes.byref(h)),
+        "tvfgp_create")
+    return h.value
+
+
+def tvfgp_destroy(h: int) -> None:
+    _ok(_lib.tvfgp_destroy(h), "tvfgp_destroy")
+
+
+def tvfgp_set_variant(h: int, variant: int | str) -> None:
+    if isinstance(variant, str):
+        variant = VARIANTS[variant]
+    _ok(_lib.tvfgp_set_variant(h, int(variant)), "tvfgp_set_variant")
+
+
+def tvfgp_set_graph(h: int, enable: bool) -> None:
+    _ok(_lib.tvfgp_set_graph(h, 1 if enable else 0), "tvfgp_set_graph")
+
+
+def tvfgp_run(h: int, b, p, r, lam: float, nsteps: int, t0: float = 1.0, stream=None,
+              n: int | None = None) -> float:
+    """nsteps FGP steps on (p, r) in place; returns t after the last step."""
+    tf = ctypes.c_double(0.0)
+    _ok(_lib.tvfgp_run(h, _addr(b, n, "b"), _addr(p, None if n is None else 3 * n, "p"),
+                       _addr(r, None if n is None else 3 * n, "r"), float(lam), int(nsteps),
+                       float(t0), _stream(stream), ctypes.byref(tf)), "tvfgp_run")
+    return tf.value
+
+
+def tvfgp_step(h: int, b, p, r_src, r_dst, lam: float, m: float, stream=None) -> None:
+    """One step with explicit momentum weight and ping-pong buffers."""
+    _ok(_lib.tvfgp_step(h, _addr(b, None, "b"), _addr(p, None, "p"), _addr(r_src, None, "r_src"),
+                        _addr(r_dst, None, "r_dst"), float(lam), float(m), _stream(stream)),
+        "tvfgp_step")
+
+
+def tvfgp_primal(h: int, b, dual, lam: float, z, stream=None) -> None:
+    """z = max(b - lam * L(dual), 0)."""
+    _ok(_lib.tvfgp_primal(h, _addr(b, None, "b"), _addr(dual, None, "dual"), float(lam),
+                          _addr(z, None, "z"), _stream(stream)), "tvfgp_primal")
+
+
+def tvfgp_check(h: int, stream=None) -> int:
+    """Synchronise the stream and return the status of the device error word
+    (TVFGP_OK or TVFGP_ERR_TIMEOUT); raises on CUDA errors."""
+    code = int(_lib.tvfgp_check(h, _stream(stream)))
+    if code not in (TVFGP_OK, TVFGP_ERR_TIMEOUT):
+        raise TvfgpError(code, "tvfgp_check")
+    return code
+
+
+def tvfgp_last_variant(h: int) -> int:
+    return int(_lib.tvfgp_last_variant(h))
+
+
+def tvfgp_launch_count(h: int) -> int:
+    return int(_lib.tvfgp_launch_count(h))
+
+
+def tvfgp_debug_timeout_probe(h: int, spins: int, stream=None) -> None:
+    _ok(_lib.tvfgp_debug_timeout_probe(h, int(spins), _stream(stream)), "tvfgp_debug_timeout_probe")
+
+
+def raw_call(name: str, *args) -> int:
+    """Call a C entry point with raw arguments and return its status code
+    (for tests of the argument checks)."""
+    return int(getattr(_lib, name)(*args))
+
+
+class Tvfgp:
+    """Owns one handle.  Tensors: b (nz, ny, nx), p and r (3, nz, ny, nx)."""
+
+    def __init__(self, nx: int, ny: int, nz: int, variant: int | str = TVFGP_VARIANT_AUTO,
+                 graph: bool = False):
+        self.shape = (int(nx), int(ny), int(nz))
+        self.n = int(nx) * int(ny) * int(nz)
+        self.h = tvfgp_create(nx, ny, nz, variant)
+        if graph:
+            tvfgp_set_graph(self.h, True)
+
+    def run(self, b, p, r, lam, nsteps, t0=1.0, stream=None) -> float:
+        return tvfgp_run(self.h, b, p, r, lam, nsteps, t0, stream, n=self.n)
+
+    def step(self, b, p, r_src, r_dst, lam, m, stream=None) -> None:
+        tvfgp_step(self.h, b, p, r_src, r_dst, lam, m, stream)
+
+    def primal(self, b, dual, lam, z=None, stream=None):
+        if z is None:
+            import torch
+            z = torch.empty_like(b)
+        tvfgp_primal(self.h, b, dual, lam, z, stream)
+        return z
+
+    def set_variant(self, v) -> None:
+        tvfgp_set_variant(self.h, v)
+
+    def set_graph(self, on: bool) -> None:
+        tvfgp_set_graph(self.h, on)
+
+    def check(self, stream=None) -> int:
+        return tvfgp_check(self.h, stream)
+
+    @property
+    def last_variant(self) -> int:
+        return tvfgp_last_variant(self.h)
+
+    @property
+    def launch_count(self) -> int:
+        return tvfgp_launch_count(self.h)
+
+    def close(self) -> None:
+        if self.h:
+            tvfgp_destroy(self.h)
+            self.h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,171 @@
+/*
+ * tvfgp: the fast-gradient-projection (FGP) step on the dual of 3D isotropic
+ * TV denoising with a nonnegativity constraint, on one NVIDIA GB300
+ * (sm_103a).  C ABI: plain pointers and sizes, no C++ or framework types.
+ *
+ * The operation (page "TV solver: the FGP step on the GPU", section "What one
+ * step does"), for every voxel i of an nx x ny x nz volume:
+ *
+ *   L(r)(j) = sum_a r_a(j) - r_a(j - e_a)          (r_a(-1) = 0)
+ *   z(j)    = max(b(j) - lambda L(r)(j), 0)
+ *   g_a     = z(i) - z(i + e_a)                      (0 where i + e_a leaves the volume)
+ *   q       = r(i) + g / (12 lambda)
+ *   p'      = q / max(1, |q|)                        (|.| = Euclidean norm of the 3-vector)
+ *   r(i)    = p' + m (p' - p(i));   p(i) = p'
+ *
+ * The momentum weight of step k is m_k = (t_k - 1) / t_{k+1} with
+ * t_{k+1} = (1 + sqrt(1 + 4 t_k^2)) / 2, the FISTA schedule of the FGP method
+ * (the page names only m; "Variants" and "What made the difference" describe
+ * the one-kernel fused step with ping-pong r buffers that this library runs).
+ *
+ * Data layout (all fp32, caller-owned DEVICE memory):
+ *   scalar volume (b, z):  N = nx*ny*nz floats, voxel (x,y,z) at
+ *                          i = x + nx*(y + ny*z)  (x fastest);
+ *   dual field (p, r):     3*N floats, planar: component a (0 = x, 1 = y,
+ *                          2 = z) of voxel i at a*N + i.
+ * Arithmetic: fp32, each operation rounded to nearest in the order
+ *   L = ((r0(j)-r0(j-ex)) + (r1(j)-r1(j-ey))) + (r2(j)-r2(j-ez)),
+ *   z = max(b - lambda*L, 0), s = fl32(1/(12*lambda)) (evaluated in double),
+ *   q_a = r_a + g_a*s, |q| = sqrt((q0*q0 + q1*q1) + q2*q2), p'_a = q_a/max(1,|q|),
+ *   r_a = p'_a + m*(p'_a - p_a); no fused multiply-add; IEEE division and sqrt.
+ *
+ * Streams: every call that touches the GPU is asynchronous on `stream` (a
+ * cudaStream_t; NULL is the legacy default stream) and performs no host
+ * synchronisation, except tvfgp_check().  Calls on one handle must not run
+ * concurrently (the handle's scratch buffer is shared); different handles
+ * are independent.
+ *
+ * Errors: every function returns a status code (TVFGP_OK = 0).  Argument
+ * errors are detected on the host before anything is enqueued, so a failing
+ * call leaves the buffers untouched.
+ */
+#ifndef TVFGP_H
+#define TVFGP_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque handle: volume shape, the scratch dual buffer, the CUDA-graph cache
+ * and the device error flag. */
+typedef struct tvfgp_handle *tvfgp_t;
+
+/* Same type as cudaStream_t (struct CUstream_st *), spelt without CUDA
+ * headers.  NULL selects the legacy default stream. */
+typedef struct CUstream_st *tvfgp_stream_t;
+
+enum tvfgp_status {
+    TVFGP_OK = 0,
+    TVFGP_ERR_ARG = 1,         /* bad dimension, lambda <= 0 or not finite, nsteps < 0,
+                                  NULL or aliased pointer, unknown variant/handle */
+    TVFGP_ERR_ALIGN = 2,       /* a pointer is not 4-byte aligned */
+    TVFGP_ERR_CUDA = 3,        /* a CUDA call failed (launch, enqueue, graph) */
+    TVFGP_ERR_OOM = 4,         /* device or host allocation failed */
+    TVFGP_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up (see tvfgp_check) */
+    TVFGP_ERR_UNSUPPORTED = 6  /* the requested variant cannot run this shape/alignment */
+};
+
+/* Kernel variants.  All compute bitwise the same result. */
+enum tvfgp_variant {
+    TVFGP_VARIANT_AUTO = 0,      /* the measured default; falls back to SCALAR when the
+                                    shape or alignment rules out the vector paths */
+    TVFGP_VARIANT_FUSED = 1,     /* one kernel per step: float4 along x, the voxel's own p
+                                    and r loads first, z recomputed at the voxel and its
+                                    three upper neighbours, carried along z in registers.
+                                    Needs nx % 4 == 0 and 16-byte aligned pointers. */
+    TVFGP_VARIANT_SCALAR = 2,    /* one voxel per thread; any shape and alignment */
+    TVFGP_VARIANT_ZMARCH_TMA = 3 /* x-y tile marching along z, planes of b and r staged in
+                                    shared memory by TMA; same requirements as FUSED */
+};
+
+/* Create a handle for an nx x ny x nz volume on the current CUDA device.
+ * Allocates the scratch dual buffer (3*nx*ny*nz floats) and a device error
+ * word.  1 <= nx, ny, nz <= 65535 and nx*ny*nz <= 2^31 - 1, else
+ * TVFGP_ERR_ARG.  *out receives the handle (NULL on failure). */
+int tvfgp_create(int nx, int ny, int nz, tvfgp_t *out);
+
+/* As tvfgp_create, choosing the kernel variant (enum tvfgp_variant).  flags
+ * must be 0. */
+int tvfgp_create_ex(int nx, int ny, int nz, int variant, unsigned flags, tvfgp_t *out);
+
+/* Release the handle, its scratch buffer and cached graphs.  Waits for
+ * nothing: the caller must make sure no work of this handle is in flight
+ * (synchronise its streams first).  NULL is accepted. */
+int tvfgp_destroy(tvfgp_t h);
+
+/* Change the kernel variant used by later calls. */
+int tvfgp_set_variant(tvfgp_t h, int variant);
+
+/* enable != 0: tvfgp_run replays a CUDA graph of its nsteps launches (built
+ * on first use for each nsteps, re-parameterised when buffers, lambda or t0
+ * change); 0: launches eagerly.  Results are bitwise identical. */
+int tvfgp_set_graph(tvfgp_t h, int enable);
+
+/* Run nsteps FGP steps (sections "What one step does" and "Variants").
+ *   b       [N]    device, read only: the volume being denoised;
+ *   p       [3N]   device, read/write: the dual, updated in place;
+ *   r       [3N]   device, read/write: the momentum copy of the dual; on
+ *                  return it holds the final r (for odd nsteps the library
+ *                  copies it back from its scratch buffer);
+ *   lambda  > 0, finite: the TV weight;
+ *   nsteps  >= 0 (0 enqueues nothing);
+ *   t0      >= 1, finite: the momentum parameter t of the first step (1 for
+ *           a fresh start or a restart; pass the previous *t_final to
+ *           continue a run);
+ *   t_final NULL or receives t after the last step (host value, available
+ *           on return).
+ * b, p, r and the scratch buffer must not overlap.  Asynchronous on stream. */
+int tvfgp_run(tvfgp_t h, const float *b, float *p, float *r, float lambda, int nsteps,
+              double t0, tvfgp_stream_t stream, double *t_final);
+
+/* One FGP step with an explicit momentum weight m and explicit ping-pong
+ * buffers: reads b, p, r_src; writes p (in place) and r_dst.  r_src and
+ * r_dst must be distinct, non-overlapping [3N] device buffers. */
+int tvfgp_step(tvfgp_t h, const float *b, float *p, const float *r_src, float *r_dst,
+               float lambda, float m, tvfgp_stream_t stream);
+
+/* The primal of a dual field, z = max(b - lambda L(dual), 0) (section "What
+ * one step does", first line).  After an FGP run the denoised volume is the
+ * primal of p.  b [N], dual [3N] read only; z [N] written; z must not overlap
+ * b or dual. */
+int tvfgp_primal(tvfgp_t h, const float *b, const float *dual, float lambda, float *z,
+                 tvfgp_stream_t stream);
+
+/* Host only: the momentum weights m[0..nsteps-1] of a run started at t0 (in
+ * double; the kernels receive each rounded once to float) and t after the
+ * last step.  m may be NULL; t_final may be NULL. */
+int tvfgp_momentum(double t0, int nsteps, double *m, double *t_final);
+
+/* Synchronise `stream`, then read and clear the handle's device error word.
+ * Returns TVFGP_ERR_TIMEOUT if a bounded device-side wait of an earlier call
+ * gave up (its outputs are then invalid), TVFGP_ERR_CUDA if the stream
+ * reports an error, else TVFGP_OK. */
+int tvfgp_check(tvfgp_t h, tvfgp_stream_t stream);
+
+/* The variant the last enqueued step actually ran (after AUTO resolution and
+ * the SCALAR fallback), or -1 before the first step. */
+int tvfgp_last_variant(tvfgp_t h);
+
+/* Kernels enqueued by this handle since creation (each step, primal and
+ * bounded-wait probe counts one; graph replays count their nodes). */
+long long tvfgp_launch_count(tvfgp_t h);
+
+/* Test hook for the bounded-wait path: launches one block that waits on a
+ * shared-memory barrier nobody arrives at, gives up after about `spins`
+ * polls, sets the handle's error word and returns.  tvfgp_check() then
+ * reports TVFGP_ERR_TIMEOUT.  1 <= spins <= 2^24. */
+int tvfgp_debug_timeout_probe(tvfgp_t h, int spins, tvfgp_stream_t stream);
+
+/* Static description of a status code. */
+const char *tvfgp_strerror(int code);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int tvfgp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TVFGP_H */

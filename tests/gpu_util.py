@@ -1,0 +1,70 @@
+"""Helpers shared by the GPU tests: run a workload through the CUDA library
+and through the CPU oracle on the same seeded inputs."""
+import numpy as np
+
+import oracle
+from fgp_dual_stencil_gb300 import synth
+
+# Parity bar: max abs diff <= 1e-5 on p and r, <= 1e-5 * max|b| on z.
+TOL_DUAL = 1e-5
+TOL_Z_REL = 1e-5
+
+
+def dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    return t.detach().cpu().numpy()
+
+
+def run_workload_gpu(w, variant="auto", graph=False, p0=None, r0=None):
+    """The workload's outer loop (fresh b per outer, t0 per outer, p and r
+    carried over) on the GPU.  Returns numpy (b_last, p, r, z_of_p, z_of_r)."""
+    import torch
+    from fgp_dual_stencil_gb300 import tvfgp as T
+    base = synth.phantom(w)
+    shape = (3, w.nz, w.ny, w.nx)
+    p = dev(p0) if p0 is not None else torch.zeros(shape, device="cuda")
+    r = dev(r0) if r0 is not None else torch.zeros(shape, device="cuda")
+    with T.Tvfgp(w.nx, w.ny, w.nz, variant, graph) as h:
+        b = None
+        for k in range(w.outers):
+            b_np = synth.make_b(w, k, base)
+            b = dev(b_np)
+            h.run(b, p, r, w.lam, w.steps, w.t0)
+        zp = h.primal(b, p, w.lam)
+        zr = h.primal(b, r, w.lam)
+        assert h.check() == T.TVFGP_OK
+        launched = h.launch_count
+    torch.cuda.synchronize()
+    return b_np, host(p), host(r), host(zp), host(zr), launched
+
+
+def run_workload_oracle(w, p0=None, r0=None):
+    base = synth.phantom(w)
+    shape = (3, w.nz, w.ny, w.nx)
+    p = np.zeros(shape, np.float32) if p0 is None else p0.copy()
+    r = np.zeros(shape, np.float32) if r0 is None else r0.copy()
+    b = None
+    for k in range(w.outers):
+        b = synth.make_b(w, k, base)
+        oracle.fgp_run(b, p, r, w.lam, w.steps, w.t0)
+    return b, p, r, oracle.primal(b, p, w.lam), oracle.primal(b, r, w.lam)
+
+
+def max_diff(a, b):
+    return float(np.abs(a.astype(np.float64) - b.astype(np.float64)).max()) if a.size else 0.0
+
+
+def assert_parity(gpu, ref, bmax, exact=False, what=""):
+    """gpu, ref: (p, r, z_p, z_r).  Checks the tolerance bar, and equality of
+    values when exact is set."""
+    names = ("p", "r", "z(p)", "z(r)")
+    tols = (TOL_DUAL, TOL_DUAL, TOL_Z_REL * bmax, TOL_Z_REL * bmax)
+    for name, g, o, tol in zip(names, gpu, ref, tols):
+        d = max_diff(g, o)
+        assert d <= tol, "%s %s: max abs diff %.3g > %.3g" % (what, name, d, tol)
+        if exact:
+            assert d == 0.0, "%s %s: not equal to the oracle (max abs diff %.3g)" % (what, name, d)
