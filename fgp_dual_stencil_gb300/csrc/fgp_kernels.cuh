@@ -137,8 +137,11 @@ __device__ __forceinline__ float4 zquad(float4 B, float4 R0, float4 R1, float4 R
 // The voxel's own p loads are issued first in every iteration, then the
 // next plane's own b and r, then row y+1: no barrier exists in this kernel.
 // Requirements: nx % 4 == 0 and 16-byte aligned b, p, rs, rd.
+#ifndef TVFGP_FUSED_MINB
+#define TVFGP_FUSED_MINB 2
+#endif
 template <int BY, int ZC>
-__global__ void __launch_bounds__(32 * BY, 2) fgp_step_fused4(const StepArgs a)
+__global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(const StepArgs a)
 {
     const int lane = threadIdx.x;
     const int x0 = (blockIdx.x * 32 + lane) * 4;

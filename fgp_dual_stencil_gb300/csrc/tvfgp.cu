@@ -26,9 +26,15 @@ namespace {
 constexpr int kMagic = 0x74766670;   // "tvfp"
 constexpr int kVersion = 10000;      // 1.0.0
 
-// launch shapes of the vector kernels
-constexpr int kFusedBY = 8;
-constexpr int kFusedZC = 8;
+// launch shapes of the vector kernels (overridable at build time)
+#ifndef TVFGP_FUSED_BY
+#define TVFGP_FUSED_BY 8
+#endif
+#ifndef TVFGP_FUSED_ZC
+#define TVFGP_FUSED_ZC 8
+#endif
+constexpr int kFusedBY = TVFGP_FUSED_BY;
+constexpr int kFusedZC = TVFGP_FUSED_ZC;
 constexpr int kPrimalBY = 8;
 
 // The default vector variant chosen by AUTO.
@@ -168,22 +174,22 @@ struct KArgs {
     void *ptrs[1];
 };
 
-void fill_kargs(const tvfgp_handle *h, int variant, const StepArgs &a, KArgs &k)
+bool fill_kargs(const tvfgp_handle *h, int variant, const StepArgs &a, KArgs &k)
 {
     k.a = a;
     if (variant == TVFGP_VARIANT_ZMARCH_TMA) {
-        zmarch_fill(h->zplan, a, h->d_err, k.za);
         k.ptrs[0] = &k.za;
-    } else {
-        k.ptrs[0] = &k.a;
+        return zmarch_fill(h->zplan, a, h->d_err, k.za);
     }
+    k.ptrs[0] = &k.a;
+    return true;
 }
 
 int launch_step(tvfgp_handle *h, int variant, const StepArgs &a, cudaStream_t st)
 {
     const LaunchCfg c = step_cfg(h, variant);
     KArgs k;
-    fill_kargs(h, variant, a, k);
+    if (!fill_kargs(h, variant, a, k)) return TVFGP_ERR_CUDA;
     cudaError_t e = cudaLaunchKernel(c.func, c.grid, c.block, k.ptrs, c.smem, st);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -202,13 +208,13 @@ void destroy_graph(GraphEntry &g)
 }
 
 // Kernel-node parameters of step k of a run.
-void step_node_params(tvfgp_handle *h, int variant, const float *b, float *p, float *r, float lam,
+bool step_node_params(tvfgp_handle *h, int variant, const float *b, float *p, float *r, float lam,
                       const std::vector<double> &m, int k, KArgs &ka, cudaKernelNodeParams &kp)
 {
     const bool even = (k % 2) == 0;
     const StepArgs a = make_args(h, b, p, even ? r : h->scratch, even ? h->scratch : r, lam,
                                  static_cast<float>(m[k]));
-    fill_kargs(h, variant, a, ka);
+    const bool ok = fill_kargs(h, variant, a, ka);
     const LaunchCfg c = step_cfg(h, variant);
     kp.func = const_cast<void *>(c.func);
     kp.gridDim = c.grid;
@@ -216,6 +222,7 @@ void step_node_params(tvfgp_handle *h, int variant, const float *b, float *p, fl
     kp.sharedMemBytes = static_cast<unsigned>(c.smem);
     kp.kernelParams = ka.ptrs;
     kp.extra = nullptr;
+    return ok;
 }
 
 int build_graph(tvfgp_handle *h, GraphEntry &g, int variant, const float *b, float *p, float *r,
@@ -229,7 +236,10 @@ int build_graph(tvfgp_handle *h, GraphEntry &g, int variant, const float *b, flo
     for (int k = 0; k < nsteps; ++k) {
         KArgs ka;
         cudaKernelNodeParams kp;
-        step_node_params(h, variant, b, p, r, lam, m, k, ka, kp);
+        if (!step_node_params(h, variant, b, p, r, lam, m, k, ka, kp)) {
+            e = cudaErrorInvalidValue;
+            break;
+        }
         e = cudaGraphAddKernelNode(&g.knodes[k], g.graph, prev ? &prev : nullptr, prev ? 1 : 0, &kp);
         if (e != cudaSuccess) break;
         prev = g.knodes[k];
@@ -261,7 +271,10 @@ int update_graph(tvfgp_handle *h, GraphEntry &g, const float *b, float *p, float
     for (int k = 0; k < g.nsteps && e == cudaSuccess; ++k) {
         KArgs ka;
         cudaKernelNodeParams kp;
-        step_node_params(h, g.variant, b, p, r, lam, m, k, ka, kp);
+        if (!step_node_params(h, g.variant, b, p, r, lam, m, k, ka, kp)) {
+            e = cudaErrorInvalidValue;
+            break;
+        }
         e = cudaGraphExecKernelNodeSetParams(g.exec, g.knodes[k], &kp);
     }
     if (e == cudaSuccess && g.cnode)
@@ -349,8 +362,7 @@ int tvfgp_create_ex(int nx, int ny, int nz, int variant, unsigned flags, tvfgp_t
     if (static_cast<long long>(nx) * ny * (static_cast<long long>(nz) + 1) > INT_MAX) return TVFGP_ERR_ARG;
     if (variant < TVFGP_VARIANT_AUTO || variant > TVFGP_VARIANT_ZMARCH_TMA || flags != 0)
         return TVFGP_ERR_ARG;
-    if (variant == TVFGP_VARIANT_ZMARCH_TMA && !zmarch_supported(nx, ny, nz))
-        return TVFGP_ERR_UNSUPPORTED;
+    if (variant == TVFGP_VARIANT_ZMARCH_TMA && !zmarch_available()) return TVFGP_ERR_UNSUPPORTED;
     tvfgp_handle *h = new (std::nothrow) tvfgp_handle();
     if (h == nullptr) return TVFGP_ERR_OOM;
     h->magic = kMagic;
@@ -405,8 +417,7 @@ int tvfgp_set_variant(tvfgp_t h, int variant)
 {
     if (!valid(h) || variant < TVFGP_VARIANT_AUTO || variant > TVFGP_VARIANT_ZMARCH_TMA)
         return TVFGP_ERR_ARG;
-    if (variant == TVFGP_VARIANT_ZMARCH_TMA && !zmarch_supported(h->nx, h->ny, h->nz))
-        return TVFGP_ERR_UNSUPPORTED;
+    if (variant == TVFGP_VARIANT_ZMARCH_TMA && !zmarch_available()) return TVFGP_ERR_UNSUPPORTED;
     h->variant = variant;
     return TVFGP_OK;
 }

@@ -1,35 +1,399 @@
-// ZMARCH_TMA variant: x-y tile marching along z with TMA-staged planes.
-// (Interface only; the kernel is not built yet, so the variant reports
-// itself unsupported.)
+// ZMARCH_TMA variant of the FGP step: an x-y tile marching along z, with the
+// planes of b and r staged in shared memory by TMA (page "TV solver: the FGP
+// step on the GPU", section "Variants", fourth row: x-y tiles marching along
+// z, two planes of r and z on chip; rebuilt here around the Blackwell tensor
+// memory accelerator instead of plain loads and barriers).
+//
+// A CTA owns the columns x0..x0+63 and computes z for the 16 rows
+// y0..y0+15 of each plane; it updates the dual on the first 15 rows (the
+// 16th row's z is the y+1 neighbour of the 15th).  It walks ZC planes in z.
+// For each plane q a TMA load brings, into one slot of a 4-deep ring:
+//   b  at x0..x0+67,   y0..y0+15          (z(x0+64) is the x+1 neighbour)
+//   r0 at x0-4..x0+67, y0..y0+15          (r0(x-1) for L)
+//   r1 at x0..x0+67,   y0-1..y0+15        (r1(y-1) for L)
+//   r2 at x0..x0+67,   y0..y0+15
+// Coordinates outside the volume read as zero, which is the r_a(-1) = 0
+// boundary of L.  A thread owns 4 consecutive x voxels of one row: it keeps
+// its own r and z of the current and next plane in registers, so only the
+// z of the x+1 and y+1 neighbours goes through shared memory (a 3-slot ring
+// of z planes: one barrier per plane suffices).  The voxel's own p is loaded
+// from global memory at the top of each plane, before any wait.
+//
+// Every wait on a TMA barrier is bounded; on timeout the kernel sets the
+// caller's error word, drains its outstanding copies (again bounded) and
+// returns, so the context stays usable (tvfgp_check reports it).
 #pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "fgp_kernels.cuh"
 
 namespace tvfgp {
 
+#ifndef TVFGP_ZM_TX
+#define TVFGP_ZM_TX 64
+#endif
+#ifndef TVFGP_ZM_ROWS
+#define TVFGP_ZM_ROWS 16
+#endif
+#ifndef TVFGP_ZM_MINB
+#define TVFGP_ZM_MINB 2
+#endif
+constexpr int ZM_TX = TVFGP_ZM_TX;        // tile width (voxels)
+constexpr int ZM_ROWS = TVFGP_ZM_ROWS;    // rows whose z is computed per plane
+constexpr int ZM_TY = ZM_ROWS - 1;        // rows whose dual is updated
+constexpr int ZM_QX = ZM_TX / 4;          // quads per row
+constexpr int ZM_THREADS = ZM_QX * ZM_ROWS;
+#ifndef TVFGP_ZM_STAGES
+#define TVFGP_ZM_STAGES 4
+#endif
+#ifndef TVFGP_ZM_ZC
+#define TVFGP_ZM_ZC 32
+#endif
+constexpr int ZM_STAGES = TVFGP_ZM_STAGES;   // TMA ring depth (planes in flight)
+constexpr int ZM_ZC = TVFGP_ZM_ZC;           // planes per CTA
+constexpr int ZM_MAX_POLLS = 1 << 22;     // bound of every barrier wait
+
+constexpr int ZM_BW = ZM_TX + 4;          // width of the b, r1, r2 boxes
+constexpr int ZM_W0 = ZM_TX + 8;          // width of the r0 box
+constexpr int ZM_HB = ZM_ROWS;            // height of the b, r0, r2 boxes
+constexpr int ZM_H1 = ZM_ROWS + 1;        // height of the r1 box
+constexpr int ZM_ZP = ZM_TX + 4;          // row pitch of a z plane
+
+constexpr int zm_round128(int v) { return (v + 127) / 128 * 128; }
+constexpr int ZM_BYTES_B = ZM_BW * ZM_HB * 4;
+constexpr int ZM_BYTES_R0 = ZM_W0 * ZM_HB * 4;
+constexpr int ZM_BYTES_R1 = ZM_BW * ZM_H1 * 4;
+constexpr int ZM_BYTES_R2 = ZM_BW * ZM_HB * 4;
+constexpr int ZM_OFF_B = 0;
+constexpr int ZM_OFF_R0 = zm_round128(ZM_OFF_B + ZM_BYTES_B);
+constexpr int ZM_OFF_R1 = zm_round128(ZM_OFF_R0 + ZM_BYTES_R0);
+constexpr int ZM_OFF_R2 = zm_round128(ZM_OFF_R1 + ZM_BYTES_R1);
+constexpr int ZM_STAGE_STRIDE = zm_round128(ZM_OFF_R2 + ZM_BYTES_R2);
+constexpr int ZM_STAGE_TX = ZM_BYTES_B + ZM_BYTES_R0 + ZM_BYTES_R1 + ZM_BYTES_R2;
+constexpr int ZM_OFF_PREV = ZM_STAGES * ZM_STAGE_STRIDE;               // r2 of plane z0-1
+constexpr int ZM_OFF_Z = zm_round128(ZM_OFF_PREV + ZM_BYTES_R2);       // 3 z planes
+constexpr int ZM_BYTES_Z = 3 * ZM_ROWS * ZM_ZP * 4;
+constexpr int ZM_OFF_BAR = zm_round128(ZM_OFF_Z + ZM_BYTES_Z);         // STAGES+1 barriers
+constexpr int ZM_OFF_FLAG = ZM_OFF_BAR + 8 * (ZM_STAGES + 1);
+constexpr int ZM_SMEM = ZM_OFF_FLAG + 16 + 128;                        // + base alignment
+
+static_assert(ZM_TX % 4 == 0 && ZM_W0 <= 256 && ZM_H1 <= 256, "TMA box limits");
+static_assert(ZM_SMEM * TVFGP_ZM_MINB <= 227 * 1024, "CTAs per SM must fit in shared memory");
+
 struct ZmarchPlan {
-    int ok;
+    dim3 grid;
 };
 
 struct ZmarchArgs {
+    CUtensorMap tb, t0, t1, t2;   // b, r0, r1, r2 of the r read by this step
     StepArgs a;
     int *err;
 };
 
-inline int zmarch_plan(int, int, int, ZmarchPlan *plan)
+// ---------------------------------------------------------------------------
+// device helpers (TMA, mbarrier)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
 {
-    plan->ok = 0;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_tma(uint64_t *bar, uint32_t parity)
+{
+    for (int k = 0; k < ZM_MAX_POLLS; ++k)
+        if (mbar_try(bar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ float4 lds4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+
+// z of the quad (row, 4*qx) of a staged plane; r2lo is r2 of the plane below.
+__device__ __forceinline__ void zm_quad(const unsigned char *st, int row, int qx, float4 r2lo,
+                                        float lam, float4 &R0, float4 &R1, float4 &R2, float4 &Z)
+{
+    const float *B = reinterpret_cast<const float *>(st + ZM_OFF_B);
+    const float *S0 = reinterpret_cast<const float *>(st + ZM_OFF_R0);
+    const float *S1 = reinterpret_cast<const float *>(st + ZM_OFF_R1);
+    const float *S2 = reinterpret_cast<const float *>(st + ZM_OFF_R2);
+    const int c = 4 * qx;
+    const float4 Bq = lds4(B + row * ZM_BW + c);
+    R0 = lds4(S0 + row * ZM_W0 + 4 + c);
+    const float left = S0[row * ZM_W0 + 3 + c];
+    R1 = lds4(S1 + (row + 1) * ZM_BW + c);
+    const float4 R1lo = lds4(S1 + row * ZM_BW + c);
+    R2 = lds4(S2 + row * ZM_BW + c);
+    Z = zquad(Bq, R0, R1, R2, left, R1lo, r2lo, lam);
+}
+
+// z at column x0+64 of a row (the x+1 neighbour of the tile's last quad).
+__device__ __forceinline__ float zm_halo(const unsigned char *st, int row, float r2lo, float lam,
+                                         float &r2here)
+{
+    const float *B = reinterpret_cast<const float *>(st + ZM_OFF_B);
+    const float *S0 = reinterpret_cast<const float *>(st + ZM_OFF_R0);
+    const float *S1 = reinterpret_cast<const float *>(st + ZM_OFF_R1);
+    const float *S2 = reinterpret_cast<const float *>(st + ZM_OFF_R2);
+    r2here = S2[row * ZM_BW + ZM_TX];
+    return zval(B[row * ZM_BW + ZM_TX], lam,
+                __fsub_rn(S0[row * ZM_W0 + 4 + ZM_TX], S0[row * ZM_W0 + 3 + ZM_TX]),
+                __fsub_rn(S1[(row + 1) * ZM_BW + ZM_TX], S1[row * ZM_BW + ZM_TX]),
+                __fsub_rn(r2here, r2lo));
+}
+
+__global__ void __launch_bounds__(ZM_THREADS, TVFGP_ZM_MINB) fgp_step_zmarch_tma(const __grid_constant__ ZmarchArgs za)
+{
+    extern __shared__ unsigned char zm_raw[];
+    unsigned char *smem = zm_raw + ((128 - (smem_addr(zm_raw) & 127)) & 127);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + ZM_OFF_BAR);   // [STAGES] + prev
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + ZM_OFF_FLAG);
+    float *zpl = reinterpret_cast<float *>(smem + ZM_OFF_Z);
+
+    const StepArgs &a = za.a;
+    const int nx = a.nx, ny = a.ny, nz = a.nz;
+    const int tid = threadIdx.x;
+    const int qx = tid % ZM_QX, row = tid / ZM_QX;
+    const int x0 = blockIdx.x * ZM_TX, y0 = blockIdx.y * ZM_TY;
+    const int z0 = blockIdx.z * ZM_ZC;
+    const int ze = min(z0 + ZM_ZC, nz);            // planes updated: [z0, ze)
+    const int qmax = min(ze, nz - 1);              // last plane whose z is needed
+    const int x = x0 + 4 * qx, y = y0 + row;
+    const bool upd = (row < ZM_TY) && (x < nx) && (y < ny);
+    const bool hasY = (y + 1 < ny);
+    const float lam = a.lam, s = a.s, m = a.m;
+
+    if (tid == 0) {
+        for (int k = 0; k <= ZM_STAGES; ++k) mbar_init(&bars[k], 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+
+    auto issue = [&](int q) {                       // thread 0 only
+        unsigned char *st = smem + ((q - z0) % ZM_STAGES) * ZM_STAGE_STRIDE;
+        uint64_t *bar = &bars[(q - z0) % ZM_STAGES];
+        mbar_expect_tx(bar, ZM_STAGE_TX);
+        tma_load_3d(st + ZM_OFF_B, &za.tb, x0, y0, q, bar);
+        tma_load_3d(st + ZM_OFF_R0, &za.t0, x0 - 4, y0, q, bar);
+        tma_load_3d(st + ZM_OFF_R1, &za.t1, x0, y0 - 1, q, bar);
+        tma_load_3d(st + ZM_OFF_R2, &za.t2, x0, y0, q, bar);
+    };
+    if (tid == 0) {
+        if (z0 > 0) {
+            mbar_expect_tx(&bars[ZM_STAGES], ZM_BYTES_R2);
+            tma_load_3d(smem + ZM_OFF_PREV, &za.t2, x0, y0, z0 - 1, &bars[ZM_STAGES]);
+        }
+        for (int q = z0; q <= qmax && q < z0 + ZM_STAGES; ++q) issue(q);
+    }
+    int next_issue = z0 + ZM_STAGES;               // next plane to load (thread 0)
+
+    auto stage_of = [&](int q) { return smem + ((q - z0) % ZM_STAGES) * ZM_STAGE_STRIDE; };
+    auto parity_of = [&](int q) { return static_cast<uint32_t>(((q - z0) / ZM_STAGES) & 1); };
+    auto zrow = [&](int q, int rr) { return zpl + ((q % 3) * ZM_ROWS + rr) * ZM_ZP; };
+
+    // prologue: z of plane z0, own r at z0
+    float4 Rc0, Rc1, Rc2, Zc;
+    float r2halo = 0.0f;                            // r2 at column x0+64 of the current plane
+    bool ok = true;
+    {
+        float4 r2lo = f4zero();
+        float r2lo_h = 0.0f;
+        if (z0 > 0) {
+            ok = mbar_wait_tma(&bars[ZM_STAGES], 0);
+            const float *P2 = reinterpret_cast<const float *>(smem + ZM_OFF_PREV);
+            r2lo = lds4(P2 + row * ZM_BW + 4 * qx);
+            r2lo_h = P2[row * ZM_BW + ZM_TX];
+        }
+        ok = ok && mbar_wait_tma(&bars[0], 0);
+        if (ok) {
+            const unsigned char *st = stage_of(z0);
+            zm_quad(st, row, qx, r2lo, lam, Rc0, Rc1, Rc2, Zc);
+            float *zr = zrow(z0, row);
+            *reinterpret_cast<float4 *>(zr + 4 * qx) = Zc;
+            if (qx == ZM_QX - 1) zr[ZM_TX] = zm_halo(st, row, r2lo_h, lam, r2halo);
+        } else {
+            *abort_flag = 1;
+        }
+    }
+    __syncthreads();
+    if (tid == 0 && *abort_flag == 0 && next_issue <= qmax) issue(next_issue++);   // z0's slot is free
+
+    float *p0 = a.p, *p1 = a.p + a.N, *p2 = a.p + 2 * a.N;
+    float *o0 = a.rd, *o1 = a.rd + a.N, *o2 = a.rd + 2 * a.N;
+
+    int zlast = z0 - 1;                            // planes <= zlast+1 were waited for
+    for (int z = z0; z < ze && *abort_flag == 0; ++z) {
+        zlast = z;
+        const long long i = x + (long long)nx * (y + (long long)ny * z);
+        // (1) the voxel's own p, before any wait
+        float4 P0 = f4zero(), P1 = f4zero(), P2 = f4zero();
+        if (upd) {
+            P0 = ld_once4(p0 + i);
+            P1 = ld_once4(p1 + i);
+            P2 = ld_once4(p2 + i);
+        }
+        // (2) z of plane z+1 from its staged planes; own r of plane z is r2lo
+        const bool hasZ = (z + 1 < nz);
+        float4 Rn0 = f4zero(), Rn1 = f4zero(), Rn2 = f4zero(), Zn = f4zero();
+        float r2halo_n = 0.0f;
+        if (hasZ) {
+            if (mbar_wait_tma(&bars[(z + 1 - z0) % ZM_STAGES], parity_of(z + 1))) {
+                const unsigned char *st = stage_of(z + 1);
+                zm_quad(st, row, qx, Rc2, lam, Rn0, Rn1, Rn2, Zn);
+                float *zr = zrow(z + 1, row);
+                *reinterpret_cast<float4 *>(zr + 4 * qx) = Zn;
+                if (qx == ZM_QX - 1) zr[ZM_TX] = zm_halo(st, row, r2halo, lam, r2halo_n);
+            } else {
+                *abort_flag = 1;
+            }
+        }
+        __syncthreads();
+        if (*abort_flag) break;
+        // plane z+1 is consumed: its slot takes the next plane
+        if (tid == 0 && hasZ && next_issue <= qmax) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(next_issue++);
+        }
+        // (3) dual update of plane z
+        if (upd) {
+            const float *zr = zrow(z, row);
+            const float zx = zr[4 * qx + 4];
+            const float4 ZY = hasY ? lds4(zrow(z, row + 1) + 4 * qx) : f4zero();
+            const float gx3 = (x + 3 < nx - 1) ? __fsub_rn(Zc.w, zx) : 0.0f;
+            float4 G1 = f4zero(), G2 = f4zero();
+            if (hasY) {
+                G1.x = __fsub_rn(Zc.x, ZY.x); G1.y = __fsub_rn(Zc.y, ZY.y);
+                G1.z = __fsub_rn(Zc.z, ZY.z); G1.w = __fsub_rn(Zc.w, ZY.w);
+            }
+            if (hasZ) {
+                G2.x = __fsub_rn(Zc.x, Zn.x); G2.y = __fsub_rn(Zc.y, Zn.y);
+                G2.z = __fsub_rn(Zc.z, Zn.z); G2.w = __fsub_rn(Zc.w, Zn.w);
+            }
+            float4 N0 = Rc0, N1 = Rc1, N2 = Rc2;
+            dual_update(N0.x, N1.x, N2.x, __fsub_rn(Zc.x, Zc.y), G1.x, G2.x, P0.x, P1.x, P2.x, s, m);
+            dual_update(N0.y, N1.y, N2.y, __fsub_rn(Zc.y, Zc.z), G1.y, G2.y, P0.y, P1.y, P2.y, s, m);
+            dual_update(N0.z, N1.z, N2.z, __fsub_rn(Zc.z, Zc.w), G1.z, G2.z, P0.z, P1.z, P2.z, s, m);
+            dual_update(N0.w, N1.w, N2.w, gx3, G1.w, G2.w, P0.w, P1.w, P2.w, s, m);
+            st4(p0 + i, P0);
+            st4(p1 + i, P1);
+            st4(p2 + i, P2);
+            st4(o0 + i, N0);
+            st4(o1 + i, N1);
+            st4(o2 + i, N2);
+        }
+        Rc0 = Rn0;
+        Rc1 = Rn1;
+        Rc2 = Rn2;
+        Zc = Zn;
+        r2halo = r2halo_n;
+    }
+
+    if (*abort_flag) {
+        // A wait gave up.  Record it, then drain (bounded) every copy this
+        // CTA issued that is still in flight: plane zlast+1 (whose wait
+        // failed, or z0 when the prologue failed) and all later ones.
+        __syncthreads();
+        if (tid == 0) {
+            atomicExch(za.err, kErrTimeout);
+            if (z0 > 0 && zlast < z0) mbar_wait_tma(&bars[ZM_STAGES], 0);
+            for (int q = zlast + 1; q < next_issue && q <= qmax; ++q)
+                mbar_wait_tma(&bars[(q - z0) % ZM_STAGES], parity_of(q));
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+inline PFN_cuTensorMapEncodeTiled_v12000 zm_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+inline bool zmarch_supported(int nx, int, int) { return nx % 4 == 0; }
+
+// The variant needs the driver's tensor-map encoder.
+inline bool zmarch_available() { return zm_encoder() != nullptr; }
+
+inline int zmarch_plan(int nx, int ny, int nz, ZmarchPlan *plan)
+{
+    plan->grid = dim3((nx + ZM_TX - 1) / ZM_TX, (ny + ZM_TY - 1) / ZM_TY, (nz + ZM_ZC - 1) / ZM_ZC);
+    if (!zmarch_supported(nx, ny, nz)) return 0;
+    if (zm_encoder() == nullptr) return 3;
+    if (cudaFuncSetAttribute(reinterpret_cast<const void *>(&fgp_step_zmarch_tma),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, ZM_SMEM) != cudaSuccess) {
+        cudaGetLastError();
+        return 3;
+    }
     return 0;
 }
-inline bool zmarch_supported(int, int, int) { return false; }
-inline const void *zmarch_kernel() { return nullptr; }
-inline int zmarch_threads() { return 0; }
-inline dim3 zmarch_grid(const ZmarchPlan &) { return dim3(1, 1, 1); }
-inline size_t zmarch_smem_bytes() { return 0; }
-inline void zmarch_fill(const ZmarchPlan &, const StepArgs &a, int *err, ZmarchArgs &za)
+
+inline const void *zmarch_kernel() { return reinterpret_cast<const void *>(&fgp_step_zmarch_tma); }
+inline int zmarch_threads() { return ZM_THREADS; }
+inline dim3 zmarch_grid(const ZmarchPlan &p) { return p.grid; }
+inline size_t zmarch_smem_bytes() { return ZM_SMEM; }
+
+inline bool zm_encode(CUtensorMap *map, const float *base, int nx, int ny, int nz, int bw, int bh)
+{
+    const cuuint64_t dims[3] = {(cuuint64_t)nx, (cuuint64_t)ny, (cuuint64_t)nz};
+    const cuuint64_t strides[2] = {(cuuint64_t)nx * 4, (cuuint64_t)nx * ny * 4};
+    const cuuint32_t box[3] = {(cuuint32_t)bw, (cuuint32_t)bh, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return zm_encoder()(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Fill the kernel arguments of one step: tensor maps of b and of the three
+// components of r_src.  Returns false if an encoding fails.
+inline bool zmarch_fill(const ZmarchPlan &, const StepArgs &a, int *err, ZmarchArgs &za)
 {
     za.a = a;
     za.err = err;
+    const float *r = a.rs;
+    return zm_encode(&za.tb, a.b, a.nx, a.ny, a.nz, ZM_BW, ZM_HB) &&
+           zm_encode(&za.t0, r, a.nx, a.ny, a.nz, ZM_W0, ZM_HB) &&
+           zm_encode(&za.t1, r + a.N, a.nx, a.ny, a.nz, ZM_BW, ZM_H1) &&
+           zm_encode(&za.t2, r + 2 * a.N, a.nx, a.ny, a.nz, ZM_BW, ZM_HB);
 }
 
 }  // namespace tvfgp

@@ -77,7 +77,9 @@ enum tvfgp_variant {
                                     Needs nx % 4 == 0 and 16-byte aligned pointers. */
     TVFGP_VARIANT_SCALAR = 2,    /* one voxel per thread; any shape and alignment */
     TVFGP_VARIANT_ZMARCH_TMA = 3 /* x-y tile marching along z, planes of b and r staged in
-                                    shared memory by TMA; same requirements as FUSED */
+                                    shared memory by TMA; same requirements as FUSED (else
+                                    the call falls back to SCALAR); TVFGP_ERR_UNSUPPORTED at
+                                    create/set time if the driver lacks the TMA encoder */
 };
 
 /* Create a handle for an nx x ny x nz volume on the current CUDA device.

@@ -21,7 +21,7 @@ def T():
     return tvfgp
 
 
-VEC_VARIANTS = ["fused", "scalar"]
+VEC_VARIANTS = ["fused", "zmarch", "scalar"]
 
 
 # ---------------------------------------------------------------------------
@@ -85,7 +85,10 @@ def test_odd_shapes_warm_start(T, shape, variant):
             zp = h.primal(bd, p, lam)
             assert h.check() == 0
             if nsteps:
-                want = T.TVFGP_VARIANT_SCALAR if (variant == "scalar" or nx % 4) else T.TVFGP_VARIANT_FUSED
+                if variant == "scalar" or nx % 4:
+                    want = T.TVFGP_VARIANT_SCALAR
+                else:
+                    want = T.VARIANTS[variant]
                 assert h.last_variant == want
         po, ro = p0.copy(), r0.copy()
         tfo = oracle.fgp_run(b, po, ro, lam, nsteps, 1.0)
@@ -165,8 +168,9 @@ def test_variants_agree_bitwise(T):
     for v in VEC_VARIANTS:
         _, p, r, zp, _, _ = run_workload_gpu(w, v)
         res.append((p, r, zp))
-    for a, b in zip(res[0], res[1]):
-        assert np.array_equal(a, b)
+    for other in res[1:]:
+        for a, b in zip(res[0], other):
+            assert np.array_equal(a, b)
 
 
 def test_misaligned_pointers_fall_back_to_scalar(T):
