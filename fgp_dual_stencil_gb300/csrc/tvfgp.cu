@@ -28,7 +28,7 @@ constexpr int kVersion = 10000;      // 1.0.0
 
 // launch shapes of the vector kernels (overridable at build time)
 #ifndef TVFGP_FUSED_BY
-#define TVFGP_FUSED_BY 8
+#define TVFGP_FUSED_BY 4
 #endif
 #ifndef TVFGP_FUSED_ZC
 #define TVFGP_FUSED_ZC 8
@@ -38,7 +38,7 @@ constexpr int kFusedZC = TVFGP_FUSED_ZC;
 constexpr int kPrimalBY = 8;
 
 // The default vector variant chosen by AUTO.
-constexpr int kAutoVariant = TVFGP_VARIANT_FUSED;
+constexpr int kAutoVariant = TVFGP_VARIANT_ZMARCH_TMA;
 
 struct LaunchCfg {
     const void *func;

@@ -46,13 +46,9 @@ constexpr int ZM_TY = ZM_ROWS - 1;        // rows whose dual is updated
 constexpr int ZM_QX = ZM_TX / 4;          // quads per row
 constexpr int ZM_THREADS = ZM_QX * ZM_ROWS;
 #ifndef TVFGP_ZM_STAGES
-#define TVFGP_ZM_STAGES 4
-#endif
-#ifndef TVFGP_ZM_ZC
-#define TVFGP_ZM_ZC 32
+#define TVFGP_ZM_STAGES 2
 #endif
 constexpr int ZM_STAGES = TVFGP_ZM_STAGES;   // TMA ring depth (planes in flight)
-constexpr int ZM_ZC = TVFGP_ZM_ZC;           // planes per CTA
 constexpr int ZM_MAX_POLLS = 1 << 22;     // bound of every barrier wait
 
 constexpr int ZM_BW = ZM_TX + 4;          // width of the b, r1, r2 boxes
@@ -84,12 +80,14 @@ static_assert(ZM_SMEM * TVFGP_ZM_MINB <= 227 * 1024, "CTAs per SM must fit in sh
 
 struct ZmarchPlan {
     dim3 grid;
+    int zc;                       // planes per CTA
 };
 
 struct ZmarchArgs {
     CUtensorMap tb, t0, t1, t2;   // b, r0, r1, r2 of the r read by this step
     StepArgs a;
     int *err;
+    int zc;                       // planes per CTA (grid.z = ceil(nz / zc))
 };
 
 // ---------------------------------------------------------------------------
@@ -181,8 +179,8 @@ __global__ void __launch_bounds__(ZM_THREADS, TVFGP_ZM_MINB) fgp_step_zmarch_tma
     const int tid = threadIdx.x;
     const int qx = tid % ZM_QX, row = tid / ZM_QX;
     const int x0 = blockIdx.x * ZM_TX, y0 = blockIdx.y * ZM_TY;
-    const int z0 = blockIdx.z * ZM_ZC;
-    const int ze = min(z0 + ZM_ZC, nz);            // planes updated: [z0, ze)
+    const int z0 = blockIdx.z * za.zc;
+    const int ze = min(z0 + za.zc, nz);            // planes updated: [z0, ze)
     const int qmax = min(ze, nz - 1);              // last plane whose z is needed
     const int x = x0 + 4 * qx, y = y0 + row;
     const bool upd = (row < ZM_TY) && (x < nx) && (y < ny);
@@ -354,16 +352,40 @@ inline bool zmarch_supported(int nx, int, int) { return nx % 4 == 0; }
 // The variant needs the driver's tensor-map encoder.
 inline bool zmarch_available() { return zm_encoder() != nullptr; }
 
+// Planes per CTA: the deepest march (fewest repeated prologue planes) that
+// still gives at least four waves of CTAs over the GPU's resident slots, so
+// the last partial wave costs little.
+inline int zmarch_pick_zc(int tiles_xy, int nz, int slots)
+{
+    static const int cand[] = {32, 24, 16, 12, 8};
+    for (int zc : cand) {
+        const long long ctas = static_cast<long long>(tiles_xy) * ((nz + zc - 1) / zc);
+        if (ctas >= 4LL * slots) return zc;
+    }
+    return 8;
+}
+
 inline int zmarch_plan(int nx, int ny, int nz, ZmarchPlan *plan)
 {
-    plan->grid = dim3((nx + ZM_TX - 1) / ZM_TX, (ny + ZM_TY - 1) / ZM_TY, (nz + ZM_ZC - 1) / ZM_ZC);
+    const int tx = (nx + ZM_TX - 1) / ZM_TX, ty = (ny + ZM_TY - 1) / ZM_TY;
+    plan->zc = 32;
+    plan->grid = dim3(tx, ty, (nz + plan->zc - 1) / plan->zc);
     if (!zmarch_supported(nx, ny, nz)) return 0;
     if (zm_encoder() == nullptr) return 3;
-    if (cudaFuncSetAttribute(reinterpret_cast<const void *>(&fgp_step_zmarch_tma),
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, ZM_SMEM) != cudaSuccess) {
+    const void *fn = reinterpret_cast<const void *>(&fgp_step_zmarch_tma);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ZM_SMEM) != cudaSuccess) {
         cudaGetLastError();
         return 3;
     }
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, ZM_THREADS, ZM_SMEM) != cudaSuccess) {
+        cudaGetLastError();
+        return 3;
+    }
+    plan->zc = zmarch_pick_zc(tx * ty, nz, sms * (per_sm > 0 ? per_sm : 1));
+    plan->grid = dim3(tx, ty, (nz + plan->zc - 1) / plan->zc);
     return 0;
 }
 
@@ -385,10 +407,11 @@ inline bool zm_encode(CUtensorMap *map, const float *base, int nx, int ny, int n
 
 // Fill the kernel arguments of one step: tensor maps of b and of the three
 // components of r_src.  Returns false if an encoding fails.
-inline bool zmarch_fill(const ZmarchPlan &, const StepArgs &a, int *err, ZmarchArgs &za)
+inline bool zmarch_fill(const ZmarchPlan &plan, const StepArgs &a, int *err, ZmarchArgs &za)
 {
     za.a = a;
     za.err = err;
+    za.zc = plan.zc;
     const float *r = a.rs;
     return zm_encode(&za.tb, a.b, a.nx, a.ny, a.nz, ZM_BW, ZM_HB) &&
            zm_encode(&za.t0, r, a.nx, a.ny, a.nz, ZM_W0, ZM_HB) &&
