@@ -16,6 +16,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -562,3 +563,117 @@ int tvfgp_debug_timeout_probe(tvfgp_t h, int spins, tvfgp_stream_t stream)
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// tvfgp_run_noalloc: FGP steps with no allocation at all
+// ---------------------------------------------------------------------------
+//
+// For callers that are not allowed to allocate device memory (see the
+// header).  The second r buffer of the ping-pong lives in this fixed,
+// file-scope device array instead of in a handle: it exists on every GPU
+// that loads the library, from module load until the process exits, and is
+// shared by every call on that GPU.
+
+static __device__ __align__(256) float g_noalloc_r[3 * static_cast<size_t>(TVFGP_NOALLOC_MAX_VOXELS)];
+
+namespace {
+
+// Device address of g_noalloc_r, looked up once per device.  The name
+// g_noalloc_r is only a host-side stand-in in host code, never an address a
+// kernel may be given.
+constexpr int kNoallocMaxDevices = 64;
+float *g_noalloc_addr[kNoallocMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+int noalloc_scratch(float **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoallocMaxDevices) {
+        cudaGetLastError();
+        return TVFGP_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_r);
+        if (e != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return TVFGP_ERR_CUDA;
+        }
+        g_noalloc_addr[dev] = static_cast<float *>(p);
+    }
+    *out = g_noalloc_addr[dev];
+    return TVFGP_OK;
+}
+
+}  // namespace
+
+extern "C" int tvfgp_run_noalloc(int nx, int ny, int nz, const float *b, float *p, float *r,
+                                 float lambda, int nsteps, double t0, tvfgp_stream_t stream,
+                                 double *t_final)
+{
+    if (nx < 1 || ny < 1 || nz < 1 || nx > 65535 || ny > 65535 || nz > 65535) return TVFGP_ERR_ARG;
+    const long long N = static_cast<long long>(nx) * ny * nz;
+    if (N > TVFGP_NOALLOC_MAX_VOXELS) return TVFGP_ERR_UNSUPPORTED;
+    int rc;
+    if ((rc = check_ptr(b)) || (rc = check_ptr(p)) || (rc = check_ptr(r))) return rc;
+    if ((rc = check_lambda(lambda))) return rc;
+    if (nsteps < 0 || !std::isfinite(t0) || t0 < 1.0) return TVFGP_ERR_ARG;
+    const size_t v = sizeof(float) * static_cast<size_t>(N);
+    if (overlap(b, v, p, 3 * v) || overlap(b, v, r, 3 * v) || overlap(p, 3 * v, r, 3 * v))
+        return TVFGP_ERR_ARG;
+    float *scratch = nullptr;
+    if ((rc = noalloc_scratch(&scratch))) return rc;
+    if (overlap(b, v, scratch, 3 * v) || overlap(p, 3 * v, scratch, 3 * v) ||
+        overlap(r, 3 * v, scratch, 3 * v))
+        return TVFGP_ERR_ARG;
+
+    // Same launches as tvfgp_run's eager path, with the momentum schedule
+    // evaluated step by step (no host buffer either).
+    const bool vec_ok = (nx % 4 == 0) && aligned16(b) && aligned16(p) && aligned16(r);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    StepArgs a;
+    a.b = b;
+    a.p = p;
+    a.lam = lambda;
+    a.s = step_of(lambda);
+    a.nx = nx;
+    a.ny = ny;
+    a.nz = nz;
+    a.N = N;
+    dim3 grid, block;
+    const void *fn;
+    if (vec_ok) {
+        fn = reinterpret_cast<const void *>(&fgp_step_fused4<kFusedBY, kFusedZC>);
+        block = dim3(32, kFusedBY, 1);
+        grid = dim3((nx / 4 + 31) / 32, (ny + kFusedBY - 1) / kFusedBY, (nz + kFusedZC - 1) / kFusedZC);
+    } else {
+        fn = reinterpret_cast<const void *>(&fgp_step_scalar);
+        block = dim3(32, 8, 1);
+        grid = dim3((nx + 31) / 32, (ny + 7) / 8, nz);
+    }
+    double t = t0;
+    for (int k = 0; k < nsteps; ++k) {
+        const double tn = (1.0 + std::sqrt(1.0 + 4.0 * t * t)) / 2.0;
+        a.m = static_cast<float>((t - 1.0) / tn);
+        t = tn;
+        const bool even = (k % 2) == 0;
+        a.rs = even ? r : scratch;
+        a.rd = even ? scratch : r;
+        void *args[] = {&a};
+        const cudaError_t e = cudaLaunchKernel(fn, grid, block, args, 0, st);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return from_cuda(e);
+        }
+    }
+    if (nsteps % 2 == 1) {
+        const cudaError_t e = cudaMemcpyAsync(r, scratch, 3 * v, cudaMemcpyDeviceToDevice, st);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return from_cuda(e);
+        }
+    }
+    if (t_final) *t_final = t;
+    return TVFGP_OK;
+}

@@ -62,6 +62,7 @@ def _load():
         "tvfgp_last_variant": ([vp], i),
         "tvfgp_launch_count": ([vp], ll),
         "tvfgp_debug_timeout_probe": ([vp, i, vp], i),
+        "tvfgp_run_noalloc": ([i, i, i, vp, vp, vp, f, i, d, vp, ctypes.POINTER(d)], i),
         "tvfgp_strerror": ([i], ctypes.c_char_p),
         "tvfgp_version": ([], i),
     }
@@ -192,6 +193,23 @@ def tvfgp_launch_count(h: int) -> int:
 
 def tvfgp_debug_timeout_probe(h: int, spins: int, stream=None) -> None:
     _ok(_lib.tvfgp_debug_timeout_probe(h, int(spins), _stream(stream)), "tvfgp_debug_timeout_probe")
+
+
+TVFGP_NOALLOC_MAX_VOXELS = 2097152
+
+
+def tvfgp_run_noalloc(nx: int, ny: int, nz: int, b, p, r, lam: float, nsteps: int,
+                      t0: float = 1.0, stream=None) -> float:
+    """tvfgp_run with no handle and no allocation (for callers that may not
+    allocate device memory); at most TVFGP_NOALLOC_MAX_VOXELS voxels, and
+    calls that overlap on the GPU must be serialised by the caller.  Returns
+    t after the last step."""
+    n = int(nx) * int(ny) * int(nz)
+    tf = ctypes.c_double(0.0)
+    _ok(_lib.tvfgp_run_noalloc(int(nx), int(ny), int(nz), _addr(b, n, "b"), _addr(p, 3 * n, "p"),
+                               _addr(r, 3 * n, "r"), float(lam), int(nsteps), float(t0),
+                               _stream(stream), ctypes.byref(tf)), "tvfgp_run_noalloc")
+    return tf.value
 
 
 def raw_call(name: str, *args) -> int:

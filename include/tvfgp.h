@@ -160,6 +160,40 @@ long long tvfgp_launch_count(tvfgp_t h);
  * reports TVFGP_ERR_TIMEOUT.  1 <= spins <= 2^24. */
 int tvfgp_debug_timeout_probe(tvfgp_t h, int spins, tvfgp_stream_t stream);
 
+/* Capacity, in voxels, of tvfgp_run_noalloc's built-in scratch buffer
+ * (2^21 voxels, e.g. 128^3: 3 * 2^21 floats = 24 MiB of device memory). */
+#define TVFGP_NOALLOC_MAX_VOXELS 2097152
+
+/* tvfgp_run without a handle and without any allocation.  The page has no
+ * counterpart: this entry point exists for callers that must not allocate
+ * device memory themselves, for example code running inside a host
+ * framework that owns the whole device memory pool, a plug-in that is given
+ * only buffers, or a loop that cannot afford the device-wide synchronisation
+ * a cudaMalloc/cudaFree may cause.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine, and no host heap allocation either.
+ *
+ * Arguments as tvfgp_run (b [N], p and r [3N] caller-owned device buffers,
+ * lambda, nsteps, t0, stream, t_final), with the shape passed directly.
+ * Results are bitwise identical to tvfgp_run's.
+ *
+ * The second r buffer of the ping-pong is a fixed device array compiled into
+ * the library (TVFGP_NOALLOC_MAX_VOXELS voxels, 24 MiB), which every GPU that
+ * loads the library holds until the process exits.  Consequences:
+ *   - nx*ny*nz > TVFGP_NOALLOC_MAX_VOXELS returns TVFGP_ERR_UNSUPPORTED
+ *     before anything is enqueued;
+ *   - all calls on one GPU share the array, which keeps the last call's
+ *     contents; nothing in it needs to start at zero (each step writes every
+ *     value before the next step reads it), but calls whose work overlaps on
+ *     the GPU (different streams, or different host threads) race on it and
+ *     must be serialised by the caller;
+ *   - the first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture is begun on the calling thread.
+ * The vector kernel runs when nx % 4 == 0 and b, p, r are 16-byte aligned,
+ * the scalar kernel otherwise. */
+int tvfgp_run_noalloc(int nx, int ny, int nz, const float *b, float *p, float *r, float lambda,
+                      int nsteps, double t0, tvfgp_stream_t stream, double *t_final);
+
 /* Static description of a status code. */
 const char *tvfgp_strerror(int code);
 
