@@ -167,8 +167,10 @@ def hbm_peak():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the device code of the step kernels (the files that hold the
+    kernels and their launch shapes); host-only changes keep it."""
     h = hashlib.sha256()
-    for fn in ("fgp_kernels.cuh", "zmarch_tma.cuh", "tvfgp.cu"):
+    for fn in ("fgp_kernels.cuh", "zmarch_tma.cuh"):
         with open(os.path.join(ROOT, "fgp_dual_stencil_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -264,26 +266,16 @@ def gpu_arm(args, world, rank, local_rank, dist):
              T.TVFGP_VARIANT_ZMARCH_TMA: "fgp_step_zmarch_tma"}.get(variant_used, "?")
     traffic = ncu_traffic(kname, N)
 
-    # end to end: pinned host b in, z out, every step, through the public API
+    # end to end: every step's b copied in from pinned host memory and its z
+    # copied back, through the public API; the copies run on their own
+    # streams (double-buffered) and overlap the previous / next step's compute
     e2e = None
     if not args.no_e2e:
-        z_host = torch.empty((w.nz, w.ny, w.nx), dtype=torch.float32).pin_memory()
-        b_in = torch.empty_like(b_dev[0])
-        Ke = K
-        barrier(dist)
-        torch.cuda.synchronize(dev)
-        t0 = time.perf_counter()
-        for j in range(Ke):
-            b_in.copy_(b_host[j % n_b], non_blocking=True)
-            h.run(b_in, p, r, w.lam, w.steps, w.t0, stream)
-            h.primal(b_in, p, w.lam, z, stream)
-            z_host.copy_(z, non_blocking=True)
-        torch.cuda.synchronize(dev)
-        e2e_s = max_over_ranks(dist, time.perf_counter() - t0)
-        barrier(dist)
-        e2e = {"value": round(world * N * w.steps * Ke / e2e_s / 1e9, 3), "unit": UNIT,
+        e2e_s = end_to_end(torch, h, w, b_host, p, r, stream, dev, K, dist)
+        e2e = {"value": round(world * N * w.steps * K / e2e_s / 1e9, 3), "unit": UNIT,
                "h2d_bytes_per_step": 4 * N, "d2h_bytes_per_step": 4 * N,
-               "ms_per_step": round(e2e_s * 1e3 / Ke, 4)}
+               "ms_per_step": round(e2e_s * 1e3 / K, 4),
+               "overlap": "H2D of step j+1 and D2H of step j on two copy streams, double-buffered"}
         if h.check(stream) != T.TVFGP_OK:
             raise RuntimeError("device error word set during the end-to-end run")
 
@@ -341,6 +333,52 @@ def gpu_arm(args, world, rank, local_rank, dist):
         "cpu_baseline": cpu,
     }
     return out
+
+
+def end_to_end(torch, h, w, b_host, p, r, stream, dev, K, dist):
+    """Wall time of K outer iterations where each step's b comes from pinned
+    host memory and its z goes back to pinned host memory."""
+    n_b = len(b_host)
+    shape = (w.nz, w.ny, w.nx)
+    b_in = [torch.empty(shape, device=dev) for _ in range(2)]
+    z_out = [torch.empty(shape, device=dev) for _ in range(2)]
+    z_host = [torch.empty(shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]       # b_in[s] filled
+    ev_done = [torch.cuda.Event() for _ in range(2)]     # step using slot s finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]      # z_host[s] filled, z_out[s] free
+
+    def h2d(j):
+        s = j % 2
+        with torch.cuda.stream(s_in):
+            if j >= 2:
+                s_in.wait_event(ev_done[s])              # b_in[s] no longer read
+            b_in[s].copy_(b_host[j % n_b], non_blocking=True)
+            ev_in[s].record(s_in)
+
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    h2d(0)
+    for j in range(K):
+        s = j % 2
+        if j + 1 < K:
+            h2d(j + 1)
+        stream.wait_event(ev_in[s])
+        if j >= 2:
+            stream.wait_event(ev_out[s])                 # z_out[s] copied out
+        h.run(b_in[s], p, r, w.lam, w.steps, w.t0, stream)
+        h.primal(b_in[s], p, w.lam, z_out[s], stream)
+        ev_done[s].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[s])
+            z_host[s].copy_(z_out[s], non_blocking=True)
+            ev_out[s].record(s_out)
+    torch.cuda.synchronize(dev)
+    dt = max_over_ranks(dist, time.perf_counter() - t0)
+    barrier(dist)
+    return dt
 
 
 def cpu_baseline(w, base):
