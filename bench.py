@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cpu-threads", default="",
+                    help="comma-separated oracle thread counts for the CPU baseline (default: all cores)")
     return ap.parse_args()
 
 
@@ -281,7 +283,8 @@ def gpu_arm(args, world, rank, local_rank, dist):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, base)
+        threads = [int(t) for t in args.cpu_threads.split(",") if t.strip()]
+        cpu = cpu_baseline(w, base, threads)
 
     h.close()
     names = {T.TVFGP_VARIANT_FUSED: "fused", T.TVFGP_VARIANT_SCALAR: "scalar",
@@ -381,24 +384,37 @@ def end_to_end(torch, h, w, b_host, p, r, stream, dev, K, dist):
     return dt
 
 
-def cpu_baseline(w, base):
-    """The CPU oracle, as it stands, on a bounded sample of the workload: one
-    outer iteration (w.steps FGP steps + primal) on the full volume, all host
-    cores."""
+def cpu_baseline(w, base, threads=()):
+    """The CPU oracle, as it stands, on a bounded sample of the workload: up to
+    10 FGP steps of the first outer iteration, then the primal, on the full
+    volume; all host cores unless thread counts are given (the first count
+    then gives `value`, each count its own entry in `by_threads`)."""
     import numpy as np
     import oracle
     from fgp_dual_stencil_gb300 import synth
     b = synth.make_b(w, 0, base)
-    p = np.zeros((3,) + b.shape, np.float32)
-    r = np.zeros_like(p)
-    t0 = time.perf_counter()
-    oracle.fgp_run(b, p, r, w.lam, w.steps, w.t0)
-    oracle.primal(b, p, w.lam)
-    dt = time.perf_counter() - t0
-    return {"value": round(w.nvox * w.steps / dt / 1e9, 4), "unit": UNIT, "cores": oracle.get_threads(),
-            "kind": "oracle",
-            "sample": "one outer iteration (%d FGP steps + primal) on the full %dx%dx%d volume, %.1f s"
-                      % (w.steps, w.nx, w.ny, w.nz, dt)}
+    steps = min(w.steps, 10)
+    all_cores = oracle.get_threads()
+    counts = list(threads) or [all_cores]
+    res = {}
+    for n in counts:
+        oracle.set_threads(n)
+        p = np.zeros((3,) + b.shape, np.float32)
+        r = np.zeros_like(p)
+        t0 = time.perf_counter()
+        oracle.fgp_run(b, p, r, w.lam, steps, w.t0)
+        oracle.primal(b, p, w.lam)
+        res[n] = time.perf_counter() - t0
+    oracle.set_threads(all_cores)
+    n0 = counts[0]
+    out = {"value": round(w.nvox * steps / res[n0] / 1e9, 4), "unit": UNIT, "cores": n0,
+           "kind": "oracle",
+           "sample": "%d FGP steps + primal of the first outer iteration on the full %dx%dx%d volume, %.1f s"
+                     % (steps, w.nx, w.ny, w.nz, res[n0])}
+    if len(counts) > 1:
+        out["by_threads"] = {str(n): {"value": round(w.nvox * steps / t / 1e9, 4),
+                                      "ms_per_fgp_step": round(t * 1e3 / steps, 2)} for n, t in res.items()}
+    return out
 
 
 # ---------------------------------------------------------------------------
