@@ -552,6 +552,32 @@ int tvfgp_check(tvfgp_t h, tvfgp_stream_t stream)
     return flag != 0 ? TVFGP_ERR_TIMEOUT : TVFGP_OK;
 }
 
+int tvfgp_host_alloc(size_t bytes, int write_combined, void **out)
+{
+    if (out == nullptr) return TVFGP_ERR_ARG;
+    *out = nullptr;
+    if (bytes == 0) return TVFGP_ERR_ARG;
+    const unsigned flags = write_combined ? cudaHostAllocWriteCombined : cudaHostAllocDefault;
+    const cudaError_t e = cudaHostAlloc(out, bytes, flags);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *out = nullptr;
+        return from_cuda(e);
+    }
+    return TVFGP_OK;
+}
+
+int tvfgp_host_free(void *p)
+{
+    if (p == nullptr) return TVFGP_OK;
+    const cudaError_t e = cudaFreeHost(p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return from_cuda(e);
+    }
+    return TVFGP_OK;
+}
+
 int tvfgp_debug_timeout_probe(tvfgp_t h, int spins, tvfgp_stream_t stream)
 {
     if (!valid(h) || spins < 1 || spins > (1 << 24)) return TVFGP_ERR_ARG;

@@ -4,20 +4,23 @@
 // z, two planes of r and z on chip; rebuilt here around the Blackwell tensor
 // memory accelerator instead of plain loads and barriers).
 //
-// A CTA owns the columns x0..x0+63 and computes z for the 16 rows
-// y0..y0+15 of each plane; it updates the dual on the first 15 rows (the
-// 16th row's z is the y+1 neighbour of the 15th).  It walks ZC planes in z.
-// For each plane q a TMA load brings, into one slot of a 4-deep ring:
-//   b  at x0..x0+67,   y0..y0+15          (z(x0+64) is the x+1 neighbour)
-//   r0 at x0-4..x0+67, y0..y0+15          (r0(x-1) for L)
-//   r1 at x0..x0+67,   y0-1..y0+15        (r1(y-1) for L)
-//   r2 at x0..x0+67,   y0..y0+15
+// A CTA owns the columns x0..x0+TX-1 (TX = 32 by default) and computes z
+// for the ROWS = 16 rows y0..y0+15 of each plane; it updates the dual on the
+// first 15 rows (the 16th row's z is the y+1 neighbour of the 15th).  It
+// walks zc planes in z (chosen per volume at set-up).  For each plane q a
+// TMA load brings, into one slot of a 4-deep ring:
+//   b  at x0..x0+TX+3,   y0..y0+15        (z(x0+TX) is the x+1 neighbour)
+//   r0 at x0-4..x0+TX+3, y0..y0+15        (r0(x-1) for L)
+//   r1 at x0..x0+TX+3,   y0-1..y0+15      (r1(y-1) for L)
+//   r2 at x0..x0+TX+3,   y0..y0+15
+//   p0, p1, p2 at x0..x0+TX-1, y0..y0+14  (the voxels' own p)
 // Coordinates outside the volume read as zero, which is the r_a(-1) = 0
 // boundary of L.  A thread owns 4 consecutive x voxels of one row: it keeps
 // its own r and z of the current and next plane in registers, so only the
 // z of the x+1 and y+1 neighbours goes through shared memory (a 3-slot ring
-// of z planes: one barrier per plane suffices).  The voxel's own p is loaded
-// from global memory at the top of each plane, before any wait.
+// of z planes: one barrier per plane suffices).  Every load of the step is a
+// TMA copy issued planes ahead, before any wait on it: the voxel's own p and
+// r arrive with their plane, and no thread issues a global load.
 //
 // Every wait on a TMA barrier is bounded; on timeout the kernel sets the
 // caller's error word, drains its outstanding copies (again bounded) and
@@ -32,13 +35,16 @@
 namespace tvfgp {
 
 #ifndef TVFGP_ZM_TX
-#define TVFGP_ZM_TX 64
+#define TVFGP_ZM_TX 32
 #endif
 #ifndef TVFGP_ZM_ROWS
 #define TVFGP_ZM_ROWS 16
 #endif
 #ifndef TVFGP_ZM_MINB
-#define TVFGP_ZM_MINB 2
+#define TVFGP_ZM_MINB 3
+#endif
+#ifndef TVFGP_ZM_L2PROMO
+#define TVFGP_ZM_L2PROMO CU_TENSOR_MAP_L2_PROMOTION_L2_256B
 #endif
 constexpr int ZM_TX = TVFGP_ZM_TX;        // tile width (voxels)
 constexpr int ZM_ROWS = TVFGP_ZM_ROWS;    // rows whose z is computed per plane
@@ -46,7 +52,7 @@ constexpr int ZM_TY = ZM_ROWS - 1;        // rows whose dual is updated
 constexpr int ZM_QX = ZM_TX / 4;          // quads per row
 constexpr int ZM_THREADS = ZM_QX * ZM_ROWS;
 #ifndef TVFGP_ZM_STAGES
-#define TVFGP_ZM_STAGES 2
+#define TVFGP_ZM_STAGES 4
 #endif
 constexpr int ZM_STAGES = TVFGP_ZM_STAGES;   // TMA ring depth (planes in flight)
 constexpr int ZM_MAX_POLLS = 1 << 22;     // bound of every barrier wait
@@ -62,12 +68,17 @@ constexpr int ZM_BYTES_B = ZM_BW * ZM_HB * 4;
 constexpr int ZM_BYTES_R0 = ZM_W0 * ZM_HB * 4;
 constexpr int ZM_BYTES_R1 = ZM_BW * ZM_H1 * 4;
 constexpr int ZM_BYTES_R2 = ZM_BW * ZM_HB * 4;
+constexpr int ZM_BYTES_P = ZM_TX * ZM_TY * 4;      // one component of p
 constexpr int ZM_OFF_B = 0;
 constexpr int ZM_OFF_R0 = zm_round128(ZM_OFF_B + ZM_BYTES_B);
 constexpr int ZM_OFF_R1 = zm_round128(ZM_OFF_R0 + ZM_BYTES_R0);
 constexpr int ZM_OFF_R2 = zm_round128(ZM_OFF_R1 + ZM_BYTES_R1);
-constexpr int ZM_STAGE_STRIDE = zm_round128(ZM_OFF_R2 + ZM_BYTES_R2);
-constexpr int ZM_STAGE_TX = ZM_BYTES_B + ZM_BYTES_R0 + ZM_BYTES_R1 + ZM_BYTES_R2;
+constexpr int ZM_OFF_P0 = zm_round128(ZM_OFF_R2 + ZM_BYTES_R2);
+constexpr int ZM_OFF_P1 = zm_round128(ZM_OFF_P0 + ZM_BYTES_P);
+constexpr int ZM_OFF_P2 = zm_round128(ZM_OFF_P1 + ZM_BYTES_P);
+constexpr int ZM_STAGE_STRIDE = zm_round128(ZM_OFF_P2 + ZM_BYTES_P);
+constexpr int ZM_STAGE_TX_BR = ZM_BYTES_B + ZM_BYTES_R0 + ZM_BYTES_R1 + ZM_BYTES_R2;
+constexpr int ZM_STAGE_TX = ZM_STAGE_TX_BR + 3 * ZM_BYTES_P;
 constexpr int ZM_OFF_PREV = ZM_STAGES * ZM_STAGE_STRIDE;               // r2 of plane z0-1
 constexpr int ZM_OFF_Z = zm_round128(ZM_OFF_PREV + ZM_BYTES_R2);       // 3 z planes
 constexpr int ZM_BYTES_Z = 3 * ZM_ROWS * ZM_ZP * 4;
@@ -76,6 +87,10 @@ constexpr int ZM_OFF_FLAG = ZM_OFF_BAR + 8 * (ZM_STAGES + 1);
 constexpr int ZM_SMEM = ZM_OFF_FLAG + 16 + 128;                        // + base alignment
 
 static_assert(ZM_TX % 4 == 0 && ZM_W0 <= 256 && ZM_H1 <= 256, "TMA box limits");
+// Plane q's slot holds its p until the dual update of q, one iteration after
+// its b and r were consumed; the next plane is loaded into the slot of q-1,
+// so a plane is issued S-1 iterations before its wait: S >= 3.
+static_assert(ZM_STAGES >= 3, "the ring needs three slots");
 static_assert(ZM_SMEM * TVFGP_ZM_MINB <= 227 * 1024, "CTAs per SM must fit in shared memory");
 
 struct ZmarchPlan {
@@ -85,6 +100,7 @@ struct ZmarchPlan {
 
 struct ZmarchArgs {
     CUtensorMap tb, t0, t1, t2;   // b, r0, r1, r2 of the r read by this step
+    CUtensorMap tp0, tp1, tp2;    // the three components of p
     StepArgs a;
     int *err;
     int zc;                       // planes per CTA (grid.z = ceil(nz / zc))
@@ -151,7 +167,7 @@ __device__ __forceinline__ void zm_quad(const unsigned char *st, int row, int qx
     Z = zquad(Bq, R0, R1, R2, left, R1lo, r2lo, lam);
 }
 
-// z at column x0+64 of a row (the x+1 neighbour of the tile's last quad).
+// z at column x0+TX of a row (the x+1 neighbour of the tile's last quad).
 __device__ __forceinline__ float zm_halo(const unsigned char *st, int row, float r2lo, float lam,
                                          float &r2here)
 {
@@ -198,7 +214,13 @@ __global__ void __launch_bounds__(ZM_THREADS, TVFGP_ZM_MINB) fgp_step_zmarch_tma
     auto issue = [&](int q) {                       // thread 0 only
         unsigned char *st = smem + ((q - z0) % ZM_STAGES) * ZM_STAGE_STRIDE;
         uint64_t *bar = &bars[(q - z0) % ZM_STAGES];
-        mbar_expect_tx(bar, ZM_STAGE_TX);
+        const bool with_p = q < ze;                 // plane ze only feeds z(i+ez)
+        mbar_expect_tx(bar, with_p ? ZM_STAGE_TX : ZM_STAGE_TX_BR);
+        if (with_p) {
+            tma_load_3d(st + ZM_OFF_P0, &za.tp0, x0, y0, q, bar);
+            tma_load_3d(st + ZM_OFF_P1, &za.tp1, x0, y0, q, bar);
+            tma_load_3d(st + ZM_OFF_P2, &za.tp2, x0, y0, q, bar);
+        }
         tma_load_3d(st + ZM_OFF_B, &za.tb, x0, y0, q, bar);
         tma_load_3d(st + ZM_OFF_R0, &za.t0, x0 - 4, y0, q, bar);
         tma_load_3d(st + ZM_OFF_R1, &za.t1, x0, y0 - 1, q, bar);
@@ -219,7 +241,7 @@ __global__ void __launch_bounds__(ZM_THREADS, TVFGP_ZM_MINB) fgp_step_zmarch_tma
 
     // prologue: z of plane z0, own r at z0
     float4 Rc0, Rc1, Rc2, Zc;
-    float r2halo = 0.0f;                            // r2 at column x0+64 of the current plane
+    float r2halo = 0.0f;                            // r2 at column x0+TX of the current plane
     bool ok = true;
     {
         float4 r2lo = f4zero();
@@ -242,7 +264,6 @@ __global__ void __launch_bounds__(ZM_THREADS, TVFGP_ZM_MINB) fgp_step_zmarch_tma
         }
     }
     __syncthreads();
-    if (tid == 0 && *abort_flag == 0 && next_issue <= qmax) issue(next_issue++);   // z0's slot is free
 
     float *p0 = a.p, *p1 = a.p + a.N, *p2 = a.p + 2 * a.N;
     float *o0 = a.rd, *o1 = a.rd + a.N, *o2 = a.rd + 2 * a.N;
@@ -251,14 +272,8 @@ __global__ void __launch_bounds__(ZM_THREADS, TVFGP_ZM_MINB) fgp_step_zmarch_tma
     for (int z = z0; z < ze && *abort_flag == 0; ++z) {
         zlast = z;
         const long long i = x + (long long)nx * (y + (long long)ny * z);
-        // (1) the voxel's own p, before any wait
-        float4 P0 = f4zero(), P1 = f4zero(), P2 = f4zero();
-        if (upd) {
-            P0 = ld_once4(p0 + i);
-            P1 = ld_once4(p1 + i);
-            P2 = ld_once4(p2 + i);
-        }
-        // (2) z of plane z+1 from its staged planes; own r of plane z is r2lo
+        // (1) z of plane z+1 from its staged planes (own r2 of plane z is its
+        //     z-lower neighbour)
         const bool hasZ = (z + 1 < nz);
         float4 Rn0 = f4zero(), Rn1 = f4zero(), Rn2 = f4zero(), Zn = f4zero();
         float r2halo_n = 0.0f;
@@ -275,13 +290,19 @@ __global__ void __launch_bounds__(ZM_THREADS, TVFGP_ZM_MINB) fgp_step_zmarch_tma
         }
         __syncthreads();
         if (*abort_flag) break;
-        // plane z+1 is consumed: its slot takes the next plane
-        if (tid == 0 && hasZ && next_issue <= qmax) {
+        // every thread finished plane z-1 (its dual update read that slot's
+        // p): the slot takes the next plane
+        if (tid == 0 && z > z0 && next_issue <= qmax) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             issue(next_issue++);
         }
-        // (3) dual update of plane z
+        // (2) dual update of plane z, with its own p from the staged plane
         if (upd) {
+            const unsigned char *stz = stage_of(z);
+            const int pofs = row * ZM_TX + 4 * qx;
+            float4 P0 = lds4(reinterpret_cast<const float *>(stz + ZM_OFF_P0) + pofs);
+            float4 P1 = lds4(reinterpret_cast<const float *>(stz + ZM_OFF_P1) + pofs);
+            float4 P2 = lds4(reinterpret_cast<const float *>(stz + ZM_OFF_P2) + pofs);
             const float *zr = zrow(z, row);
             const float zx = zr[4 * qx + 4];
             const float4 ZY = hasY ? lds4(zrow(z, row + 1) + 4 * qx) : f4zero();
@@ -402,7 +423,7 @@ inline bool zm_encode(CUtensorMap *map, const float *base, int nx, int ny, int n
     const cuuint32_t estr[3] = {1, 1, 1};
     return zm_encoder()(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides,
                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+                        TVFGP_ZM_L2PROMO, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Fill the kernel arguments of one step: tensor maps of b and of the three
@@ -413,7 +434,10 @@ inline bool zmarch_fill(const ZmarchPlan &plan, const StepArgs &a, int *err, Zma
     za.err = err;
     za.zc = plan.zc;
     const float *r = a.rs;
-    return zm_encode(&za.tb, a.b, a.nx, a.ny, a.nz, ZM_BW, ZM_HB) &&
+    return zm_encode(&za.tp0, a.p, a.nx, a.ny, a.nz, ZM_TX, ZM_TY) &&
+           zm_encode(&za.tp1, a.p + a.N, a.nx, a.ny, a.nz, ZM_TX, ZM_TY) &&
+           zm_encode(&za.tp2, a.p + 2 * a.N, a.nx, a.ny, a.nz, ZM_TX, ZM_TY) &&
+           zm_encode(&za.tb, a.b, a.nx, a.ny, a.nz, ZM_BW, ZM_HB) &&
            zm_encode(&za.t0, r, a.nx, a.ny, a.nz, ZM_W0, ZM_HB) &&
            zm_encode(&za.t1, r + a.N, a.nx, a.ny, a.nz, ZM_BW, ZM_H1) &&
            zm_encode(&za.t2, r + 2 * a.N, a.nx, a.ny, a.nz, ZM_BW, ZM_HB);

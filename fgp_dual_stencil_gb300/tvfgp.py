@@ -63,6 +63,8 @@ def _load():
         "tvfgp_launch_count": ([vp], ll),
         "tvfgp_debug_timeout_probe": ([vp, i, vp], i),
         "tvfgp_run_noalloc": ([i, i, i, vp, vp, vp, f, i, d, vp, ctypes.POINTER(d)], i),
+        "tvfgp_host_alloc": ([ctypes.c_size_t, i, ctypes.POINTER(vp)], i),
+        "tvfgp_host_free": ([vp], i),
         "tvfgp_strerror": ([i], ctypes.c_char_p),
         "tvfgp_version": ([], i),
     }
@@ -210,6 +212,35 @@ def tvfgp_run_noalloc(nx: int, ny: int, nz: int, b, p, r, lam: float, nsteps: in
                                _addr(r, 3 * n, "r"), float(lam), int(nsteps), float(t0),
                                _stream(stream), ctypes.byref(tf)), "tvfgp_run_noalloc")
     return tf.value
+
+
+def tvfgp_host_alloc(nbytes: int, write_combined: bool = False) -> int:
+    """Page-locked host memory (an int address); see include/tvfgp.h."""
+    p = ctypes.c_void_p()
+    _ok(_lib.tvfgp_host_alloc(int(nbytes), 1 if write_combined else 0, ctypes.byref(p)),
+        "tvfgp_host_alloc")
+    return p.value
+
+
+def tvfgp_host_free(addr: int) -> None:
+    _ok(_lib.tvfgp_host_free(addr), "tvfgp_host_free")
+
+
+def host_tensor(shape, write_combined: bool = False):
+    """A float32 CPU torch tensor of `shape` over tvfgp_host_alloc memory,
+    freed when the tensor (and any view of it) is garbage collected.
+    Write-combined memory suits host-to-device inputs: fast to fill, slow to
+    read back on the CPU."""
+    import weakref
+    import numpy as np
+    import torch
+    n = 1
+    for s_ in shape:
+        n *= int(s_)
+    addr = tvfgp_host_alloc(4 * n, write_combined)
+    arr = np.ctypeslib.as_array((ctypes.c_float * n).from_address(addr)).reshape(tuple(shape))
+    weakref.finalize(arr, _lib.tvfgp_host_free, addr)
+    return torch.from_numpy(arr)
 
 
 def raw_call(name: str, *args) -> int:

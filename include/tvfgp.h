@@ -154,6 +154,19 @@ int tvfgp_last_variant(tvfgp_t h);
  * bounded-wait probe counts one; graph replays count their nodes). */
 long long tvfgp_launch_count(tvfgp_t h);
 
+/* Page-locked host memory for staging volumes between the host and the GPU
+ * (for callers whose b comes from, or whose z goes to, host memory).  With
+ * write_combined != 0 the memory is write-combined: the CPU writes it at full
+ * speed and the GPU reads it at a steady rate without snooping CPU caches,
+ * but CPU reads of it are very slow, so use it for host-to-device inputs
+ * only.  *out receives the allocation (NULL on failure; TVFGP_ERR_OOM or
+ * TVFGP_ERR_CUDA).  bytes must be > 0.  Release with tvfgp_host_free. */
+int tvfgp_host_alloc(size_t bytes, int write_combined, void **out);
+
+/* Release memory from tvfgp_host_alloc.  NULL is accepted.  The caller must
+ * make sure no copy from or to it is still in flight. */
+int tvfgp_host_free(void *p);
+
 /* Test hook for the bounded-wait path: launches one block that waits on a
  * shared-memory barrier nobody arrives at, gives up after about `spins`
  * polls, sets the handle's error word and returns.  tvfgp_check() then

@@ -94,3 +94,11 @@ def test_create_without_a_gpu_reports_a_cuda_error(T):
     h = ctypes.c_void_p()
     assert T.raw_call("tvfgp_create", 8, 8, 8, ctypes.byref(h)) in (T.TVFGP_ERR_CUDA, T.TVFGP_ERR_OOM)
     assert h.value is None
+
+
+def test_host_alloc_argument_checks(T):
+    p = ctypes.c_void_p(1)
+    assert T.raw_call("tvfgp_host_alloc", 0, 0, ctypes.byref(p)) == T.TVFGP_ERR_ARG
+    assert p.value is None
+    assert T.raw_call("tvfgp_host_alloc", 16, 0, None) == T.TVFGP_ERR_ARG
+    assert T.raw_call("tvfgp_host_free", None) == T.TVFGP_OK

@@ -249,3 +249,22 @@ def test_bounded_wait_reports_timeout_and_context_survives(T):
     po = np.zeros_like(host(p)); ro = np.zeros_like(po)
     oracle.fgp_run(synth.make_b(w, 0), po, ro, w.lam, w.steps, 1.0)
     assert max_diff(host(p), po) == 0.0
+
+
+@pytest.mark.parametrize("wc", [False, True])
+def test_host_staging_memory_round_trip(T, wc):
+    """Pinned (and write-combined) host memory from the library as the source
+    of an input copy and the target of a result copy."""
+    import torch
+    torch.zeros(1, device="cuda")          # torch reports pinning only once CUDA is up
+    shape = (33, 17, 9)
+    src = T.host_tensor((shape[2], shape[1], shape[0]), write_combined=wc)
+    assert src.is_pinned()
+    b = synth.random_case(shape, 5)
+    src.numpy()[...] = b
+    d = torch.empty_like(src, device="cuda")
+    d.copy_(src, non_blocking=True)
+    out = T.host_tensor(src.shape, write_combined=False)
+    out.copy_(d * 2, non_blocking=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.numpy(), 2 * b)
