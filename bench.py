@@ -51,7 +51,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", default="c4", help="c1..c5 (default c4: 512^3)")
-    ap.add_argument("--variant", default="auto", choices=["auto", "fused", "scalar", "zmarch"])
+    ap.add_argument("--variant", default="auto", choices=["auto", "fused", "scalar", "zmarch", "zmarch2"])
     ap.add_argument("--eager", action="store_true", help="launch eagerly instead of graph replay")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -272,7 +272,8 @@ def gpu_arm(args, world, rank, local_rank, dist):
     peak, peak_kind = hbm_peak()
     achieved = BYTES_PER_VOXEL_STEP * N / fgp_launch_s / 1e9
     kname = {T.TVFGP_VARIANT_FUSED: "fgp_step_fused4", T.TVFGP_VARIANT_SCALAR: "fgp_step_scalar",
-             T.TVFGP_VARIANT_ZMARCH_TMA: "fgp_step_zmarch_tma"}.get(variant_used, "?")
+             T.TVFGP_VARIANT_ZMARCH_TMA: "fgp_step_zmarch_tma",
+             T.TVFGP_VARIANT_ZMARCH2_TMA: "fgp_step2_zmarch_tma"}.get(variant_used, "?")
     traffic = ncu_traffic(kname, N)
 
     # end to end: every step's b copied in from pinned host memory and its z
@@ -297,7 +298,7 @@ def gpu_arm(args, world, rank, local_rank, dist):
 
     h.close()
     names = {T.TVFGP_VARIANT_FUSED: "fused", T.TVFGP_VARIANT_SCALAR: "scalar",
-             T.TVFGP_VARIANT_ZMARCH_TMA: "zmarch"}
+             T.TVFGP_VARIANT_ZMARCH_TMA: "zmarch", T.TVFGP_VARIANT_ZMARCH2_TMA: "zmarch2"}
     out = {
         "metric": METRIC,
         "value": round(value, 3),

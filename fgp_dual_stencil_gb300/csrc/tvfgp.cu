@@ -9,6 +9,7 @@
 #include "tvfgp.h"
 #include "fgp_kernels.cuh"
 #include "zmarch_tma.cuh"
+#include "zmarch2_tma.cuh"
 
 #include <cuda_runtime.h>
 
@@ -76,8 +77,10 @@ struct tvfgp_handle {
     int last_variant;
     long long launches;
     float *scratch;
+    float *pair_scratch;        // 9N floats, two-step runs only
     int *d_err;
     ZmarchPlan zplan;
+    Zmarch2Plan z2plan;
     GraphEntry graphs[kGraphSlots];
     unsigned long long graph_clock;
 };
@@ -122,7 +125,7 @@ float step_of(float lam) { return static_cast<float>(1.0 / (12.0 * static_cast<d
 int resolve_variant(const tvfgp_handle *h, int requested, bool vec_ok)
 {
     int v = requested == TVFGP_VARIANT_AUTO ? kAutoVariant : requested;
-    if (v == TVFGP_VARIANT_FUSED || v == TVFGP_VARIANT_ZMARCH_TMA) {
+    if (v == TVFGP_VARIANT_FUSED || v == TVFGP_VARIANT_ZMARCH_TMA || v == TVFGP_VARIANT_ZMARCH2_TMA) {
         if (!vec_ok) return TVFGP_VARIANT_SCALAR;
     }
     return v;
@@ -168,37 +171,118 @@ LaunchCfg step_cfg(const tvfgp_handle *h, int variant)
     return c;
 }
 
-// Kernel-argument storage for one launch of either kernel family.
+// One kernel launch of a run: a single step (p updated in place, r_src ->
+// r_dst) or a two-step launch (p_src -> p_dst and r_src -> r_dst).
+struct Item {
+    int kernel;             // a TVFGP_VARIANT_* value
+    const float *p_src;
+    float *p_dst;
+    const float *r_src;
+    float *r_dst;
+    float m0, m1;           // momentum weights of its step(s)
+};
+
+// Kernel-argument storage for one launch of any kernel family.
 struct KArgs {
     StepArgs a;
     ZmarchArgs za;
+    Zmarch2Args z2;
     void *ptrs[1];
 };
 
-bool fill_kargs(const tvfgp_handle *h, int variant, const StepArgs &a, KArgs &k)
+LaunchCfg item_cfg(const tvfgp_handle *h, int kernel)
 {
-    k.a = a;
-    if (variant == TVFGP_VARIANT_ZMARCH_TMA) {
+    if (kernel == TVFGP_VARIANT_ZMARCH2_TMA) {
+        LaunchCfg c;
+        c.func = zmarch2_kernel();
+        c.block = dim3(zmarch2_threads(), 1, 1);
+        c.grid = h->z2plan.grid;
+        c.smem = zmarch2_smem_bytes();
+        return c;
+    }
+    return step_cfg(h, kernel);
+}
+
+bool fill_item(const tvfgp_handle *h, const Item &it, const float *b, float lam, KArgs &k)
+{
+    if (it.kernel == TVFGP_VARIANT_ZMARCH2_TMA) {
+        k.ptrs[0] = &k.z2;
+        return zmarch2_fill(h->z2plan, b, it.p_src, it.p_dst, it.r_src, it.r_dst, lam, step_of(lam),
+                            it.m0, it.m1, h->nx, h->ny, h->nz, h->N, h->d_err, k.z2);
+    }
+    k.a = make_args(h, b, it.p_dst, it.r_src, it.r_dst, lam, it.m0);
+    if (it.kernel == TVFGP_VARIANT_ZMARCH_TMA) {
         k.ptrs[0] = &k.za;
-        return zmarch_fill(h->zplan, a, h->d_err, k.za);
+        return zmarch_fill(h->zplan, k.a, h->d_err, k.za);
     }
     k.ptrs[0] = &k.a;
     return true;
 }
 
-int launch_step(tvfgp_handle *h, int variant, const StepArgs &a, cudaStream_t st)
+// Buffers a field passes through in `moves` out-of-place updates that start
+// and end in buf[0] (moves >= 2): buf[0] -> buf[1] -> buf[2] -> buf[1] ... -> buf[0].
+void route(int moves, float *const buf[3], std::vector<float *> &seq)
 {
-    const LaunchCfg c = step_cfg(h, variant);
+    seq.assign(static_cast<size_t>(moves) + 1, buf[0]);
+    if (moves >= 1) seq[1] = buf[1];
+    for (int i = 2; i < moves; ++i) seq[i] = seq[i - 1] == buf[1] ? buf[2] : buf[1];
+    seq[moves] = buf[0];
+}
+
+// The launches of an nsteps run.  Two-step launches are used from four steps
+// on; p and r then travel through the handle's two extra buffer sets and end
+// in the caller's buffers, with no copy.  Single steps ping-pong r with the
+// scratch buffer; an odd count then needs one copy back (*copy_back).
+void plan_run(const tvfgp_handle *h, int variant, float *p, float *r, const std::vector<double> &m,
+              std::vector<Item> &items, bool *copy_back)
+{
+    const int n = static_cast<int>(m.size());
+    items.clear();
+    *copy_back = false;
+    if (variant == TVFGP_VARIANT_ZMARCH2_TMA && n >= 4 && h->pair_scratch != nullptr) {
+        const size_t N3 = 3 * static_cast<size_t>(h->N);
+        const int pairs = n / 2, single = n % 2;
+        float *pb[3] = {p, h->pair_scratch, h->pair_scratch + N3};
+        float *rb[3] = {r, h->scratch, h->pair_scratch + 2 * N3};
+        std::vector<float *> sp, sr;
+        route(pairs, pb, sp);
+        route(pairs + single, rb, sr);
+        for (int j = 0; j < pairs; ++j)
+            items.push_back({TVFGP_VARIANT_ZMARCH2_TMA, sp[j], sp[j + 1], sr[j], sr[j + 1],
+                             static_cast<float>(m[2 * j]), static_cast<float>(m[2 * j + 1])});
+        if (single)
+            items.push_back({TVFGP_VARIANT_ZMARCH_TMA, p, p, sr[pairs], sr[pairs + 1],
+                             static_cast<float>(m[n - 1]), 0.0f});
+        return;
+    }
+    const int v = variant == TVFGP_VARIANT_ZMARCH2_TMA ? TVFGP_VARIANT_ZMARCH_TMA : variant;
+    for (int k = 0; k < n; ++k) {
+        const bool even = (k % 2) == 0;
+        items.push_back({v, p, p, even ? r : h->scratch, even ? h->scratch : r,
+                         static_cast<float>(m[k]), 0.0f});
+    }
+    *copy_back = (n % 2) == 1;
+}
+
+int launch_item(tvfgp_handle *h, const Item &it, const float *b, float lam, cudaStream_t st)
+{
+    const LaunchCfg c = item_cfg(h, it.kernel);
     KArgs k;
-    if (!fill_kargs(h, variant, a, k)) return TVFGP_ERR_CUDA;
+    if (!fill_item(h, it, b, lam, k)) return TVFGP_ERR_CUDA;
     cudaError_t e = cudaLaunchKernel(c.func, c.grid, c.block, k.ptrs, c.smem, st);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return from_cuda(e);
     }
     h->launches += 1;
-    h->last_variant = variant;
+    h->last_variant = it.kernel;
     return TVFGP_OK;
+}
+
+int launch_step(tvfgp_handle *h, int variant, const StepArgs &a, cudaStream_t st)
+{
+    const Item it{variant, a.p, a.p, a.rs, a.rd, a.m, 0.0f};
+    return launch_item(h, it, a.b, a.lam, st);
 }
 
 void destroy_graph(GraphEntry &g)
@@ -208,15 +292,11 @@ void destroy_graph(GraphEntry &g)
     g = GraphEntry();
 }
 
-// Kernel-node parameters of step k of a run.
-bool step_node_params(tvfgp_handle *h, int variant, const float *b, float *p, float *r, float lam,
-                      const std::vector<double> &m, int k, KArgs &ka, cudaKernelNodeParams &kp)
+bool node_params(tvfgp_handle *h, const Item &it, const float *b, float lam, KArgs &ka,
+                 cudaKernelNodeParams &kp)
 {
-    const bool even = (k % 2) == 0;
-    const StepArgs a = make_args(h, b, p, even ? r : h->scratch, even ? h->scratch : r, lam,
-                                 static_cast<float>(m[k]));
-    const bool ok = fill_kargs(h, variant, a, ka);
-    const LaunchCfg c = step_cfg(h, variant);
+    const bool ok = fill_item(h, it, b, lam, ka);
+    const LaunchCfg c = item_cfg(h, it.kernel);
     kp.func = const_cast<void *>(c.func);
     kp.gridDim = c.grid;
     kp.blockDim = c.block;
@@ -227,17 +307,17 @@ bool step_node_params(tvfgp_handle *h, int variant, const float *b, float *p, fl
 }
 
 int build_graph(tvfgp_handle *h, GraphEntry &g, int variant, const float *b, float *p, float *r,
-                float lam, int nsteps, double t0, const std::vector<double> &m)
+                float lam, int nsteps, double t0, const std::vector<Item> &items, bool copy_back)
 {
     destroy_graph(g);
     cudaError_t e = cudaGraphCreate(&g.graph, 0);
     if (e != cudaSuccess) return from_cuda(e);
     cudaGraphNode_t prev = nullptr;
-    g.knodes.resize(nsteps);
-    for (int k = 0; k < nsteps; ++k) {
+    g.knodes.resize(items.size());
+    for (size_t k = 0; k < items.size(); ++k) {
         KArgs ka;
         cudaKernelNodeParams kp;
-        if (!step_node_params(h, variant, b, p, r, lam, m, k, ka, kp)) {
+        if (!node_params(h, items[k], b, lam, ka, kp)) {
             e = cudaErrorInvalidValue;
             break;
         }
@@ -245,7 +325,7 @@ int build_graph(tvfgp_handle *h, GraphEntry &g, int variant, const float *b, flo
         if (e != cudaSuccess) break;
         prev = g.knodes[k];
     }
-    if (e == cudaSuccess && (nsteps % 2) == 1)
+    if (e == cudaSuccess && copy_back)
         e = cudaGraphAddMemcpyNode1D(&g.cnode, g.graph, &prev, 1, r, h->scratch,
                                      sizeof(float) * 3 * static_cast<size_t>(h->N),
                                      cudaMemcpyDeviceToDevice);
@@ -266,13 +346,13 @@ int build_graph(tvfgp_handle *h, GraphEntry &g, int variant, const float *b, flo
 }
 
 int update_graph(tvfgp_handle *h, GraphEntry &g, const float *b, float *p, float *r, float lam,
-                 double t0, const std::vector<double> &m)
+                 double t0, const std::vector<Item> &items)
 {
     cudaError_t e = cudaSuccess;
-    for (int k = 0; k < g.nsteps && e == cudaSuccess; ++k) {
+    for (size_t k = 0; k < items.size() && e == cudaSuccess; ++k) {
         KArgs ka;
         cudaKernelNodeParams kp;
-        if (!step_node_params(h, g.variant, b, p, r, lam, m, k, ka, kp)) {
+        if (!node_params(h, items[k], b, lam, ka, kp)) {
             e = cudaErrorInvalidValue;
             break;
         }
@@ -295,7 +375,8 @@ int update_graph(tvfgp_handle *h, GraphEntry &g, const float *b, float *p, float
 }
 
 int run_graph(tvfgp_handle *h, int variant, const float *b, float *p, float *r, float lam,
-              int nsteps, double t0, const std::vector<double> &m, cudaStream_t st)
+              int nsteps, double t0, const std::vector<Item> &items, bool copy_back,
+              cudaStream_t st)
 {
     GraphEntry *g = nullptr;
     for (auto &e : h->graphs)
@@ -306,9 +387,9 @@ int run_graph(tvfgp_handle *h, int variant, const float *b, float *p, float *r, 
         for (auto &e : h->graphs)
             if (!e.exec || e.use < victim->use) victim = &e;
         g = victim;
-        rc = build_graph(h, *g, variant, b, p, r, lam, nsteps, t0, m);
+        rc = build_graph(h, *g, variant, b, p, r, lam, nsteps, t0, items, copy_back);
     } else if (g->b != b || g->p != p || g->r != r || g->lam != lam || g->t0 != t0) {
-        rc = update_graph(h, *g, b, p, r, lam, t0, m);
+        rc = update_graph(h, *g, b, p, r, lam, t0, items);
     }
     if (rc != TVFGP_OK) return rc;
     g->use = ++h->graph_clock;
@@ -317,8 +398,22 @@ int run_graph(tvfgp_handle *h, int variant, const float *b, float *p, float *r, 
         cudaGetLastError();
         return from_cuda(e);
     }
-    h->launches += nsteps;
-    h->last_variant = variant;
+    h->launches += static_cast<long long>(items.size());
+    h->last_variant = items.empty() ? variant : items.front().kernel;
+    return TVFGP_OK;
+}
+
+// The two extra buffer sets of two-step runs (p twice, r once more; the
+// handle's scratch is the other r).
+int ensure_pair_scratch(tvfgp_handle *h)
+{
+    if (h->pair_scratch) return TVFGP_OK;
+    cudaError_t e = cudaMalloc(&h->pair_scratch, sizeof(float) * 9 * static_cast<size_t>(h->N));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        h->pair_scratch = nullptr;
+        return from_cuda(e);
+    }
     return TVFGP_OK;
 }
 
@@ -361,9 +456,11 @@ int tvfgp_create_ex(int nx, int ny, int nz, int variant, unsigned flags, tvfgp_t
     *out = nullptr;
     if (nx < 1 || ny < 1 || nz < 1 || nx > 65535 || ny > 65535 || nz > 65535) return TVFGP_ERR_ARG;
     if (static_cast<long long>(nx) * ny * (static_cast<long long>(nz) + 1) > INT_MAX) return TVFGP_ERR_ARG;
-    if (variant < TVFGP_VARIANT_AUTO || variant > TVFGP_VARIANT_ZMARCH_TMA || flags != 0)
+    if (variant < TVFGP_VARIANT_AUTO || variant > TVFGP_VARIANT_ZMARCH2_TMA || flags != 0)
         return TVFGP_ERR_ARG;
-    if (variant == TVFGP_VARIANT_ZMARCH_TMA && !zmarch_available()) return TVFGP_ERR_UNSUPPORTED;
+    if ((variant == TVFGP_VARIANT_ZMARCH_TMA || variant == TVFGP_VARIANT_ZMARCH2_TMA) &&
+        !zmarch_available())
+        return TVFGP_ERR_UNSUPPORTED;
     tvfgp_handle *h = new (std::nothrow) tvfgp_handle();
     if (h == nullptr) return TVFGP_ERR_OOM;
     h->magic = kMagic;
@@ -377,17 +474,24 @@ int tvfgp_create_ex(int nx, int ny, int nz, int variant, unsigned flags, tvfgp_t
     h->launches = 0;
     h->graph_clock = 0;
     h->scratch = nullptr;
+    h->pair_scratch = nullptr;
     h->d_err = nullptr;
     cudaError_t e = cudaMalloc(&h->scratch, sizeof(float) * 3 * static_cast<size_t>(h->N));
     if (e == cudaSuccess) e = cudaMalloc(&h->d_err, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(int));
     if (e == cudaSuccess) {
-        const int rc = zmarch_plan(nx, ny, nz, &h->zplan);
-        if (rc != TVFGP_OK) e = cudaErrorInvalidValue;
+        if (zmarch_plan(nx, ny, nz, &h->zplan) != TVFGP_OK ||
+            zmarch2_plan(nx, ny, nz, &h->z2plan) != TVFGP_OK)
+            e = cudaErrorInvalidValue;
     }
+    const int want_pairs = variant == TVFGP_VARIANT_ZMARCH2_TMA ||
+                           (variant == TVFGP_VARIANT_AUTO && kAutoVariant == TVFGP_VARIANT_ZMARCH2_TMA);
+    if (e == cudaSuccess && want_pairs && nx % 4 == 0 && ensure_pair_scratch(h) != TVFGP_OK)
+        e = cudaErrorMemoryAllocation;
     if (e != cudaSuccess) {
         cudaGetLastError();
         cudaFree(h->scratch);
+        cudaFree(h->pair_scratch);
         cudaFree(h->d_err);
         h->magic = 0;
         delete h;
@@ -408,6 +512,7 @@ int tvfgp_destroy(tvfgp_t h)
     if (!valid(h)) return TVFGP_ERR_ARG;
     for (auto &g : h->graphs) destroy_graph(g);
     cudaFree(h->scratch);
+    cudaFree(h->pair_scratch);
     cudaFree(h->d_err);
     h->magic = 0;
     delete h;
@@ -416,9 +521,17 @@ int tvfgp_destroy(tvfgp_t h)
 
 int tvfgp_set_variant(tvfgp_t h, int variant)
 {
-    if (!valid(h) || variant < TVFGP_VARIANT_AUTO || variant > TVFGP_VARIANT_ZMARCH_TMA)
+    if (!valid(h) || variant < TVFGP_VARIANT_AUTO || variant > TVFGP_VARIANT_ZMARCH2_TMA)
         return TVFGP_ERR_ARG;
-    if (variant == TVFGP_VARIANT_ZMARCH_TMA && !zmarch_available()) return TVFGP_ERR_UNSUPPORTED;
+    if ((variant == TVFGP_VARIANT_ZMARCH_TMA || variant == TVFGP_VARIANT_ZMARCH2_TMA) &&
+        !zmarch_available())
+        return TVFGP_ERR_UNSUPPORTED;
+    const int want_pairs = variant == TVFGP_VARIANT_ZMARCH2_TMA ||
+                           (variant == TVFGP_VARIANT_AUTO && kAutoVariant == TVFGP_VARIANT_ZMARCH2_TMA);
+    if (want_pairs && h->nx % 4 == 0) {
+        const int rc = ensure_pair_scratch(h);
+        if (rc != TVFGP_OK) return rc;
+    }
     h->variant = variant;
     return TVFGP_OK;
 }
@@ -450,7 +563,8 @@ int tvfgp_step(tvfgp_t h, const float *b, float *p, const float *r_src, float *r
         return TVFGP_ERR_ARG;
     const bool vec_ok = (h->nx % 4 == 0) && aligned16(b) && aligned16(p) && aligned16(r_src) &&
                         aligned16(r_dst);
-    const int variant = resolve_variant(h, h->variant, vec_ok);
+    int variant = resolve_variant(h, h->variant, vec_ok);
+    if (variant == TVFGP_VARIANT_ZMARCH2_TMA) variant = TVFGP_VARIANT_ZMARCH_TMA;   // one step only
     return launch_step(h, variant, make_args(h, b, p, r_src, r_dst, lambda, m),
                        reinterpret_cast<cudaStream_t>(stream));
 }
@@ -468,6 +582,10 @@ int tvfgp_run(tvfgp_t h, const float *b, float *p, float *r, float lambda, int n
         overlap(b, v, h->scratch, 3 * v) || overlap(p, 3 * v, h->scratch, 3 * v) ||
         overlap(r, 3 * v, h->scratch, 3 * v))
         return TVFGP_ERR_ARG;
+    if (h->pair_scratch && (overlap(b, v, h->pair_scratch, 9 * v) ||
+                            overlap(p, 3 * v, h->pair_scratch, 9 * v) ||
+                            overlap(r, 3 * v, h->pair_scratch, 9 * v)))
+        return TVFGP_ERR_ARG;
     std::vector<double> m(static_cast<size_t>(nsteps));
     double tf = t0;
     tvfgp_momentum(t0, nsteps, m.data(), &tf);
@@ -477,18 +595,16 @@ int tvfgp_run(tvfgp_t h, const float *b, float *p, float *r, float lambda, int n
     }
     const bool vec_ok = (h->nx % 4 == 0) && aligned16(b) && aligned16(p) && aligned16(r);
     const int variant = resolve_variant(h, h->variant, vec_ok);
+    std::vector<Item> items;
+    bool copy_back = false;
+    plan_run(h, variant, p, r, m, items, &copy_back);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (h->graph_on) {
-        rc = run_graph(h, variant, b, p, r, lambda, nsteps, t0, m, st);
+        rc = run_graph(h, variant, b, p, r, lambda, nsteps, t0, items, copy_back, st);
     } else {
-        for (int k = 0; k < nsteps && rc == TVFGP_OK; ++k) {
-            const bool even = (k % 2) == 0;
-            rc = launch_step(h, variant,
-                             make_args(h, b, p, even ? r : h->scratch, even ? h->scratch : r, lambda,
-                                       static_cast<float>(m[k])),
-                             st);
-        }
-        if (rc == TVFGP_OK && (nsteps % 2) == 1) {
+        for (size_t k = 0; k < items.size() && rc == TVFGP_OK; ++k)
+            rc = launch_item(h, items[k], b, lambda, st);
+        if (rc == TVFGP_OK && copy_back) {
             cudaError_t e = cudaMemcpyAsync(r, h->scratch, 3 * v, cudaMemcpyDeviceToDevice, st);
             if (e != cudaSuccess) {
                 cudaGetLastError();
@@ -496,7 +612,10 @@ int tvfgp_run(tvfgp_t h, const float *b, float *p, float *r, float lambda, int n
             }
         }
     }
-    if (rc == TVFGP_OK && t_final) *t_final = tf;
+    if (rc == TVFGP_OK) {
+        h->last_variant = items.front().kernel;
+        if (t_final) *t_final = tf;
+    }
     return rc;
 }
 

@@ -76,10 +76,17 @@ enum tvfgp_variant {
                                     three upper neighbours, carried along z in registers.
                                     Needs nx % 4 == 0 and 16-byte aligned pointers. */
     TVFGP_VARIANT_SCALAR = 2,    /* one voxel per thread; any shape and alignment */
-    TVFGP_VARIANT_ZMARCH_TMA = 3 /* x-y tile marching along z, planes of b and r staged in
-                                    shared memory by TMA; same requirements as FUSED (else
-                                    the call falls back to SCALAR); TVFGP_ERR_UNSUPPORTED at
-                                    create/set time if the driver lacks the TMA encoder */
+    TVFGP_VARIANT_ZMARCH_TMA = 3, /* x-y tile marching along z, planes of b, r and p staged
+                                     in shared memory by TMA; same requirements as FUSED (else
+                                     the call falls back to SCALAR); TVFGP_ERR_UNSUPPORTED at
+                                     create/set time if the driver lacks the TMA encoder */
+    TVFGP_VARIANT_ZMARCH2_TMA = 4 /* two FGP steps per pass over memory (13 volumes per two
+                                     steps instead of per step), same results; used by
+                                     tvfgp_run for nsteps >= 4 (a last odd step and shorter
+                                     runs use ZMARCH_TMA).  The handle then owns two more
+                                     buffer sets (9*nx*ny*nz more floats), allocated by
+                                     tvfgp_create_ex / tvfgp_set_variant.  Same requirements
+                                     as ZMARCH_TMA. */
 };
 
 /* Create a handle for an nx x ny x nz volume on the current CUDA device.

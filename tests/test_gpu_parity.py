@@ -21,7 +21,7 @@ def T():
     return tvfgp
 
 
-VEC_VARIANTS = ["fused", "zmarch", "scalar"]
+VEC_VARIANTS = ["fused", "zmarch", "zmarch2", "scalar"]
 
 
 # ---------------------------------------------------------------------------
@@ -35,7 +35,8 @@ def test_small_workloads_exact(T, key, variant):
     b, *gpu, launched = run_workload_gpu(w, variant)
     ref = run_workload_oracle(w)
     assert_parity(gpu, ref[1:], float(np.abs(b).max()), exact=True, what=key)
-    assert launched == w.total_steps + 2
+    per_outer = w.steps // 2 + w.steps % 2 if (variant == "zmarch2" and w.steps >= 4) else w.steps
+    assert launched == w.outers * per_outer + 2
 
 
 def test_256_warm_started_outers_graph(T):
@@ -77,7 +78,7 @@ def test_odd_shapes_warm_start(T, shape, variant):
     p0 = synth.random_dual(shape, seed, scale=0.4)
     r0 = synth.random_dual(shape, seed + 1, scale=0.6)
     lam = 0.07
-    for nsteps in (0, 1, 2, 3, 7):
+    for nsteps in ((0, 1, 2, 3, 4, 5, 6, 7, 10) if variant == "zmarch2" else (0, 1, 2, 3, 7)):
         p, r = dev(p0), dev(r0)
         bd = dev(b)
         with T.Tvfgp(nx, ny, nz, variant) as h:
@@ -87,6 +88,8 @@ def test_odd_shapes_warm_start(T, shape, variant):
             if nsteps:
                 if variant == "scalar" or nx % 4:
                     want = T.TVFGP_VARIANT_SCALAR
+                elif variant == "zmarch2" and nsteps < 4:
+                    want = T.TVFGP_VARIANT_ZMARCH_TMA      # two-step launches from 4 steps on
                 else:
                     want = T.VARIANTS[variant]
                 assert h.last_variant == want
