@@ -15,8 +15,8 @@
 //   q_a = r_a + g_a*s,  s = 1/(12 lambda) rounded to float once
 //   |q| = sqrt((q0*q0 + q1*q1) + q2*q2);  p'_a = q_a / max(1, |q|)
 //   r_a = p'_a + m*(p'_a - p_a)
-// Dividing by max(1,|q|) equals q itself when |q| <= 1, so the division is
-// only issued when |q| > 1 (IEEE x/1 == x).
+// Dividing by max(1,|q|) equals q itself when |q| <= 1, so the square root
+// and the division are only issued when |q|^2 > 1 (IEEE x/1 == x).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -72,8 +72,11 @@ __device__ __forceinline__ void dual_update(float &r0, float &r1, float &r2,
     float q1 = __fadd_rn(r1, __fmul_rn(g1, s));
     float q2 = __fadd_rn(r2, __fmul_rn(g2, s));
     const float nn = __fadd_rn(__fadd_rn(__fmul_rn(q0, q0), __fmul_rn(q1, q1)), __fmul_rn(q2, q2));
-    const float n = __fsqrt_rn(nn);
-    if (n > 1.0f) {
+    // max(1, |q|) > 1 exactly when |q|^2 > 1 (a correctly rounded square root
+    // is monotone and sqrt(1) = 1); where |q|^2 > 1 but |q| rounds to 1, the
+    // division by 1 leaves q unchanged, as the definition does.
+    if (nn > 1.0f) {
+        const float n = __fsqrt_rn(nn);
         q0 = __fdiv_rn(q0, n);
         q1 = __fdiv_rn(q1, n);
         q2 = __fdiv_rn(q2, n);

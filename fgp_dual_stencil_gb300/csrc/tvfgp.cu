@@ -40,7 +40,7 @@ constexpr int kFusedZC = TVFGP_FUSED_ZC;
 constexpr int kPrimalBY = 8;
 
 // The default vector variant chosen by AUTO.
-constexpr int kAutoVariant = TVFGP_VARIANT_ZMARCH_TMA;
+constexpr int kAutoVariant = TVFGP_VARIANT_ZMARCH2_TMA;
 
 struct LaunchCfg {
     const void *func;

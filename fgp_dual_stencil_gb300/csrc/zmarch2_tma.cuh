@@ -16,12 +16,19 @@
 //
 //   at iteration q:
 //     A  z^k     of plane q+1 on x0-1..x0+TX+1, y0-1..y0+TY+1   (staged b, r^k)
-//     B  step k  of plane q   on x0-1..x0+TX,   y0-1..y0+TY     (-> r^{k+1}, p^{k+1} in shared memory)
+//     B  step k  of plane q   on x0-1..x0+TX,   y0-1..y0+TY     (-> r^{k+1} shared, p^{k+1} registers)
+//     -- barrier
 //     C  z^{k+1} of plane q   on x0..x0+TX,     y0..y0+TY       (b, r^{k+1})
 //     D  step k+1 of plane q-1 on the tile                      (-> p^{k+2}, r^{k+2} in HBM)
+//     -- barrier
 //
-// with a barrier after A, B and C.  Voxels of the ring that lie outside the
-// volume get r^{k+1} = 0: that is the r(-1) = 0 boundary step k+1 sees.
+// Each thread owns one quad (four x voxels) and runs A and B, and C and D,
+// on it: the voxel's own z^k, z^{k+1} and p^{k+1} stay in its registers from
+// the phase that makes them to the phase that uses them, and only the x+1 /
+// y+1 neighbours' z and the r^{k+1} halo go through shared memory (rings of
+// two planes), so two barriers per plane suffice.  Voxels of the ring that
+// lie outside the volume get r^{k+1} = 0: that is the r(-1) = 0 boundary step
+// k+1 sees.
 // Every value is computed by the same expressions, in the same order, as in
 // the one-step kernels, so the result is bitwise that of two single steps.
 //
@@ -42,21 +49,17 @@ namespace tvfgp {
 #define TVFGP_Z2_TX 32
 #endif
 #ifndef TVFGP_Z2_TY
-#define TVFGP_Z2_TY 16
-#endif
-#ifndef TVFGP_Z2_THREADS
-#define TVFGP_Z2_THREADS 256
+#define TVFGP_Z2_TY 12
 #endif
 #ifndef TVFGP_Z2_STAGES
 #define TVFGP_Z2_STAGES 3
 #endif
 #ifndef TVFGP_Z2_MINB
-#define TVFGP_Z2_MINB 2
+#define TVFGP_Z2_MINB 3
 #endif
 
 constexpr int Z2_TX = TVFGP_Z2_TX;          // output tile width
 constexpr int Z2_TY = TVFGP_Z2_TY;          // output tile height
-constexpr int Z2_THREADS = TVFGP_Z2_THREADS;
 constexpr int Z2_STAGES = TVFGP_Z2_STAGES;
 
 // staged boxes: all start at x0-4 (a 16-byte aligned column) and are TX+8 wide
@@ -78,23 +81,40 @@ constexpr int Z2_STAGE_STRIDE = Z2_OFF_P2 + zm_round128(Z2_BYTES_P);
 constexpr int Z2_TX_BR = Z2_BYTES_B + 3 * Z2_BYTES_R;
 constexpr int Z2_TX_ALL = Z2_TX_BR + 3 * Z2_BYTES_P;
 
-// regions (local coordinates lx = x - x0, ly = y - y0)
-constexpr int Z2_ZKW = Z2_TX + 3, Z2_ZKH = Z2_TY + 3;     // z^k:     lx -1..TX+1, ly -1..TY+1
-constexpr int Z2_UKW = Z2_TX + 2, Z2_UKH = Z2_TY + 2;     // step k:  lx -1..TX,   ly -1..TY
-constexpr int Z2_Z1W = Z2_TX + 1, Z2_Z1H = Z2_TY + 1;     // z^{k+1}: lx  0..TX,   ly  0..TY
-constexpr int Z2_PITCH = Z2_TX + 4;                       // row pitch of the shared rings
+// Regions (local coordinates lx = x - x0, ly = y - y0), in quads of four x
+// voxels so that shared memory moves float4s.  Each region covers what the
+// next phase needs (and a few columns more, which nothing reads):
+//   z^k      lx -4..TX+3 (needed -1..TX+1),  ly -1..TY+1
+//   step k   lx -4..TX+3 (needed -1..TX),    ly -1..TY
+//   z^{k+1}  lx  0..TX+3 (needed  0..TX),    ly  0..TY
+//   step k+1 lx  0..TX-1,                    ly  0..TY-1
+constexpr int Z2_QA = Z2_BW / 4;                          // quads per row, z^k and step k
+constexpr int Z2_QC = (Z2_TX + 4) / 4;                    // quads per row, z^{k+1}
+constexpr int Z2_QD = Z2_TX / 4;                          // quads per row, step k+1
+constexpr int Z2_TASKS_A = Z2_QA * (Z2_TY + 3);
+constexpr int Z2_TASKS_B = Z2_QA * (Z2_TY + 2);
+constexpr int Z2_TASKS_C = Z2_QC * (Z2_TY + 1);
+constexpr int Z2_TASKS_D = Z2_QD * Z2_TY;
+// One thread per z^k quad; the threads of the tile's quads also run z^{k+1}
+// and step k+1 on them, and the quads of z^{k+1}'s x+1 column and y+1 row go
+// to the threads past the step-k region.
+constexpr int Z2_THREADS = (Z2_TASKS_A + 31) / 32 * 32;
+constexpr int Z2_HALO_C = (Z2_TY + 1) + Z2_QD;            // z^{k+1} quads outside the tile
+constexpr int Z2_HALO_T = Z2_THREADS - Z2_TASKS_B;        // threads that take them
+static_assert(Z2_TASKS_B <= Z2_THREADS && Z2_HALO_T > 0, "thread roles");
 
 // shared rings, two slots each (a plane is written two iterations after the
-// slot was last read, with a barrier in between)
-constexpr int Z2_RING_ZK = Z2_ZKH * Z2_PITCH;             // floats per slot
-constexpr int Z2_RING_MR = 3 * Z2_UKH * Z2_PITCH;
-constexpr int Z2_RING_MP = 3 * Z2_TY * Z2_TX;
-constexpr int Z2_RING_Z1 = Z2_Z1H * Z2_PITCH;
+// slot was last read, with a barrier in between); pitches in floats
+constexpr int Z2_PK = Z2_BW;                              // z^k and r^{k+1}: columns lx+4
+constexpr int Z2_P1 = Z2_TX + 4;                          // z^{k+1}: columns lx
+constexpr int Z2_RING_ZK = (Z2_TY + 3) * Z2_PK;           // floats per slot
+constexpr int Z2_MR_COMP = (Z2_TY + 2) * Z2_PK;
+constexpr int Z2_RING_MR = 3 * Z2_MR_COMP;
+constexpr int Z2_RING_Z1 = (Z2_TY + 1) * Z2_P1;
 constexpr int Z2_OFF_PREV = Z2_STAGES * Z2_STAGE_STRIDE;  // r2^k of the plane below the first
 constexpr int Z2_OFF_ZK = zm_round128(Z2_OFF_PREV + Z2_BYTES_R);
 constexpr int Z2_OFF_MR = zm_round128(Z2_OFF_ZK + 2 * Z2_RING_ZK * 4);
-constexpr int Z2_OFF_MP = zm_round128(Z2_OFF_MR + 2 * Z2_RING_MR * 4);
-constexpr int Z2_OFF_Z1 = zm_round128(Z2_OFF_MP + 2 * Z2_RING_MP * 4);
+constexpr int Z2_OFF_Z1 = zm_round128(Z2_OFF_MR + 2 * Z2_RING_MR * 4);
 constexpr int Z2_OFF_BAR = zm_round128(Z2_OFF_Z1 + 2 * Z2_RING_Z1 * 4);
 constexpr int Z2_OFF_FLAG = Z2_OFF_BAR + 8 * (Z2_STAGES + 1);
 constexpr int Z2_SMEM = Z2_OFF_FLAG + 16 + 128;
@@ -122,7 +142,6 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Z2_OFF_FLAG);
     float *ZK = reinterpret_cast<float *>(smem + Z2_OFF_ZK);
     float *MR = reinterpret_cast<float *>(smem + Z2_OFF_MR);
-    float *MP = reinterpret_cast<float *>(smem + Z2_OFF_MP);
     float *Z1 = reinterpret_cast<float *>(smem + Z2_OFF_Z1);
 
     const int nx = za.nx, ny = za.ny, nz = za.nz;
@@ -162,40 +181,39 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
         }
     };
 
-    // element accessors of a staged plane (local coordinates)
-    auto sB = [](const unsigned char *st, int lx, int ly) {
-        return reinterpret_cast<const float *>(st + Z2_OFF_B)[(ly + 1) * Z2_BW + lx + 4];
-    };
-    auto sR = [](const unsigned char *st, int off, int lx, int ly) {
-        return reinterpret_cast<const float *>(st + off)[(ly + 2) * Z2_BW + lx + 4];
-    };
-    auto sP = [](const unsigned char *st, int off, int lx, int ly) {
-        return reinterpret_cast<const float *>(st + off)[(ly + 1) * Z2_BW + lx + 4];
-    };
-    auto zk = [&](int q, int lx, int ly) -> float & {
-        return ZK[(q & 1) * Z2_RING_ZK + (ly + 1) * Z2_PITCH + lx + 1];
-    };
-    auto mr = [&](int q, int a, int lx, int ly) -> float & {
-        return MR[(q & 1) * Z2_RING_MR + (a * Z2_UKH + ly + 1) * Z2_PITCH + lx + 1];
-    };
-    auto mp = [&](int q, int a, int lx, int ly) -> float & {
-        return MP[(q & 1) * Z2_RING_MP + (a * Z2_TY + ly) * Z2_TX + lx];
-    };
-    auto z1 = [&](int q, int lx, int ly) -> float & {
-        return Z1[(q & 1) * Z2_RING_Z1 + ly * Z2_PITCH + lx];
-    };
+    auto F = [](const unsigned char *st, int off) { return reinterpret_cast<const float *>(st + off); };
+    auto zkp = [&](int q) { return ZK + (q & 1) * Z2_RING_ZK; };
+    auto mrp = [&](int q, int a) { return MR + (q & 1) * Z2_RING_MR + a * Z2_MR_COMP; };
+    auto z1p = [&](int q) { return Z1 + (q & 1) * Z2_RING_Z1; };
 
-    // z^k of plane q on the grown region; r2lo_st: the staged plane q-1 (or
-    // the r2 buffer of the plane below the first), nullptr at plane 0
-    auto zk_plane = [&](int q, const unsigned char *st, const float *r2lo) {
-        for (int idx = tid; idx < Z2_ZKW * Z2_ZKH; idx += Z2_THREADS) {
-            const int lx = idx % Z2_ZKW - 1, ly = idx / Z2_ZKW - 1;
-            const float d0 = __fsub_rn(sR(st, Z2_OFF_R0, lx, ly), sR(st, Z2_OFF_R0, lx - 1, ly));
-            const float d1 = __fsub_rn(sR(st, Z2_OFF_R1, lx, ly), sR(st, Z2_OFF_R1, lx, ly - 1));
-            const float lo = r2lo ? r2lo[(ly + 2) * Z2_BW + lx + 4] : 0.0f;
-            const float d2 = __fsub_rn(sR(st, Z2_OFF_R2, lx, ly), lo);
-            zk(q, lx, ly) = zval(sB(st, lx, ly), lam, d0, d1, d2);
-        }
+    // this thread's quad in the z^k / step-k grid (c = lx + 4, row = ly + 1)
+    const int my_c = 4 * (tid % Z2_QA), my_row = tid / Z2_QA;
+    const bool doA = tid < Z2_TASKS_A;
+    const bool doB = tid < Z2_TASKS_B;
+    const bool my_tile = doB && my_c >= 4 && my_c < Z2_TX + 4 && my_row >= 1 && my_row <= Z2_TY;
+
+    // z^k of plane q for this thread's quad, from the staged plane st and the
+    // r2 of the plane below (lo: a staged r2 box, or nullptr at plane 0);
+    // stored for the neighbours and returned
+    auto zk_quad = [&](int q, const unsigned char *st, const float *lo) {
+        const int rr = (my_row + 1) * Z2_BW + my_c;                  // r box row of ly
+        const float *R0 = F(st, Z2_OFF_R0), *R1 = F(st, Z2_OFF_R1);
+        const float left = my_c > 0 ? R0[rr - 1] : 0.0f;
+        const float4 r2lo = lo ? lds4(lo + rr) : f4zero();
+        const float4 Z = zquad(lds4(F(st, Z2_OFF_B) + my_row * Z2_BW + my_c), lds4(R0 + rr), lds4(R1 + rr),
+                               lds4(F(st, Z2_OFF_R2) + rr), left, lds4(R1 + rr - Z2_BW), r2lo, lam);
+        *reinterpret_cast<float4 *>(zkp(q) + my_row * Z2_PK + my_c) = Z;
+        return Z;
+    };
+    // z^{k+1} of plane q for the quad at (c = lx, ly), stored and returned
+    auto z1_quad = [&](int q, int c, int ly) {
+        const float *M0 = mrp(q, 0), *M1 = mrp(q, 1), *M2 = mrp(q, 2);
+        const int mo = (ly + 1) * Z2_PK + c + 4;                     // r^{k+1} at (lx = c, ly)
+        const float4 Z = zquad(lds4(F(stage(q), Z2_OFF_B) + (ly + 1) * Z2_BW + c + 4), lds4(M0 + mo),
+                               lds4(M1 + mo), lds4(M2 + mo), M0[mo - 1], lds4(M1 + mo - Z2_PK),
+                               q > 0 ? lds4(mrp(q - 1, 2) + mo) : f4zero(), lam);
+        *reinterpret_cast<float4 *>(z1p(q) + ly * Z2_P1 + c) = Z;
+        return Z;
     };
 
     if (tid == 0) {
@@ -207,14 +225,15 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     }
     int next_issue = f + Z2_STAGES;
 
+    float4 ZKc = f4zero();                      // z^k of this quad, current plane
     // prologue: z^k of plane f
     {
         bool ok = true;
         if (f > 0) ok = mbar_wait_tma(&bars[Z2_STAGES], 0);
         ok = ok && mbar_wait_tma(&bars[slot(f)], parity(f));
         if (ok) {
-            const float *lo = f > 0 ? reinterpret_cast<const float *>(smem + Z2_OFF_PREV) : nullptr;
-            zk_plane(f, stage(f), lo);
+            if (doA)
+                ZKc = zk_quad(f, stage(f), f > 0 ? reinterpret_cast<const float *>(smem + Z2_OFF_PREV) : nullptr);
         } else {
             *abort_flag = 1;
         }
@@ -223,97 +242,130 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
 
     float *p0d = za.p_dst, *p1d = za.p_dst + za.N, *p2d = za.p_dst + 2 * za.N;
     float *r0d = za.r_dst, *r1d = za.r_dst + za.N, *r2d = za.r_dst + 2 * za.N;
+    float4 cP0 = f4zero(), cP1 = f4zero(), cP2 = f4zero();   // p^{k+1} of plane q-1 (tile quads)
+    float4 Z1c = f4zero();                                    // z^{k+1} of plane q-1 (tile quads)
 
     int qlast = f - 1;                          // planes <= qlast+1 were waited for
     for (int q = f; q <= ze && *abort_flag == 0; ++q) {
         qlast = q;
-        // A: z^k of plane q+1
+        // ---- A: z^k of plane q+1 -------------------------------------------
+        float4 ZKn = f4zero();
         if (q + 1 <= last) {
             if (mbar_wait_tma(&bars[slot(q + 1)], parity(q + 1))) {
-                const float *lo = reinterpret_cast<const float *>(stage(q) + Z2_OFF_R2);
-                zk_plane(q + 1, stage(q + 1), lo);
+                if (doA) ZKn = zk_quad(q + 1, stage(q + 1), F(stage(q), Z2_OFF_R2));
             } else {
                 *abort_flag = 1;
             }
         }
+        // ---- B: step k on plane q over the grown tile ----------------------
+        float4 nP0 = f4zero(), nP1 = f4zero(), nP2 = f4zero();
+        if (q <= uk_last && doB) {
+            const unsigned char *st = stage(q);
+            const bool hasZ = q + 1 < nz;
+            const float *Zq = zkp(q);
+            const int c = my_c, row = my_row;                        // row = ly + 1
+            const int ly = row - 1, lx = c - 4;
+            const int x = x0 + lx, y = y0 + ly;
+            const int zo = row * Z2_PK + c;
+            const float4 zc = ZKc;
+            const float zx = c + 4 < Z2_PK ? Zq[zo + 4] : 0.0f;
+            const float4 zy = lds4(Zq + zo + Z2_PK);
+            const float4 zz = hasZ ? ZKn : f4zero();
+            const int ro = (row + 1) * Z2_BW + c, po = row * Z2_BW + c;
+            float4 R0 = lds4(F(st, Z2_OFF_R0) + ro), R1 = lds4(F(st, Z2_OFF_R1) + ro),
+                   R2 = lds4(F(st, Z2_OFF_R2) + ro);
+            float4 P0 = lds4(F(st, Z2_OFF_P0) + po), P1 = lds4(F(st, Z2_OFF_P1) + po),
+                   P2 = lds4(F(st, Z2_OFF_P2) + po);
+            const bool yin = y >= 0 && y < ny;
+            const bool gy = y < ny - 1;
+            float *r0 = &R0.x, *r1 = &R1.x, *r2 = &R2.x, *p0 = &P0.x, *p1 = &P1.x, *p2 = &P2.x;
+            const float zcv[5] = {zc.x, zc.y, zc.z, zc.w, zx};
+            const float zyv[4] = {zy.x, zy.y, zy.z, zy.w};
+            const float zzv[4] = {zz.x, zz.y, zz.z, zz.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int xe = x + e;
+                if (yin && xe >= 0 && xe < nx) {
+                    const float g0 = (xe < nx - 1) ? __fsub_rn(zcv[e], zcv[e + 1]) : 0.0f;
+                    const float g1 = gy ? __fsub_rn(zcv[e], zyv[e]) : 0.0f;
+                    const float g2 = hasZ ? __fsub_rn(zcv[e], zzv[e]) : 0.0f;
+                    dual_update(r0[e], r1[e], r2[e], g0, g1, g2, p0[e], p1[e], p2[e], s, m0);
+                } else {
+                    r0[e] = r1[e] = r2[e] = 0.0f;            // the r(-1) = 0 boundary of step k+1
+                }
+            }
+            const int mo = row * Z2_PK + c;
+            *reinterpret_cast<float4 *>(mrp(q, 0) + mo) = R0;
+            *reinterpret_cast<float4 *>(mrp(q, 1) + mo) = R1;
+            *reinterpret_cast<float4 *>(mrp(q, 2) + mo) = R2;
+            nP0 = P0;
+            nP1 = P1;
+            nP2 = P2;
+        }
+        ZKc = ZKn;
         __syncthreads();
         if (*abort_flag) break;
 
-        // B: step k on plane q over the grown tile -> r^{k+1}, p^{k+1}
-        if (q <= uk_last) {
-            const unsigned char *st = stage(q);
-            const bool hasZ = q + 1 < nz;
-            for (int idx = tid; idx < Z2_UKW * Z2_UKH; idx += Z2_THREADS) {
-                const int lx = idx % Z2_UKW - 1, ly = idx / Z2_UKW - 1;
-                const int x = x0 + lx, y = y0 + ly;
-                float r0 = 0.0f, r1 = 0.0f, r2 = 0.0f;
-                float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f;
-                if (x >= 0 && x < nx && y >= 0 && y < ny) {
-                    const float zc = zk(q, lx, ly);
-                    const float g0 = (x < nx - 1) ? __fsub_rn(zc, zk(q, lx + 1, ly)) : 0.0f;
-                    const float g1 = (y < ny - 1) ? __fsub_rn(zc, zk(q, lx, ly + 1)) : 0.0f;
-                    const float g2 = hasZ ? __fsub_rn(zc, zk(q + 1, lx, ly)) : 0.0f;
-                    r0 = sR(st, Z2_OFF_R0, lx, ly);
-                    r1 = sR(st, Z2_OFF_R1, lx, ly);
-                    r2 = sR(st, Z2_OFF_R2, lx, ly);
-                    p0 = sP(st, Z2_OFF_P0, lx, ly);
-                    p1 = sP(st, Z2_OFF_P1, lx, ly);
-                    p2 = sP(st, Z2_OFF_P2, lx, ly);
-                    dual_update(r0, r1, r2, g0, g1, g2, p0, p1, p2, s, m0);
-                }
-                mr(q, 0, lx, ly) = r0;
-                mr(q, 1, lx, ly) = r1;
-                mr(q, 2, lx, ly) = r2;
-                if (lx >= 0 && lx < Z2_TX && ly >= 0 && ly < Z2_TY) {
-                    mp(q, 0, lx, ly) = p0;
-                    mp(q, 1, lx, ly) = p1;
-                    mp(q, 2, lx, ly) = p2;
-                }
-            }
-        }
-        __syncthreads();
-
-        // C: z^{k+1} of plane q on the tile plus its x+1 column and y+1 row
+        // ---- C: z^{k+1} of plane q on the tile, its x+1 column and y+1 row ---
+        float4 Z1n = f4zero();
         if (q >= z0 && q <= uk_last) {
-            const unsigned char *st = stage(q);
-            for (int idx = tid; idx < Z2_Z1W * Z2_Z1H; idx += Z2_THREADS) {
-                const int lx = idx % Z2_Z1W, ly = idx / Z2_Z1W;
-                const float d0 = __fsub_rn(mr(q, 0, lx, ly), mr(q, 0, lx - 1, ly));
-                const float d1 = __fsub_rn(mr(q, 1, lx, ly), mr(q, 1, lx, ly - 1));
-                const float d2 = __fsub_rn(mr(q, 2, lx, ly), q > 0 ? mr(q - 1, 2, lx, ly) : 0.0f);
-                z1(q, lx, ly) = zval(sB(st, lx, ly), lam, d0, d1, d2);
+            if (my_tile) Z1n = z1_quad(q, my_c - 4, my_row - 1);
+            for (int h = tid - Z2_TASKS_B; h >= 0 && h < Z2_HALO_C; h += Z2_HALO_T) {
+                if (h <= Z2_TY)
+                    z1_quad(q, Z2_TX, h);                            // x+1 column, rows 0..TY
+                else
+                    z1_quad(q, 4 * (h - Z2_TY - 1), Z2_TY);          // y+1 row
             }
         }
+        // ---- D: step k+1 on plane q-1 over the tile -> p^{k+2}, r^{k+2} -----
+        const int qd = q - 1;
+        if (my_tile && qd >= z0 && qd < ze) {
+            const int c = my_c - 4, ly = my_row - 1;
+            const int x = x0 + c, y = y0 + ly;
+            if (x < nx && y < ny) {
+                const bool hasZ = qd + 1 < nz;
+                const float *Zd = z1p(qd);
+                const int zo = ly * Z2_P1 + c;
+                const float4 zc = Z1c;
+                const float zx = Zd[zo + 4];
+                const float4 zy = lds4(Zd + zo + Z2_P1);
+                const float4 zz = hasZ ? Z1n : f4zero();
+                const int mo = (ly + 1) * Z2_PK + c + 4;
+                float4 R0 = lds4(mrp(qd, 0) + mo), R1 = lds4(mrp(qd, 1) + mo), R2 = lds4(mrp(qd, 2) + mo);
+                float4 P0 = cP0, P1 = cP1, P2 = cP2;
+                const bool gy = y < ny - 1;
+                float4 G1 = f4zero(), G2 = f4zero();
+                if (gy) {
+                    G1.x = __fsub_rn(zc.x, zy.x); G1.y = __fsub_rn(zc.y, zy.y);
+                    G1.z = __fsub_rn(zc.z, zy.z); G1.w = __fsub_rn(zc.w, zy.w);
+                }
+                if (hasZ) {
+                    G2.x = __fsub_rn(zc.x, zz.x); G2.y = __fsub_rn(zc.y, zz.y);
+                    G2.z = __fsub_rn(zc.z, zz.z); G2.w = __fsub_rn(zc.w, zz.w);
+                }
+                const float gx3 = (x + 3 < nx - 1) ? __fsub_rn(zc.w, zx) : 0.0f;
+                dual_update(R0.x, R1.x, R2.x, __fsub_rn(zc.x, zc.y), G1.x, G2.x, P0.x, P1.x, P2.x, s, m1);
+                dual_update(R0.y, R1.y, R2.y, __fsub_rn(zc.y, zc.z), G1.y, G2.y, P0.y, P1.y, P2.y, s, m1);
+                dual_update(R0.z, R1.z, R2.z, __fsub_rn(zc.z, zc.w), G1.z, G2.z, P0.z, P1.z, P2.z, s, m1);
+                dual_update(R0.w, R1.w, R2.w, gx3, G1.w, G2.w, P0.w, P1.w, P2.w, s, m1);
+                const long long i = x + (long long)nx * (y + (long long)ny * qd);
+                st4(p0d + i, P0);
+                st4(p1d + i, P1);
+                st4(p2d + i, P2);
+                st4(r0d + i, R0);
+                st4(r1d + i, R1);
+                st4(r2d + i, R2);
+            }
+        }
+        Z1c = Z1n;
+        cP0 = nP0;
+        cP1 = nP1;
+        cP2 = nP2;
         __syncthreads();
         // every read of plane q's stage is done: the slot takes the next plane
         if (tid == 0 && next_issue <= last && q <= uk_last) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             issue(next_issue++);
-        }
-
-        // D: step k+1 on plane q-1 over the tile -> p^{k+2}, r^{k+2} in HBM
-        const int qd = q - 1;
-        if (qd >= z0 && qd < ze) {
-            const bool hasZ = qd + 1 < nz;
-            for (int idx = tid; idx < Z2_TX * Z2_TY; idx += Z2_THREADS) {
-                const int lx = idx % Z2_TX, ly = idx / Z2_TX;
-                const int x = x0 + lx, y = y0 + ly;
-                if (x >= nx || y >= ny) continue;
-                const float zc = z1(qd, lx, ly);
-                const float g0 = (x < nx - 1) ? __fsub_rn(zc, z1(qd, lx + 1, ly)) : 0.0f;
-                const float g1 = (y < ny - 1) ? __fsub_rn(zc, z1(qd, lx, ly + 1)) : 0.0f;
-                const float g2 = hasZ ? __fsub_rn(zc, z1(qd + 1, lx, ly)) : 0.0f;
-                float r0 = mr(qd, 0, lx, ly), r1 = mr(qd, 1, lx, ly), r2 = mr(qd, 2, lx, ly);
-                float p0 = mp(qd, 0, lx, ly), p1 = mp(qd, 1, lx, ly), p2 = mp(qd, 2, lx, ly);
-                dual_update(r0, r1, r2, g0, g1, g2, p0, p1, p2, s, m1);
-                const long long i = x + (long long)nx * (y + (long long)ny * qd);
-                p0d[i] = p0;
-                p1d[i] = p1;
-                p2d[i] = p2;
-                r0d[i] = r0;
-                r1d[i] = r1;
-                r2d[i] = r2;
-            }
         }
     }
 

@@ -49,12 +49,13 @@ def test_256_warm_started_outers_graph(T):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("key", ["c4", "c5"])
-def test_large_workloads(T, key):
+@pytest.mark.parametrize("key,variant", [("c4", "auto"), ("c5", "auto"), ("c4", "zmarch2")])
+def test_large_workloads(T, key, variant):
     """The 512^3 workload in the configuration the bench times (AUTO variant,
-    graph replay), and the 1000x600x300 blob volume."""
+    graph replay), the 1000x600x300 blob volume, and 512^3 with two steps per
+    launch."""
     w = synth.WORKLOADS[key]
-    b, *gpu, _ = run_workload_gpu(w, "auto", graph=(key == "c4"))
+    b, *gpu, _ = run_workload_gpu(w, variant, graph=(key == "c4"))
     ref = run_workload_oracle(w)
     assert_parity(gpu, ref[1:], float(np.abs(b).max()), exact=False, what=key)
     # the result is still checked for exact equality, reported separately
