@@ -51,7 +51,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", default="c4", help="c1..c5 (default c4: 512^3)")
-    ap.add_argument("--variant", default="auto", choices=["auto", "fused", "scalar", "zmarch", "zmarch2"])
+    ap.add_argument("--variant", default="auto", choices=["auto", "fused", "scalar", "zmarch", "zmarch2", "separate"])
     ap.add_argument("--eager", action="store_true", help="launch eagerly instead of graph replay")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -269,7 +269,8 @@ def gpu_arm(args, world, rank, local_rank, dist):
     # step-kernel launches per run: two steps per launch for the two-step
     # kernel (a last odd step runs alone)
     pairs = variant_used == T.TVFGP_VARIANT_ZMARCH2_TMA and w.steps >= 4
-    launches_per_run = (w.steps // 2 + w.steps % 2) if pairs else w.steps
+    separate = variant_used == T.TVFGP_VARIANT_SEPARATE       # two launches, 18 volumes per step
+    launches_per_run = (w.steps // 2 + w.steps % 2) if pairs else (2 * w.steps if separate else w.steps)
     steps_per_launch = w.steps / launches_per_run
     launch_s = run_ms / 1e3 / (K * launches_per_run)
     step_s = run_ms / 1e3 / (K * w.steps)
@@ -278,11 +279,12 @@ def gpu_arm(args, world, rank, local_rank, dist):
     peak, peak_kind = hbm_peak()
     # algorithmic bytes: 52 per voxel and FGP step, times the voxel-steps one
     # launch processes
-    alg_bytes = BYTES_PER_VOXEL_STEP * N * steps_per_launch
+    alg_bytes = (72 if separate else BYTES_PER_VOXEL_STEP) * N * steps_per_launch
     achieved = alg_bytes / launch_s / 1e9
     kname = {T.TVFGP_VARIANT_FUSED: "fgp_step_fused4", T.TVFGP_VARIANT_SCALAR: "fgp_step_scalar",
              T.TVFGP_VARIANT_ZMARCH_TMA: "fgp_step_zmarch_tma",
-             T.TVFGP_VARIANT_ZMARCH2_TMA: "fgp_step2_zmarch_tma"}.get(variant_used, "?")
+             T.TVFGP_VARIANT_ZMARCH2_TMA: "fgp_step2_zmarch_tma",
+             T.TVFGP_VARIANT_SEPARATE: "primal_vec4 + dual_from_z_vec4"}.get(variant_used, "?")
     traffic = ncu_traffic(kname, N)             # DRAM bytes per launch (ncu), or None
 
     # end to end: every step's b copied in from pinned host memory and its z
@@ -307,7 +309,8 @@ def gpu_arm(args, world, rank, local_rank, dist):
 
     h.close()
     names = {T.TVFGP_VARIANT_FUSED: "fused", T.TVFGP_VARIANT_SCALAR: "scalar",
-             T.TVFGP_VARIANT_ZMARCH_TMA: "zmarch", T.TVFGP_VARIANT_ZMARCH2_TMA: "zmarch2"}
+             T.TVFGP_VARIANT_ZMARCH_TMA: "zmarch", T.TVFGP_VARIANT_ZMARCH2_TMA: "zmarch2",
+             T.TVFGP_VARIANT_SEPARATE: "separate"}
     out = {
         "metric": METRIC,
         "value": round(value, 3),

@@ -364,6 +364,99 @@ __global__ void __launch_bounds__(256) primal_scalar(const PrimalArgs a)
 }
 
 // ---------------------------------------------------------------------------
+// SEPARATE: the step as two kernels, z written by one and read by the next
+// (page "TV solver: the FGP step on the GPU", section "Variants", first row:
+// 18 volumes per step).  The first kernel is primal_vec4 / primal_scalar on
+// r_src; this one reads z at the voxel and its three upper neighbours.
+// ---------------------------------------------------------------------------
+
+struct DualArgs {
+    const float *z;    // primal of r_src, [N]
+    float *p;
+    const float *rs;
+    float *rd;
+    float s, m;
+    int nx, ny, nz;
+    long long N;
+};
+
+template <int BY>
+__global__ void __launch_bounds__(32 * BY) dual_from_z_vec4(const DualArgs a)
+{
+    const int lane = threadIdx.x;
+    const int x0 = (blockIdx.x * 32 + lane) * 4;
+    const int y = blockIdx.y * BY + threadIdx.y;
+    const int z = blockIdx.z;
+    const int nx = a.nx, ny = a.ny, nz = a.nz;
+    if (y >= ny) return;                         // whole warp: y is warp-uniform
+    const bool xin = x0 < nx;
+    const int sz = nx * ny;
+    const int i = x0 + nx * (y + ny * z);
+    const bool hasY = y + 1 < ny, hasZ = z + 1 < nz;
+    float4 P0 = f4zero(), P1 = f4zero(), P2 = f4zero(), R0 = f4zero(), R1 = f4zero(), R2 = f4zero();
+    float4 Zc = f4zero(), ZY = f4zero(), ZZ = f4zero();
+    if (xin) {
+        // the voxel's own p and r first
+        P0 = ld_once4(a.p + i);
+        P1 = ld_once4(a.p + a.N + i);
+        P2 = ld_once4(a.p + 2 * a.N + i);
+        R0 = ld_ro4(a.rs + i);
+        R1 = ld_ro4(a.rs + a.N + i);
+        R2 = ld_ro4(a.rs + 2 * a.N + i);
+        Zc = ld_ro4(a.z + i);
+        if (hasY) ZY = ld_ro4(a.z + i + nx);
+        if (hasZ) ZZ = ld_ro4(a.z + i + sz);
+    }
+    float zx = __shfl_down_sync(kFull, Zc.x, 1);
+    if (lane == 31 && x0 + 4 < nx) zx = __ldg(a.z + i + 4);
+    if (!xin) return;
+    const float gx3 = (x0 + 3 < nx - 1) ? __fsub_rn(Zc.w, zx) : 0.0f;
+    float4 G1 = f4zero(), G2 = f4zero();
+    if (hasY) {
+        G1.x = __fsub_rn(Zc.x, ZY.x); G1.y = __fsub_rn(Zc.y, ZY.y);
+        G1.z = __fsub_rn(Zc.z, ZY.z); G1.w = __fsub_rn(Zc.w, ZY.w);
+    }
+    if (hasZ) {
+        G2.x = __fsub_rn(Zc.x, ZZ.x); G2.y = __fsub_rn(Zc.y, ZZ.y);
+        G2.z = __fsub_rn(Zc.z, ZZ.z); G2.w = __fsub_rn(Zc.w, ZZ.w);
+    }
+    dual_update(R0.x, R1.x, R2.x, __fsub_rn(Zc.x, Zc.y), G1.x, G2.x, P0.x, P1.x, P2.x, a.s, a.m);
+    dual_update(R0.y, R1.y, R2.y, __fsub_rn(Zc.y, Zc.z), G1.y, G2.y, P0.y, P1.y, P2.y, a.s, a.m);
+    dual_update(R0.z, R1.z, R2.z, __fsub_rn(Zc.z, Zc.w), G1.z, G2.z, P0.z, P1.z, P2.z, a.s, a.m);
+    dual_update(R0.w, R1.w, R2.w, gx3, G1.w, G2.w, P0.w, P1.w, P2.w, a.s, a.m);
+    st4(a.p + i, P0);
+    st4(a.p + a.N + i, P1);
+    st4(a.p + 2 * a.N + i, P2);
+    st4(a.rd + i, R0);
+    st4(a.rd + a.N + i, R1);
+    st4(a.rd + 2 * a.N + i, R2);
+}
+
+__global__ void __launch_bounds__(256) dual_from_z_scalar(const DualArgs a)
+{
+    const int x = blockIdx.x * 32 + threadIdx.x;
+    const int y = blockIdx.y * 8 + threadIdx.y;
+    const int z = blockIdx.z;
+    const int nx = a.nx, ny = a.ny, nz = a.nz;
+    if (x >= nx || y >= ny) return;
+    const long long sz = (long long)nx * ny;
+    const long long i = x + (long long)nx * y + sz * z;
+    float P0 = __ldcs(a.p + i), P1 = __ldcs(a.p + a.N + i), P2 = __ldcs(a.p + 2 * a.N + i);
+    float R0 = __ldg(a.rs + i), R1 = __ldg(a.rs + a.N + i), R2 = __ldg(a.rs + 2 * a.N + i);
+    const float zc = __ldg(a.z + i);
+    const float g0 = (x < nx - 1) ? __fsub_rn(zc, __ldg(a.z + i + 1)) : 0.0f;
+    const float g1 = (y < ny - 1) ? __fsub_rn(zc, __ldg(a.z + i + nx)) : 0.0f;
+    const float g2 = (z < nz - 1) ? __fsub_rn(zc, __ldg(a.z + i + sz)) : 0.0f;
+    dual_update(R0, R1, R2, g0, g1, g2, P0, P1, P2, a.s, a.m);
+    a.p[i] = P0;
+    a.p[a.N + i] = P1;
+    a.p[2 * a.N + i] = P2;
+    a.rd[i] = R0;
+    a.rd[a.N + i] = R1;
+    a.rd[2 * a.N + i] = R2;
+}
+
+// ---------------------------------------------------------------------------
 // bounded waits
 // ---------------------------------------------------------------------------
 

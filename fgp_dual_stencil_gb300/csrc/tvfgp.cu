@@ -78,6 +78,7 @@ struct tvfgp_handle {
     long long launches;
     float *scratch;
     float *pair_scratch;        // 9N floats, two-step runs only
+    float *zscratch;            // N floats, two-kernel variant only
     int *d_err;
     ZmarchPlan zplan;
     Zmarch2Plan z2plan;
@@ -171,8 +172,15 @@ LaunchCfg step_cfg(const tvfgp_handle *h, int variant)
     return c;
 }
 
+// Kernels that are halves of a step of the two-kernel variant.
+constexpr int kKernPrimalZVec = 100;     // z = primal of r_src into the handle's z buffer
+constexpr int kKernPrimalZScalar = 101;
+constexpr int kKernDualZVec = 102;       // the rest of the step, reading that z
+constexpr int kKernDualZScalar = 103;
+
 // One kernel launch of a run: a single step (p updated in place, r_src ->
-// r_dst) or a two-step launch (p_src -> p_dst and r_src -> r_dst).
+// r_dst), a two-step launch (p_src -> p_dst and r_src -> r_dst), or a half
+// of a two-kernel step.
 struct Item {
     int kernel;             // a TVFGP_VARIANT_* value
     const float *p_src;
@@ -187,11 +195,26 @@ struct KArgs {
     StepArgs a;
     ZmarchArgs za;
     Zmarch2Args z2;
+    PrimalArgs pa;
+    DualArgs da;
     void *ptrs[1];
 };
 
 LaunchCfg item_cfg(const tvfgp_handle *h, int kernel)
 {
+    if (kernel >= kKernPrimalZVec) {
+        LaunchCfg c;
+        c.smem = 0;
+        c.block = dim3(32, 8, 1);
+        const bool vec = kernel == kKernPrimalZVec || kernel == kKernDualZVec;
+        c.grid = vec ? dim3((h->nx / 4 + 31) / 32, (h->ny + 7) / 8, h->nz)
+                     : dim3((h->nx + 31) / 32, (h->ny + 7) / 8, h->nz);
+        if (kernel == kKernPrimalZVec) c.func = reinterpret_cast<const void *>(&primal_vec4<8>);
+        else if (kernel == kKernPrimalZScalar) c.func = reinterpret_cast<const void *>(&primal_scalar);
+        else if (kernel == kKernDualZVec) c.func = reinterpret_cast<const void *>(&dual_from_z_vec4<8>);
+        else c.func = reinterpret_cast<const void *>(&dual_from_z_scalar);
+        return c;
+    }
     if (kernel == TVFGP_VARIANT_ZMARCH2_TMA) {
         LaunchCfg c;
         c.func = zmarch2_kernel();
@@ -205,6 +228,32 @@ LaunchCfg item_cfg(const tvfgp_handle *h, int kernel)
 
 bool fill_item(const tvfgp_handle *h, const Item &it, const float *b, float lam, KArgs &k)
 {
+    if (it.kernel == kKernPrimalZVec || it.kernel == kKernPrimalZScalar) {
+        k.pa.b = b;
+        k.pa.d = it.r_src;
+        k.pa.z = h->zscratch;
+        k.pa.lam = lam;
+        k.pa.nx = h->nx;
+        k.pa.ny = h->ny;
+        k.pa.nz = h->nz;
+        k.pa.N = h->N;
+        k.ptrs[0] = &k.pa;
+        return h->zscratch != nullptr;
+    }
+    if (it.kernel == kKernDualZVec || it.kernel == kKernDualZScalar) {
+        k.da.z = h->zscratch;
+        k.da.p = it.p_dst;
+        k.da.rs = it.r_src;
+        k.da.rd = it.r_dst;
+        k.da.s = step_of(lam);
+        k.da.m = it.m0;
+        k.da.nx = h->nx;
+        k.da.ny = h->ny;
+        k.da.nz = h->nz;
+        k.da.N = h->N;
+        k.ptrs[0] = &k.da;
+        return h->zscratch != nullptr;
+    }
     if (it.kernel == TVFGP_VARIANT_ZMARCH2_TMA) {
         k.ptrs[0] = &k.z2;
         return zmarch2_fill(h->z2plan, b, it.p_src, it.p_dst, it.r_src, it.r_dst, lam, step_of(lam),
@@ -233,12 +282,23 @@ void route(int moves, float *const buf[3], std::vector<float *> &seq)
 // on; p and r then travel through the handle's two extra buffer sets and end
 // in the caller's buffers, with no copy.  Single steps ping-pong r with the
 // scratch buffer; an odd count then needs one copy back (*copy_back).
-void plan_run(const tvfgp_handle *h, int variant, float *p, float *r, const std::vector<double> &m,
-              std::vector<Item> &items, bool *copy_back)
+void plan_run(const tvfgp_handle *h, int variant, bool vec_ok, float *p, float *r,
+              const std::vector<double> &m, std::vector<Item> &items, bool *copy_back)
 {
     const int n = static_cast<int>(m.size());
     items.clear();
     *copy_back = false;
+    if (variant == TVFGP_VARIANT_SEPARATE) {
+        for (int k = 0; k < n; ++k) {
+            const bool even = (k % 2) == 0;
+            float *rs = even ? r : h->scratch, *rd = even ? h->scratch : r;
+            const float mk = static_cast<float>(m[k]);
+            items.push_back({vec_ok ? kKernPrimalZVec : kKernPrimalZScalar, p, p, rs, rd, mk, 0.0f});
+            items.push_back({vec_ok ? kKernDualZVec : kKernDualZScalar, p, p, rs, rd, mk, 0.0f});
+        }
+        *copy_back = (n % 2) == 1;
+        return;
+    }
     if (variant == TVFGP_VARIANT_ZMARCH2_TMA && n >= 4 && h->pair_scratch != nullptr) {
         const size_t N3 = 3 * static_cast<size_t>(h->N);
         const int pairs = n / 2, single = n % 2;
@@ -405,6 +465,19 @@ int run_graph(tvfgp_handle *h, int variant, const float *b, float *p, float *r, 
 
 // The two extra buffer sets of two-step runs (p twice, r once more; the
 // handle's scratch is the other r).
+// The z volume of the two-kernel variant.
+int ensure_z_scratch(tvfgp_handle *h)
+{
+    if (h->zscratch) return TVFGP_OK;
+    cudaError_t e = cudaMalloc(&h->zscratch, sizeof(float) * static_cast<size_t>(h->N));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        h->zscratch = nullptr;
+        return from_cuda(e);
+    }
+    return TVFGP_OK;
+}
+
 int ensure_pair_scratch(tvfgp_handle *h)
 {
     if (h->pair_scratch) return TVFGP_OK;
@@ -456,7 +529,7 @@ int tvfgp_create_ex(int nx, int ny, int nz, int variant, unsigned flags, tvfgp_t
     *out = nullptr;
     if (nx < 1 || ny < 1 || nz < 1 || nx > 65535 || ny > 65535 || nz > 65535) return TVFGP_ERR_ARG;
     if (static_cast<long long>(nx) * ny * (static_cast<long long>(nz) + 1) > INT_MAX) return TVFGP_ERR_ARG;
-    if (variant < TVFGP_VARIANT_AUTO || variant > TVFGP_VARIANT_ZMARCH2_TMA || flags != 0)
+    if (variant < TVFGP_VARIANT_AUTO || variant > TVFGP_VARIANT_SEPARATE || flags != 0)
         return TVFGP_ERR_ARG;
     if ((variant == TVFGP_VARIANT_ZMARCH_TMA || variant == TVFGP_VARIANT_ZMARCH2_TMA) &&
         !zmarch_available())
@@ -475,6 +548,7 @@ int tvfgp_create_ex(int nx, int ny, int nz, int variant, unsigned flags, tvfgp_t
     h->graph_clock = 0;
     h->scratch = nullptr;
     h->pair_scratch = nullptr;
+    h->zscratch = nullptr;
     h->d_err = nullptr;
     cudaError_t e = cudaMalloc(&h->scratch, sizeof(float) * 3 * static_cast<size_t>(h->N));
     if (e == cudaSuccess) e = cudaMalloc(&h->d_err, sizeof(int));
@@ -488,10 +562,13 @@ int tvfgp_create_ex(int nx, int ny, int nz, int variant, unsigned flags, tvfgp_t
                            (variant == TVFGP_VARIANT_AUTO && kAutoVariant == TVFGP_VARIANT_ZMARCH2_TMA);
     if (e == cudaSuccess && want_pairs && nx % 4 == 0 && ensure_pair_scratch(h) != TVFGP_OK)
         e = cudaErrorMemoryAllocation;
+    if (e == cudaSuccess && variant == TVFGP_VARIANT_SEPARATE && ensure_z_scratch(h) != TVFGP_OK)
+        e = cudaErrorMemoryAllocation;
     if (e != cudaSuccess) {
         cudaGetLastError();
         cudaFree(h->scratch);
         cudaFree(h->pair_scratch);
+        cudaFree(h->zscratch);
         cudaFree(h->d_err);
         h->magic = 0;
         delete h;
@@ -513,6 +590,7 @@ int tvfgp_destroy(tvfgp_t h)
     for (auto &g : h->graphs) destroy_graph(g);
     cudaFree(h->scratch);
     cudaFree(h->pair_scratch);
+    cudaFree(h->zscratch);
     cudaFree(h->d_err);
     h->magic = 0;
     delete h;
@@ -521,8 +599,12 @@ int tvfgp_destroy(tvfgp_t h)
 
 int tvfgp_set_variant(tvfgp_t h, int variant)
 {
-    if (!valid(h) || variant < TVFGP_VARIANT_AUTO || variant > TVFGP_VARIANT_ZMARCH2_TMA)
+    if (!valid(h) || variant < TVFGP_VARIANT_AUTO || variant > TVFGP_VARIANT_SEPARATE)
         return TVFGP_ERR_ARG;
+    if (variant == TVFGP_VARIANT_SEPARATE) {
+        const int rc = ensure_z_scratch(h);
+        if (rc != TVFGP_OK) return rc;
+    }
     if ((variant == TVFGP_VARIANT_ZMARCH_TMA || variant == TVFGP_VARIANT_ZMARCH2_TMA) &&
         !zmarch_available())
         return TVFGP_ERR_UNSUPPORTED;
@@ -565,8 +647,16 @@ int tvfgp_step(tvfgp_t h, const float *b, float *p, const float *r_src, float *r
                         aligned16(r_dst);
     int variant = resolve_variant(h, h->variant, vec_ok);
     if (variant == TVFGP_VARIANT_ZMARCH2_TMA) variant = TVFGP_VARIANT_ZMARCH_TMA;   // one step only
-    return launch_step(h, variant, make_args(h, b, p, r_src, r_dst, lambda, m),
-                       reinterpret_cast<cudaStream_t>(stream));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (variant == TVFGP_VARIANT_SEPARATE) {
+        const Item first{vec_ok ? kKernPrimalZVec : kKernPrimalZScalar, p, p, r_src, r_dst, m, 0.0f};
+        const Item second{vec_ok ? kKernDualZVec : kKernDualZScalar, p, p, r_src, r_dst, m, 0.0f};
+        int rc2 = launch_item(h, first, b, lambda, st);
+        if (rc2 == TVFGP_OK) rc2 = launch_item(h, second, b, lambda, st);
+        if (rc2 == TVFGP_OK) h->last_variant = TVFGP_VARIANT_SEPARATE;
+        return rc2;
+    }
+    return launch_step(h, variant, make_args(h, b, p, r_src, r_dst, lambda, m), st);
 }
 
 int tvfgp_run(tvfgp_t h, const float *b, float *p, float *r, float lambda, int nsteps, double t0,
@@ -597,7 +687,7 @@ int tvfgp_run(tvfgp_t h, const float *b, float *p, float *r, float lambda, int n
     const int variant = resolve_variant(h, h->variant, vec_ok);
     std::vector<Item> items;
     bool copy_back = false;
-    plan_run(h, variant, p, r, m, items, &copy_back);
+    plan_run(h, variant, vec_ok, p, r, m, items, &copy_back);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (h->graph_on) {
         rc = run_graph(h, variant, b, p, r, lambda, nsteps, t0, items, copy_back, st);
@@ -613,7 +703,8 @@ int tvfgp_run(tvfgp_t h, const float *b, float *p, float *r, float lambda, int n
         }
     }
     if (rc == TVFGP_OK) {
-        h->last_variant = items.front().kernel;
+        h->last_variant = items.front().kernel >= kKernPrimalZVec ? TVFGP_VARIANT_SEPARATE
+                                                                : items.front().kernel;
         if (t_final) *t_final = tf;
     }
     return rc;

@@ -31,10 +31,11 @@ TVFGP_VARIANT_FUSED = 1
 TVFGP_VARIANT_SCALAR = 2
 TVFGP_VARIANT_ZMARCH_TMA = 3
 TVFGP_VARIANT_ZMARCH2_TMA = 4
+TVFGP_VARIANT_SEPARATE = 5
 
 VARIANTS = {"auto": TVFGP_VARIANT_AUTO, "fused": TVFGP_VARIANT_FUSED,
             "scalar": TVFGP_VARIANT_SCALAR, "zmarch": TVFGP_VARIANT_ZMARCH_TMA,
-            "zmarch2": TVFGP_VARIANT_ZMARCH2_TMA}
+            "zmarch2": TVFGP_VARIANT_ZMARCH2_TMA, "separate": TVFGP_VARIANT_SEPARATE}
 
 
 class TvfgpError(RuntimeError):

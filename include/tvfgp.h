@@ -80,13 +80,17 @@ enum tvfgp_variant {
                                      in shared memory by TMA; same requirements as FUSED (else
                                      the call falls back to SCALAR); TVFGP_ERR_UNSUPPORTED at
                                      create/set time if the driver lacks the TMA encoder */
-    TVFGP_VARIANT_ZMARCH2_TMA = 4 /* two FGP steps per pass over memory (13 volumes per two
+    TVFGP_VARIANT_ZMARCH2_TMA = 4, /* two FGP steps per pass over memory (13 volumes per two
                                      steps instead of per step), same results; used by
                                      tvfgp_run for nsteps >= 4 (a last odd step and shorter
                                      runs use ZMARCH_TMA).  The handle then owns two more
                                      buffer sets (9*nx*ny*nz more floats), allocated by
                                      tvfgp_create_ex / tvfgp_set_variant.  Same requirements
                                      as ZMARCH_TMA. */
+    TVFGP_VARIANT_SEPARATE = 5     /* the page's two-kernel step ("Variants", first row): one
+                                     kernel writes z, the next reads it (18 volumes per step
+                                     instead of 13); for comparison.  Any shape; the handle
+                                     then owns an N-float z buffer. */
 };
 
 /* Create a handle for an nx x ny x nz volume on the current CUDA device.

@@ -21,7 +21,7 @@ def T():
     return tvfgp
 
 
-VEC_VARIANTS = ["fused", "zmarch", "zmarch2", "scalar"]
+VEC_VARIANTS = ["fused", "zmarch", "zmarch2", "scalar", "separate"]
 
 
 # ---------------------------------------------------------------------------
@@ -36,6 +36,8 @@ def test_small_workloads_exact(T, key, variant):
     ref = run_workload_oracle(w)
     assert_parity(gpu, ref[1:], float(np.abs(b).max()), exact=True, what=key)
     per_outer = w.steps // 2 + w.steps % 2 if (variant == "zmarch2" and w.steps >= 4) else w.steps
+    if variant == "separate":
+        per_outer = 2 * w.steps
     assert launched == w.outers * per_outer + 2
 
 
@@ -87,7 +89,9 @@ def test_odd_shapes_warm_start(T, shape, variant):
             zp = h.primal(bd, p, lam)
             assert h.check() == 0
             if nsteps:
-                if variant == "scalar" or nx % 4:
+                if variant == "separate":
+                    want = T.TVFGP_VARIANT_SEPARATE
+                elif variant == "scalar" or nx % 4:
                     want = T.TVFGP_VARIANT_SCALAR
                 elif variant == "zmarch2" and nsteps < 4:
                     want = T.TVFGP_VARIANT_ZMARCH_TMA      # two-step launches from 4 steps on
