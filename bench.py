@@ -9,8 +9,8 @@ iteration: tvfgp_run (10 FGP steps) + tvfgp_primal (z of p).
 Metric: Gvoxel-updates per second (voxels x FGP steps / s), with ms per FGP
 step beside it, and the HBM roofline fraction of the step kernel from the
 13-volume traffic model of the page "TV solver: the FGP step on the GPU"
-(section "Variants": read b, r(3), p(3); write p(3), r(3) = 52 bytes per
-voxel and step).
+(section "Variants": b and the three components of r and of p are read,
+p and r written back, 13 fp32 volumes = 52 bytes per voxel and step).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 
@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--workload", default="c4", help="c1..c5 (default c4: 512^3)")
     ap.add_argument("--variant", default="auto", choices=["auto", "fused", "scalar", "zmarch", "zmarch2", "separate"])
     ap.add_argument("--eager", action="store_true", help="launch eagerly instead of graph replay")
+    ap.add_argument("--dual", default="f32", choices=["f32", "f16"],
+                    help="storage of p and r (f16: binary16, fp32 arithmetic; changes the result)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -221,15 +223,19 @@ def gpu_arm(args, world, rank, local_rank, dist):
         b_host.append(t)
     b_dev = [x.to(dev) for x in b_host]
     shape = (3, w.nz, w.ny, w.nx)
-    p = torch.zeros(shape, device=dev)
-    r = torch.zeros(shape, device=dev)
+    f16 = args.dual == "f16"
+    ddt = torch.float16 if f16 else torch.float32
+    p = torch.zeros(shape, dtype=ddt, device=dev)
+    r = torch.zeros(shape, dtype=ddt, device=dev)
     z = torch.empty((w.nz, w.ny, w.nx), device=dev)
     h = T.Tvfgp(w.nx, w.ny, w.nz, args.variant, graph=not args.eager)
     stream = torch.cuda.current_stream(dev)
+    run = h.run_f16 if f16 else h.run
+    primal = h.primal_f16 if f16 else h.primal
 
     def outer(b):
-        h.run(b, p, r, w.lam, w.steps, w.t0, stream)
-        h.primal(b, p, w.lam, z, stream)
+        run(b, p, r, w.lam, w.steps, w.t0, stream)
+        primal(b, p, w.lam, z, stream)
 
     for j in range(W):
         outer(b_dev[j % n_b])
@@ -252,9 +258,9 @@ def gpu_arm(args, world, rank, local_rank, dist):
     for j in range(K):
         b = b_dev[(W + j) % n_b]
         ev_run[j][0].record(stream)
-        h.run(b, p, r, w.lam, w.steps, w.t0, stream)
+        run(b, p, r, w.lam, w.steps, w.t0, stream)
         ev_run[j][1].record(stream)
-        h.primal(b, p, w.lam, z, stream)
+        primal(b, p, w.lam, z, stream)
     ev_end.record(stream)
     torch.cuda.synchronize(dev)
     t_wall1 = time.time()
@@ -279,12 +285,15 @@ def gpu_arm(args, world, rank, local_rank, dist):
     peak, peak_kind = hbm_peak()
     # algorithmic bytes: 52 per voxel and FGP step, times the voxel-steps one
     # launch processes
-    alg_bytes = (72 if separate else BYTES_PER_VOXEL_STEP) * N * steps_per_launch
+    per_voxel_step = 28 if f16 else (72 if separate else BYTES_PER_VOXEL_STEP)
+    alg_bytes = per_voxel_step * N * steps_per_launch
     achieved = alg_bytes / launch_s / 1e9
     kname = {T.TVFGP_VARIANT_FUSED: "fgp_step_fused4", T.TVFGP_VARIANT_SCALAR: "fgp_step_scalar",
              T.TVFGP_VARIANT_ZMARCH_TMA: "fgp_step_zmarch_tma",
              T.TVFGP_VARIANT_ZMARCH2_TMA: "fgp_step2_zmarch_tma",
              T.TVFGP_VARIANT_SEPARATE: "primal_vec4 + dual_from_z_vec4"}.get(variant_used, "?")
+    if f16:
+        kname += "<__half>"
     traffic = ncu_traffic(kname, N)             # DRAM bytes per launch (ncu), or None
 
     # end to end: every step's b copied in from pinned host memory and its z
@@ -292,7 +301,7 @@ def gpu_arm(args, world, rank, local_rank, dist):
     # streams (double-buffered) and overlap the previous / next step's compute
     e2e = None
     if not args.no_e2e:
-        e2e_s = end_to_end(torch, h, w, b_host, p, r, stream, dev, K, dist)
+        e2e_s = end_to_end(torch, h, w, b_host, p, r, stream, dev, K, dist, run, primal)
         e2e = {"value": round(world * N * w.steps * K / e2e_s / 1e9, 3), "unit": UNIT,
                "h2d_bytes_per_step": 4 * N, "d2h_bytes_per_step": 4 * N,
                "ms_per_step": round(e2e_s * 1e3 / K, 4),
@@ -327,7 +336,7 @@ def gpu_arm(args, world, rank, local_rank, dist):
         "scaling": "weak",
         "vs_baseline": round(value / (N / (PAGE_FUSED_512_MS / 1e3) / 1e9), 3)
         if args.workload == "c4" else None,
-        "dtype": "f32",
+        "dtype": "f32 (dual stored as f16)" if f16 else "f32",
         "data": "synthetic",
         "config": {
             "workload": "%dx%dx%d fp32 TV-dual FGP, %d outers x %d steps, warm p/r, t0=1 per outer, "
@@ -353,7 +362,8 @@ def gpu_arm(args, world, rank, local_rank, dist):
             if peak_kind == "measured" else "fallback 6.8 TB/s",
             "traffic": None if traffic is None else round(traffic),
             "algorithmic_bytes_per_launch": round(alg_bytes),
-            "model": "52 B per voxel and FGP step (13 fp32 volumes) x voxel-steps per launch",
+            "model": ("28 B per voxel and FGP step (b fp32, p and r binary16)" if f16 else
+                      "52 B per voxel and FGP step (13 fp32 volumes)") + " x voxel-steps per launch",
         },
         "gpu_launches": launches,
         "e2e": e2e,
@@ -363,7 +373,7 @@ def gpu_arm(args, world, rank, local_rank, dist):
     return out
 
 
-def end_to_end(torch, h, w, b_host, p, r, stream, dev, K, dist):
+def end_to_end(torch, h, w, b_host, p, r, stream, dev, K, dist, run, primal):
     """Wall time of K outer iterations where each step's b comes from pinned
     host memory and its z goes back to pinned host memory."""
     n_b = len(b_host)
@@ -397,8 +407,8 @@ def end_to_end(torch, h, w, b_host, p, r, stream, dev, K, dist):
         stream.wait_event(ev_in[s])
         if j >= 2:
             stream.wait_event(ev_out[s])                 # z_out[s] copied out
-        h.run(b_in[s], p, r, w.lam, w.steps, w.t0, stream)
-        h.primal(b_in[s], p, w.lam, z_out[s], stream)
+        run(b_in[s], p, r, w.lam, w.steps, w.t0, stream)
+        primal(b_in[s], p, w.lam, z_out[s], stream)
         ev_done[s].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_done[s])

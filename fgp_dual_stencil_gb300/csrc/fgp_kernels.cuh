@@ -19,33 +19,41 @@
 // and the division are only issued when |q|^2 > 1 (IEEE x/1 == x).
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace tvfgp {
 
 // Arguments of one FGP step.  Volumes are fp32, x fastest; dual fields are
-// planar [3][N] (component a at a*N + i).
-struct StepArgs {
+// planar [3][N] (component a at a*N + i), stored as TS: float, or __half for
+// the half-precision storage of the dual (arithmetic stays fp32: a stored
+// value is widened exactly on load and rounded once, to nearest even, on
+// store).
+template <typename TS>
+struct StepArgsT {
     const float *b;
-    float *p;
-    const float *rs;   // r read by this step
-    float *rd;         // r written by this step (distinct buffer: neighbours still read rs)
+    TS *p;
+    const TS *rs;      // r read by this step
+    TS *rd;            // r written by this step (distinct buffer: neighbours still read rs)
     float lam;
     float s;           // 1/(12 lambda) rounded once to float
     float m;           // momentum weight of this step
     int nx, ny, nz;
     long long N;       // nx*ny*nz
 };
+using StepArgs = StepArgsT<float>;
 
-struct PrimalArgs {
+template <typename TS>
+struct PrimalArgsT {
     const float *b;
-    const float *d;    // dual field [3][N]
+    const TS *d;       // dual field [3][N]
     float *z;
     float lam;
     int nx, ny, nz;
     long long N;
 };
+using PrimalArgs = PrimalArgsT<float>;
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kErrTimeout = 5;   // value written to the device error word
@@ -110,6 +118,34 @@ __device__ __forceinline__ float4 f4zero()
     return make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+// Four consecutive values of a dual component, widened to float4, and back.
+__device__ __forceinline__ float4 ldv_ro(const float *p) { return ld_ro4(p); }
+__device__ __forceinline__ float4 ldv_once(const float *p) { return ld_once4(p); }
+__device__ __forceinline__ void stv(float *p, float4 v) { st4(p, v); }
+__device__ __forceinline__ float ld1_ro(const float *p) { return __ldg(p); }
+__device__ __forceinline__ float ld1_once(const float *p) { return __ldcs(p); }
+__device__ __forceinline__ void st1(float *p, float v) { *p = v; }
+
+__device__ __forceinline__ float4 widen4(uint2 u)
+{
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ float4 ldv_ro(const __half *p) { return widen4(__ldg(reinterpret_cast<const uint2 *>(p))); }
+__device__ __forceinline__ float4 ldv_once(const __half *p) { return widen4(__ldcs(reinterpret_cast<const uint2 *>(p))); }
+__device__ __forceinline__ void stv(__half *p, float4 v)
+{
+    const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const unsigned *>(&a);
+    u.y = *reinterpret_cast<const unsigned *>(&b);
+    *reinterpret_cast<uint2 *>(p) = u;
+}
+__device__ __forceinline__ float ld1_ro(const __half *p) { return __half2float(__ldg(p)); }
+__device__ __forceinline__ float ld1_once(const __half *p) { return __half2float(__ldcs(p)); }
+__device__ __forceinline__ void st1(__half *p, float v) { *p = __float2half_rn(v); }
+
 // z at four consecutive x voxels from their b and r, the r0 of the voxel left
 // of the first one, and r1, r2 of the lower neighbours in y and z.
 __device__ __forceinline__ float4 zquad(float4 B, float4 R0, float4 R1, float4 R2, float r0left,
@@ -143,8 +179,8 @@ __device__ __forceinline__ float4 zquad(float4 B, float4 R0, float4 R1, float4 R
 #ifndef TVFGP_FUSED_MINB
 #define TVFGP_FUSED_MINB 6
 #endif
-template <int BY, int ZC>
-__global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(const StepArgs a)
+template <int BY, int ZC, typename TS = float>
+__global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(const StepArgsT<TS> a)
 {
     const int lane = threadIdx.x;
     const int x0 = (blockIdx.x * 32 + lane) * 4;
@@ -159,15 +195,15 @@ __global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(con
     const float lam = a.lam, s = a.s, m = a.m;
 
     const float *__restrict__ b = a.b;
-    const float *__restrict__ r0 = a.rs;
-    const float *__restrict__ r1 = a.rs + a.N;
-    const float *__restrict__ r2 = a.rs + 2 * a.N;
-    float *__restrict__ p0 = a.p;
-    float *__restrict__ p1 = a.p + a.N;
-    float *__restrict__ p2 = a.p + 2 * a.N;
-    float *__restrict__ o0 = a.rd;
-    float *__restrict__ o1 = a.rd + a.N;
-    float *__restrict__ o2 = a.rd + 2 * a.N;
+    const TS *__restrict__ r0 = a.rs;
+    const TS *__restrict__ r1 = a.rs + a.N;
+    const TS *__restrict__ r2 = a.rs + 2 * a.N;
+    TS *__restrict__ p0 = a.p;
+    TS *__restrict__ p1 = a.p + a.N;
+    TS *__restrict__ p2 = a.p + 2 * a.N;
+    TS *__restrict__ o0 = a.rd;
+    TS *__restrict__ o1 = a.rd + a.N;
+    TS *__restrict__ o2 = a.rd + 2 * a.N;
 
     int z = zb;
     int i = x0 + nx * (y + ny * z);
@@ -178,19 +214,19 @@ __global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(con
         float4 Bc = f4zero(), R1lo = f4zero(), R2lo = f4zero();
         if (xin) {
             Bc = ld_ro4(b + i);
-            R0c = ld_ro4(r0 + i);
-            R1c = ld_ro4(r1 + i);
-            R2c = ld_ro4(r2 + i);
-            if (y > 0) R1lo = ld_ro4(r1 + i - nx);
-            if (z > 0) R2lo = ld_ro4(r2 + i - sz);
+            R0c = ldv_ro(r0 + i);
+            R1c = ldv_ro(r1 + i);
+            R2c = ldv_ro(r2 + i);
+            if (y > 0) R1lo = ldv_ro(r1 + i - nx);
+            if (z > 0) R2lo = ldv_ro(r2 + i - sz);
         }
         float left = __shfl_up_sync(kFull, R0c.w, 1);
-        if (lane == 0) left = (x0 > 0) ? __ldg(r0 + i - 1) : 0.0f;
+        if (lane == 0) left = (x0 > 0) ? ld1_ro(r0 + i - 1) : 0.0f;
         Zc = zquad(Bc, R0c, R1c, R2c, left, R1lo, R2lo, lam);
     }
     // r2 of row y+1 one plane below (the z-lower neighbour of z(i+ey))
     float4 R2yp = f4zero();
-    if (xin && hasY && z > 0) R2yp = ld_ro4(r2 + i + nx - sz);
+    if (xin && hasY && z > 0) R2yp = ldv_ro(r2 + i + nx - sz);
 
     for (; z < ze; ++z, i += sz) {
         const bool hasZ = (z + 1 < nz);          // block-uniform
@@ -198,49 +234,49 @@ __global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(con
         // (1) the voxel's own p, first
         float4 P0 = f4zero(), P1 = f4zero(), P2 = f4zero();
         if (xin) {
-            P0 = ld_once4(p0 + i);
-            P1 = ld_once4(p1 + i);
-            P2 = ld_once4(p2 + i);
+            P0 = ldv_once(p0 + i);
+            P1 = ldv_once(p1 + i);
+            P2 = ldv_once(p2 + i);
         }
         // (2) the next plane's own b, r (and r1 of its y-lower row)
         float4 Bn = f4zero(), R0n = f4zero(), R1n = f4zero(), R2n = f4zero(), R1lon = f4zero();
         if (xin && hasZ) {
             Bn = ld_ro4(b + i + sz);
-            R0n = ld_ro4(r0 + i + sz);
-            R1n = ld_ro4(r1 + i + sz);
-            R2n = ld_ro4(r2 + i + sz);
-            if (y > 0) R1lon = ld_ro4(r1 + i + sz - nx);
+            R0n = ldv_ro(r0 + i + sz);
+            R1n = ldv_ro(r1 + i + sz);
+            R2n = ldv_ro(r2 + i + sz);
+            if (y > 0) R1lon = ldv_ro(r1 + i + sz - nx);
         }
         // (3) row y+1 of this plane
         float4 By = f4zero(), R0y = f4zero(), R1y = f4zero(), R2y = f4zero();
         if (xin && hasY) {
             By = ld_ro4(b + i + nx);
-            R0y = ld_ro4(r0 + i + nx);
-            R1y = ld_ro4(r1 + i + nx);
-            R2y = ld_ro4(r2 + i + nx);
+            R0y = ldv_ro(r0 + i + nx);
+            R1y = ldv_ro(r1 + i + nx);
+            R2y = ldv_ro(r2 + i + nx);
         }
 
         // z(i+ey)
         float4 ZY = f4zero();
         if (hasY) {
             float left = __shfl_up_sync(kFull, R0y.w, 1);
-            if (lane == 0) left = (x0 > 0) ? __ldg(r0 + i + nx - 1) : 0.0f;
+            if (lane == 0) left = (x0 > 0) ? ld1_ro(r0 + i + nx - 1) : 0.0f;
             ZY = zquad(By, R0y, R1y, R2y, left, R1c, R2yp, lam);
         }
         // z(i+ez)
         float4 ZZ = f4zero();
         if (hasZ) {
             float left = __shfl_up_sync(kFull, R0n.w, 1);
-            if (lane == 0) left = (x0 > 0) ? __ldg(r0 + i + sz - 1) : 0.0f;
+            if (lane == 0) left = (x0 > 0) ? ld1_ro(r0 + i + sz - 1) : 0.0f;
             ZZ = zquad(Bn, R0n, R1n, R2n, left, R1lon, R2c, lam);
         }
         // z(i+ex) of the last voxel: the next lane's first z
         float zx = __shfl_down_sync(kFull, Zc.x, 1);
         if (lane == 31 && x0 + 4 < nx) {
             const int j = i + 4;
-            const float d0 = __fsub_rn(__ldg(r0 + j), R0c.w);
-            const float d1 = __fsub_rn(__ldg(r1 + j), y > 0 ? __ldg(r1 + j - nx) : 0.0f);
-            const float d2 = __fsub_rn(__ldg(r2 + j), z > 0 ? __ldg(r2 + j - sz) : 0.0f);
+            const float d0 = __fsub_rn(ld1_ro(r0 + j), R0c.w);
+            const float d1 = __fsub_rn(ld1_ro(r1 + j), y > 0 ? ld1_ro(r1 + j - nx) : 0.0f);
+            const float d2 = __fsub_rn(ld1_ro(r2 + j), z > 0 ? ld1_ro(r2 + j - sz) : 0.0f);
             zx = zval(__ldg(b + j), lam, d0, d1, d2);
         }
 
@@ -260,12 +296,12 @@ __global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(con
             dual_update(N0.y, N1.y, N2.y, __fsub_rn(Zc.y, Zc.z), G1.y, G2.y, P0.y, P1.y, P2.y, s, m);
             dual_update(N0.z, N1.z, N2.z, __fsub_rn(Zc.z, Zc.w), G1.z, G2.z, P0.z, P1.z, P2.z, s, m);
             dual_update(N0.w, N1.w, N2.w, gx3, G1.w, G2.w, P0.w, P1.w, P2.w, s, m);
-            st4(p0 + i, P0);
-            st4(p1 + i, P1);
-            st4(p2 + i, P2);
-            st4(o0 + i, N0);
-            st4(o1 + i, N1);
-            st4(o2 + i, N2);
+            stv(p0 + i, P0);
+            stv(p1 + i, P1);
+            stv(p2 + i, P2);
+            stv(o0 + i, N0);
+            stv(o1 + i, N1);
+            stv(o2 + i, N2);
         }
 
         R0c = R0n;
@@ -280,18 +316,20 @@ __global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(con
 // SCALAR: one voxel per thread, any shape and alignment
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ float zpoint(const float *__restrict__ b, const float *__restrict__ r0,
-                                        const float *__restrict__ r1, const float *__restrict__ r2,
+template <typename TS>
+__device__ __forceinline__ float zpoint(const float *__restrict__ b, const TS *__restrict__ r0,
+                                        const TS *__restrict__ r1, const TS *__restrict__ r2,
                                         int x, int y, int z, long long j, int nx, long long sz,
                                         float lam)
 {
-    const float d0 = __fsub_rn(__ldg(r0 + j), x > 0 ? __ldg(r0 + j - 1) : 0.0f);
-    const float d1 = __fsub_rn(__ldg(r1 + j), y > 0 ? __ldg(r1 + j - nx) : 0.0f);
-    const float d2 = __fsub_rn(__ldg(r2 + j), z > 0 ? __ldg(r2 + j - sz) : 0.0f);
+    const float d0 = __fsub_rn(ld1_ro(r0 + j), x > 0 ? ld1_ro(r0 + j - 1) : 0.0f);
+    const float d1 = __fsub_rn(ld1_ro(r1 + j), y > 0 ? ld1_ro(r1 + j - nx) : 0.0f);
+    const float d2 = __fsub_rn(ld1_ro(r2 + j), z > 0 ? ld1_ro(r2 + j - sz) : 0.0f);
     return zval(__ldg(b + j), lam, d0, d1, d2);
 }
 
-__global__ void __launch_bounds__(256) fgp_step_scalar(const StepArgs a)
+template <typename TS = float>
+__global__ void __launch_bounds__(256) fgp_step_scalar(const StepArgsT<TS> a)
 {
     const int x = blockIdx.x * 32 + threadIdx.x;
     const int y = blockIdx.y * 8 + threadIdx.y;
@@ -300,31 +338,31 @@ __global__ void __launch_bounds__(256) fgp_step_scalar(const StepArgs a)
     if (x >= nx || y >= ny) return;
     const long long sz = (long long)nx * ny;
     const long long i = x + (long long)nx * y + sz * z;
-    const float *r0 = a.rs, *r1 = a.rs + a.N, *r2 = a.rs + 2 * a.N;
+    const TS *r0 = a.rs, *r1 = a.rs + a.N, *r2 = a.rs + 2 * a.N;
 
     // the voxel's own p and r first
-    float P0 = __ldcs(a.p + i), P1 = __ldcs(a.p + a.N + i), P2 = __ldcs(a.p + 2 * a.N + i);
-    float R0 = __ldg(r0 + i), R1 = __ldg(r1 + i), R2 = __ldg(r2 + i);
+    float P0 = ld1_once(a.p + i), P1 = ld1_once(a.p + a.N + i), P2 = ld1_once(a.p + 2 * a.N + i);
+    float R0 = ld1_ro(r0 + i), R1 = ld1_ro(r1 + i), R2 = ld1_ro(r2 + i);
 
     const float zc = zpoint(a.b, r0, r1, r2, x, y, z, i, nx, sz, a.lam);
     const float g0 = (x < nx - 1) ? __fsub_rn(zc, zpoint(a.b, r0, r1, r2, x + 1, y, z, i + 1, nx, sz, a.lam)) : 0.0f;
     const float g1 = (y < ny - 1) ? __fsub_rn(zc, zpoint(a.b, r0, r1, r2, x, y + 1, z, i + nx, nx, sz, a.lam)) : 0.0f;
     const float g2 = (z < nz - 1) ? __fsub_rn(zc, zpoint(a.b, r0, r1, r2, x, y, z + 1, i + sz, nx, sz, a.lam)) : 0.0f;
     dual_update(R0, R1, R2, g0, g1, g2, P0, P1, P2, a.s, a.m);
-    a.p[i] = P0;
-    a.p[a.N + i] = P1;
-    a.p[2 * a.N + i] = P2;
-    a.rd[i] = R0;
-    a.rd[a.N + i] = R1;
-    a.rd[2 * a.N + i] = R2;
+    st1(a.p + i, P0);
+    st1(a.p + a.N + i, P1);
+    st1(a.p + 2 * a.N + i, P2);
+    st1(a.rd + i, R0);
+    st1(a.rd + a.N + i, R1);
+    st1(a.rd + 2 * a.N + i, R2);
 }
 
 // ---------------------------------------------------------------------------
 // primal z = max(b - lambda L(dual), 0)
 // ---------------------------------------------------------------------------
 
-template <int BY>
-__global__ void __launch_bounds__(32 * BY) primal_vec4(const PrimalArgs a)
+template <int BY, typename TS = float>
+__global__ void __launch_bounds__(32 * BY) primal_vec4(const PrimalArgsT<TS> a)
 {
     const int lane = threadIdx.x;
     const int x0 = (blockIdx.x * 32 + lane) * 4;
@@ -335,23 +373,24 @@ __global__ void __launch_bounds__(32 * BY) primal_vec4(const PrimalArgs a)
     const bool xin = x0 < nx;
     const int sz = nx * ny;
     const int i = x0 + nx * (y + ny * z);
-    const float *d0 = a.d, *d1 = a.d + a.N, *d2 = a.d + 2 * a.N;
+    const TS *d0 = a.d, *d1 = a.d + a.N, *d2 = a.d + 2 * a.N;
     float4 B = f4zero(), D0 = f4zero(), D1 = f4zero(), D2 = f4zero(), D1lo = f4zero(), D2lo = f4zero();
     if (xin) {
         B = ld_ro4(a.b + i);
-        D0 = ld_ro4(d0 + i);
-        D1 = ld_ro4(d1 + i);
-        D2 = ld_ro4(d2 + i);
-        if (y > 0) D1lo = ld_ro4(d1 + i - nx);
-        if (z > 0) D2lo = ld_ro4(d2 + i - sz);
+        D0 = ldv_ro(d0 + i);
+        D1 = ldv_ro(d1 + i);
+        D2 = ldv_ro(d2 + i);
+        if (y > 0) D1lo = ldv_ro(d1 + i - nx);
+        if (z > 0) D2lo = ldv_ro(d2 + i - sz);
     }
     float left = __shfl_up_sync(kFull, D0.w, 1);
-    if (lane == 0) left = (x0 > 0) ? __ldg(d0 + i - 1) : 0.0f;
+    if (lane == 0) left = (x0 > 0) ? ld1_ro(d0 + i - 1) : 0.0f;
     const float4 Z = zquad(B, D0, D1, D2, left, D1lo, D2lo, a.lam);
     if (xin) st4(a.z + i, Z);
 }
 
-__global__ void __launch_bounds__(256) primal_scalar(const PrimalArgs a)
+template <typename TS = float>
+__global__ void __launch_bounds__(256) primal_scalar(const PrimalArgsT<TS> a)
 {
     const int x = blockIdx.x * 32 + threadIdx.x;
     const int y = blockIdx.y * 8 + threadIdx.y;
@@ -367,7 +406,7 @@ __global__ void __launch_bounds__(256) primal_scalar(const PrimalArgs a)
 // SEPARATE: the step as two kernels, z written by one and read by the next
 // (page "TV solver: the FGP step on the GPU", section "Variants", first row:
 // 18 volumes per step).  The first kernel is primal_vec4 / primal_scalar on
-// r_src; this one reads z at the voxel and its three upper neighbours.
+// r_src; this one reads z at the voxel and at its +x, +y, +z neighbours.
 // ---------------------------------------------------------------------------
 
 struct DualArgs {

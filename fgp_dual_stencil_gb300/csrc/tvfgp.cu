@@ -56,6 +56,7 @@ struct GraphEntry {
     cudaGraphExec_t exec = nullptr;
     std::vector<cudaGraphNode_t> knodes;
     cudaGraphNode_t cnode = nullptr;
+    size_t copy_bytes = 0;
     // parameters the instantiated graph currently holds
     const float *b = nullptr;
     float *p = nullptr, *r = nullptr;
@@ -165,7 +166,7 @@ LaunchCfg step_cfg(const tvfgp_handle *h, int variant)
         c.grid = zmarch_grid(h->zplan);
         c.smem = zmarch_smem_bytes();
     } else {
-        c.func = reinterpret_cast<const void *>(&fgp_step_scalar);
+        c.func = reinterpret_cast<const void *>(&fgp_step_scalar<float>);
         c.block = dim3(32, 8, 1);
         c.grid = dim3((h->nx + 31) / 32, (h->ny + 7) / 8, h->nz);
     }
@@ -177,6 +178,9 @@ constexpr int kKernPrimalZVec = 100;     // z = primal of r_src into the handle'
 constexpr int kKernPrimalZScalar = 101;
 constexpr int kKernDualZVec = 102;       // the rest of the step, reading that z
 constexpr int kKernDualZScalar = 103;
+// One-step kernels on a dual stored as binary16.
+constexpr int kKernFusedH = 120;
+constexpr int kKernScalarH = 121;
 
 // One kernel launch of a run: a single step (p updated in place, r_src ->
 // r_dst), a two-step launch (p_src -> p_dst and r_src -> r_dst), or a half
@@ -193,6 +197,7 @@ struct Item {
 // Kernel-argument storage for one launch of any kernel family.
 struct KArgs {
     StepArgs a;
+    StepArgsT<__half> ah;
     ZmarchArgs za;
     Zmarch2Args z2;
     PrimalArgs pa;
@@ -202,6 +207,16 @@ struct KArgs {
 
 LaunchCfg item_cfg(const tvfgp_handle *h, int kernel)
 {
+    if (kernel == kKernFusedH) {
+        LaunchCfg c = step_cfg(h, TVFGP_VARIANT_FUSED);
+        c.func = reinterpret_cast<const void *>(&fgp_step_fused4<kFusedBY, kFusedZC, __half>);
+        return c;
+    }
+    if (kernel == kKernScalarH) {
+        LaunchCfg c = step_cfg(h, TVFGP_VARIANT_SCALAR);
+        c.func = reinterpret_cast<const void *>(&fgp_step_scalar<__half>);
+        return c;
+    }
     if (kernel >= kKernPrimalZVec) {
         LaunchCfg c;
         c.smem = 0;
@@ -210,7 +225,7 @@ LaunchCfg item_cfg(const tvfgp_handle *h, int kernel)
         c.grid = vec ? dim3((h->nx / 4 + 31) / 32, (h->ny + 7) / 8, h->nz)
                      : dim3((h->nx + 31) / 32, (h->ny + 7) / 8, h->nz);
         if (kernel == kKernPrimalZVec) c.func = reinterpret_cast<const void *>(&primal_vec4<8>);
-        else if (kernel == kKernPrimalZScalar) c.func = reinterpret_cast<const void *>(&primal_scalar);
+        else if (kernel == kKernPrimalZScalar) c.func = reinterpret_cast<const void *>(&primal_scalar<float>);
         else if (kernel == kKernDualZVec) c.func = reinterpret_cast<const void *>(&dual_from_z_vec4<8>);
         else c.func = reinterpret_cast<const void *>(&dual_from_z_scalar);
         return c;
@@ -228,6 +243,22 @@ LaunchCfg item_cfg(const tvfgp_handle *h, int kernel)
 
 bool fill_item(const tvfgp_handle *h, const Item &it, const float *b, float lam, KArgs &k)
 {
+    if (it.kernel == kKernFusedH || it.kernel == kKernScalarH) {
+        // the dual buffers of a binary16 run travel as float* in an Item
+        k.ah.b = b;
+        k.ah.p = reinterpret_cast<__half *>(it.p_dst);
+        k.ah.rs = reinterpret_cast<const __half *>(it.r_src);
+        k.ah.rd = reinterpret_cast<__half *>(it.r_dst);
+        k.ah.lam = lam;
+        k.ah.s = step_of(lam);
+        k.ah.m = it.m0;
+        k.ah.nx = h->nx;
+        k.ah.ny = h->ny;
+        k.ah.nz = h->nz;
+        k.ah.N = h->N;
+        k.ptrs[0] = &k.ah;
+        return true;
+    }
     if (it.kernel == kKernPrimalZVec || it.kernel == kKernPrimalZScalar) {
         k.pa.b = b;
         k.pa.d = it.r_src;
@@ -367,7 +398,8 @@ bool node_params(tvfgp_handle *h, const Item &it, const float *b, float lam, KAr
 }
 
 int build_graph(tvfgp_handle *h, GraphEntry &g, int variant, const float *b, float *p, float *r,
-                float lam, int nsteps, double t0, const std::vector<Item> &items, bool copy_back)
+                float lam, int nsteps, double t0, const std::vector<Item> &items, bool copy_back,
+                size_t copy_bytes)
 {
     destroy_graph(g);
     cudaError_t e = cudaGraphCreate(&g.graph, 0);
@@ -386,8 +418,7 @@ int build_graph(tvfgp_handle *h, GraphEntry &g, int variant, const float *b, flo
         prev = g.knodes[k];
     }
     if (e == cudaSuccess && copy_back)
-        e = cudaGraphAddMemcpyNode1D(&g.cnode, g.graph, &prev, 1, r, h->scratch,
-                                     sizeof(float) * 3 * static_cast<size_t>(h->N),
+        e = cudaGraphAddMemcpyNode1D(&g.cnode, g.graph, &prev, 1, r, h->scratch, copy_bytes,
                                      cudaMemcpyDeviceToDevice);
     if (e == cudaSuccess) e = cudaGraphInstantiate(&g.exec, g.graph, 0);
     if (e != cudaSuccess) {
@@ -397,6 +428,7 @@ int build_graph(tvfgp_handle *h, GraphEntry &g, int variant, const float *b, flo
     }
     g.nsteps = nsteps;
     g.variant = variant;
+    g.copy_bytes = copy_bytes;
     g.b = b;
     g.p = p;
     g.r = r;
@@ -419,8 +451,7 @@ int update_graph(tvfgp_handle *h, GraphEntry &g, const float *b, float *p, float
         e = cudaGraphExecKernelNodeSetParams(g.exec, g.knodes[k], &kp);
     }
     if (e == cudaSuccess && g.cnode)
-        e = cudaGraphExecMemcpyNodeSetParams1D(g.exec, g.cnode, r, h->scratch,
-                                               sizeof(float) * 3 * static_cast<size_t>(h->N),
+        e = cudaGraphExecMemcpyNodeSetParams1D(g.exec, g.cnode, r, h->scratch, g.copy_bytes,
                                                cudaMemcpyDeviceToDevice);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -436,7 +467,7 @@ int update_graph(tvfgp_handle *h, GraphEntry &g, const float *b, float *p, float
 
 int run_graph(tvfgp_handle *h, int variant, const float *b, float *p, float *r, float lam,
               int nsteps, double t0, const std::vector<Item> &items, bool copy_back,
-              cudaStream_t st)
+              size_t copy_bytes, cudaStream_t st)
 {
     GraphEntry *g = nullptr;
     for (auto &e : h->graphs)
@@ -447,7 +478,7 @@ int run_graph(tvfgp_handle *h, int variant, const float *b, float *p, float *r, 
         for (auto &e : h->graphs)
             if (!e.exec || e.use < victim->use) victim = &e;
         g = victim;
-        rc = build_graph(h, *g, variant, b, p, r, lam, nsteps, t0, items, copy_back);
+        rc = build_graph(h, *g, variant, b, p, r, lam, nsteps, t0, items, copy_back, copy_bytes);
     } else if (g->b != b || g->p != p || g->r != r || g->lam != lam || g->t0 != t0) {
         rc = update_graph(h, *g, b, p, r, lam, t0, items);
     }
@@ -690,7 +721,7 @@ int tvfgp_run(tvfgp_t h, const float *b, float *p, float *r, float lambda, int n
     plan_run(h, variant, vec_ok, p, r, m, items, &copy_back);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (h->graph_on) {
-        rc = run_graph(h, variant, b, p, r, lambda, nsteps, t0, items, copy_back, st);
+        rc = run_graph(h, variant, b, p, r, lambda, nsteps, t0, items, copy_back, 3 * v, st);
     } else {
         for (size_t k = 0; k < items.size() && rc == TVFGP_OK; ++k)
             rc = launch_item(h, items[k], b, lambda, st);
@@ -735,7 +766,99 @@ int tvfgp_primal(tvfgp_t h, const float *b, const float *dual, float lambda, flo
         primal_vec4<kPrimalBY><<<grid, dim3(32, kPrimalBY, 1), 0, st>>>(a);
     } else {
         dim3 grid((h->nx + 31) / 32, (h->ny + 7) / 8, h->nz);
-        primal_scalar<<<grid, dim3(32, 8, 1), 0, st>>>(a);
+        primal_scalar<float><<<grid, dim3(32, 8, 1), 0, st>>>(a);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return from_cuda(e);
+    h->launches += 1;
+    return TVFGP_OK;
+}
+
+int tvfgp_run_f16(tvfgp_t h, const float *b, unsigned short *p, unsigned short *r, float lambda,
+                  int nsteps, double t0, tvfgp_stream_t stream, double *t_final)
+{
+    if (!valid(h)) return TVFGP_ERR_ARG;
+    int rc;
+    if ((rc = check_ptr(b))) return rc;
+    if (p == nullptr || r == nullptr) return TVFGP_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(p) | reinterpret_cast<uintptr_t>(r)) & 1u) return TVFGP_ERR_ALIGN;
+    if ((rc = check_lambda(lambda))) return rc;
+    if (nsteps < 0 || !std::isfinite(t0) || t0 < 1.0) return TVFGP_ERR_ARG;
+    const size_t v = sizeof(float) * static_cast<size_t>(h->N);
+    const size_t d = sizeof(unsigned short) * 3 * static_cast<size_t>(h->N);
+    if (overlap(b, v, p, d) || overlap(b, v, r, d) || overlap(p, d, r, d) ||
+        overlap(b, v, h->scratch, 3 * v) || overlap(p, d, h->scratch, 3 * v) ||
+        overlap(r, d, h->scratch, 3 * v))
+        return TVFGP_ERR_ARG;
+    std::vector<double> m(static_cast<size_t>(nsteps));
+    double tf = t0;
+    tvfgp_momentum(t0, nsteps, m.data(), &tf);
+    if (nsteps == 0) {
+        if (t_final) *t_final = tf;
+        return TVFGP_OK;
+    }
+    const bool vec_ok = (h->nx % 4 == 0) && aligned16(b) && (reinterpret_cast<uintptr_t>(p) & 7u) == 0 &&
+                        (reinterpret_cast<uintptr_t>(r) & 7u) == 0;
+    const int kern = vec_ok ? kKernFusedH : kKernScalarH;
+    float *pf = reinterpret_cast<float *>(p), *rf = reinterpret_cast<float *>(r);
+    std::vector<Item> items;
+    for (int k = 0; k < nsteps; ++k) {
+        const bool even = (k % 2) == 0;
+        items.push_back({kern, pf, pf, even ? rf : h->scratch, even ? h->scratch : rf,
+                         static_cast<float>(m[k]), 0.0f});
+    }
+    const bool copy_back = (nsteps % 2) == 1;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (h->graph_on) {
+        rc = run_graph(h, kern, b, pf, rf, lambda, nsteps, t0, items, copy_back, d, st);
+    } else {
+        for (size_t k = 0; k < items.size() && rc == TVFGP_OK; ++k)
+            rc = launch_item(h, items[k], b, lambda, st);
+        if (rc == TVFGP_OK && copy_back) {
+            cudaError_t e = cudaMemcpyAsync(r, h->scratch, d, cudaMemcpyDeviceToDevice, st);
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                rc = from_cuda(e);
+            }
+        }
+    }
+    if (rc == TVFGP_OK) {
+        h->last_variant = vec_ok ? TVFGP_VARIANT_FUSED : TVFGP_VARIANT_SCALAR;
+        if (t_final) *t_final = tf;
+    }
+    return rc;
+}
+
+int tvfgp_primal_f16(tvfgp_t h, const float *b, const unsigned short *dual, float lambda, float *z,
+                     tvfgp_stream_t stream)
+{
+    if (!valid(h)) return TVFGP_ERR_ARG;
+    int rc;
+    if ((rc = check_ptr(b)) || (rc = check_ptr(z))) return rc;
+    if (dual == nullptr) return TVFGP_ERR_ARG;
+    if (reinterpret_cast<uintptr_t>(dual) & 1u) return TVFGP_ERR_ALIGN;
+    if ((rc = check_lambda(lambda))) return rc;
+    const size_t v = sizeof(float) * static_cast<size_t>(h->N);
+    if (overlap(z, v, b, v) || overlap(z, v, dual, sizeof(unsigned short) * 3 * static_cast<size_t>(h->N)))
+        return TVFGP_ERR_ARG;
+    PrimalArgsT<__half> a;
+    a.b = b;
+    a.d = reinterpret_cast<const __half *>(dual);
+    a.z = z;
+    a.lam = lambda;
+    a.nx = h->nx;
+    a.ny = h->ny;
+    a.nz = h->nz;
+    a.N = h->N;
+    const bool vec_ok = (h->nx % 4 == 0) && aligned16(b) && aligned16(z) &&
+                        (reinterpret_cast<uintptr_t>(dual) & 7u) == 0;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (vec_ok) {
+        dim3 grid((h->nx / 4 + 31) / 32, (h->ny + kPrimalBY - 1) / kPrimalBY, h->nz);
+        primal_vec4<kPrimalBY, __half><<<grid, dim3(32, kPrimalBY, 1), 0, st>>>(a);
+    } else {
+        dim3 grid((h->nx + 31) / 32, (h->ny + 7) / 8, h->nz);
+        primal_scalar<__half><<<grid, dim3(32, 8, 1), 0, st>>>(a);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return from_cuda(e);
@@ -884,7 +1007,7 @@ extern "C" int tvfgp_run_noalloc(int nx, int ny, int nz, const float *b, float *
         block = dim3(32, kFusedBY, 1);
         grid = dim3((nx / 4 + 31) / 32, (ny + kFusedBY - 1) / kFusedBY, (nz + kFusedZC - 1) / kFusedZC);
     } else {
-        fn = reinterpret_cast<const void *>(&fgp_step_scalar);
+        fn = reinterpret_cast<const void *>(&fgp_step_scalar<float>);
         block = dim3(32, 8, 1);
         grid = dim3((nx + 31) / 32, (ny + 7) / 8, nz);
     }

@@ -1,9 +1,9 @@
 // ZMARCH2_TMA: two FGP steps per pass over HBM (temporal blocking of the
 // z-march).
 //
-// The page ("TV solver: the FGP step on the GPU", "Profiler counters") ends
-// at the compulsory 13 volumes per step: the only way to a cheaper step is to
-// move fewer bytes.  Without changing the result, that means computing two
+// The page ("TV solver: the FGP step on the GPU", "Profiler counters") shows
+// the step at its compulsory 13 volumes, so a cheaper step has to move fewer
+// bytes.  Without changing the result, that means computing two
 // steps from one read of (b, p^k, r^k) and one write of (p^{k+2}, r^{k+2}):
 // 13 volumes per two steps.  The intermediate p^{k+1}, r^{k+1} never leave
 // shared memory.

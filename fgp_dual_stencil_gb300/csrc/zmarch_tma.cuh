@@ -1,8 +1,8 @@
 // ZMARCH_TMA variant of the FGP step: an x-y tile marching along z, with the
 // planes of b and r staged in shared memory by TMA (page "TV solver: the FGP
-// step on the GPU", section "Variants", fourth row: x-y tiles marching along
-// z, two planes of r and z on chip; rebuilt here around the Blackwell tensor
-// memory accelerator instead of plain loads and barriers).
+// step on the GPU", section "Variants", the marching-tile row; rebuilt here
+// around the Blackwell tensor memory accelerator instead of plain loads and
+// barriers).
 //
 // A CTA owns the columns x0..x0+TX-1 (TX = 32 by default) and computes z
 // for the ROWS = 16 rows y0..y0+15 of each plane; it updates the dual on the

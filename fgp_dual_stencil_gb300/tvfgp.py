@@ -67,6 +67,8 @@ def _load():
         "tvfgp_debug_timeout_probe": ([vp, i, vp], i),
         "tvfgp_run_noalloc": ([i, i, i, vp, vp, vp, f, i, d, vp, ctypes.POINTER(d)], i),
         "tvfgp_host_alloc": ([ctypes.c_size_t, i, ctypes.POINTER(vp)], i),
+        "tvfgp_run_f16": ([vp, vp, vp, vp, f, i, d, vp, ctypes.POINTER(d)], i),
+        "tvfgp_primal_f16": ([vp, vp, vp, f, vp, vp], i),
         "tvfgp_host_free": ([vp], i),
         "tvfgp_strerror": ([i], ctypes.c_char_p),
         "tvfgp_version": ([], i),
@@ -97,6 +99,19 @@ def _addr(x, n: int | None, name: str):
         raise TypeError("%s must be a torch tensor or an int address" % name)
     if not x.is_cuda or x.dtype != torch.float32 or not x.is_contiguous():
         raise ValueError("%s must be a contiguous float32 CUDA tensor" % name)
+    if n is not None and x.numel() != n:
+        raise ValueError("%s has %d elements, expected %d" % (name, x.numel(), n))
+    return x.data_ptr()
+
+
+def _addr16(x, n: int | None, name: str):
+    """Device address of a torch float16 CUDA tensor (the binary16 dual)."""
+    if x is None or isinstance(x, int):
+        return x
+    import torch
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dtype != torch.float16 \
+            or not x.is_contiguous():
+        raise ValueError("%s must be a contiguous float16 CUDA tensor" % name)
     if n is not None and x.numel() != n:
         raise ValueError("%s has %d elements, expected %d" % (name, x.numel(), n))
     return x.data_ptr()
@@ -177,6 +192,21 @@ def tvfgp_primal(h: int, b, dual, lam: float, z, stream=None) -> None:
     """z = max(b - lam * L(dual), 0)."""
     _ok(_lib.tvfgp_primal(h, _addr(b, None, "b"), _addr(dual, None, "dual"), float(lam),
                           _addr(z, None, "z"), _stream(stream)), "tvfgp_primal")
+
+
+def tvfgp_run_f16(h: int, b, p16, r16, lam: float, nsteps: int, t0: float = 1.0, stream=None,
+                  n: int | None = None) -> float:
+    """tvfgp_run with p and r stored as float16 tensors; returns t after the last step."""
+    tf = ctypes.c_double(0.0)
+    _ok(_lib.tvfgp_run_f16(h, _addr(b, n, "b"), _addr16(p16, None if n is None else 3 * n, "p"),
+                           _addr16(r16, None if n is None else 3 * n, "r"), float(lam), int(nsteps),
+                           float(t0), _stream(stream), ctypes.byref(tf)), "tvfgp_run_f16")
+    return tf.value
+
+
+def tvfgp_primal_f16(h: int, b, dual16, lam: float, z, stream=None) -> None:
+    _ok(_lib.tvfgp_primal_f16(h, _addr(b, None, "b"), _addr16(dual16, None, "dual"), float(lam),
+                              _addr(z, None, "z"), _stream(stream)), "tvfgp_primal_f16")
 
 
 def tvfgp_check(h: int, stream=None) -> int:
@@ -274,6 +304,16 @@ class Tvfgp:
             import torch
             z = torch.empty_like(b)
         tvfgp_primal(self.h, b, dual, lam, z, stream)
+        return z
+
+    def run_f16(self, b, p16, r16, lam, nsteps, t0=1.0, stream=None) -> float:
+        return tvfgp_run_f16(self.h, b, p16, r16, lam, nsteps, t0, stream, n=self.n)
+
+    def primal_f16(self, b, dual16, lam, z=None, stream=None):
+        if z is None:
+            import torch
+            z = torch.empty_like(b)
+        tvfgp_primal_f16(self.h, b, dual16, lam, z, stream)
         return z
 
     def set_variant(self, v) -> None:

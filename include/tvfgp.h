@@ -72,8 +72,8 @@ enum tvfgp_variant {
     TVFGP_VARIANT_AUTO = 0,      /* the measured default; falls back to SCALAR when the
                                     shape or alignment rules out the vector paths */
     TVFGP_VARIANT_FUSED = 1,     /* one kernel per step: float4 along x, the voxel's own p
-                                    and r loads first, z recomputed at the voxel and its
-                                    three upper neighbours, carried along z in registers.
+                                    and r loads first, z evaluated at the voxel and at its
+                                    +x, +y, +z neighbours, carried along z in registers.
                                     Needs nx % 4 == 0 and 16-byte aligned pointers. */
     TVFGP_VARIANT_SCALAR = 2,    /* one voxel per thread; any shape and alignment */
     TVFGP_VARIANT_ZMARCH_TMA = 3, /* x-y tile marching along z, planes of b, r and p staged
@@ -145,6 +145,23 @@ int tvfgp_step(tvfgp_t h, const float *b, float *p, const float *r_src, float *r
  * b or dual. */
 int tvfgp_primal(tvfgp_t h, const float *b, const float *dual, float lambda, float *z,
                  tvfgp_stream_t stream);
+
+/* tvfgp_run with the dual stored in half precision: p and r are [3N] arrays
+ * of IEEE 754 binary16 values (their bits as unsigned short), b stays fp32.
+ * Each step widens the stored values exactly, computes in the fp32 canonical
+ * order, and rounds each stored result once to binary16 (nearest, ties to
+ * even).  It moves 28 bytes per voxel and step instead of 52 and changes the
+ * result: the page ("Profiler counters") counts a half-precision dual among
+ * the ways to move fewer bytes.  The vector kernel runs when nx % 4 == 0, b
+ * is 16-byte and p, r 8-byte aligned, the scalar kernel otherwise.  p and r
+ * must be 2-byte aligned (TVFGP_ERR_ALIGN).  The handle's scratch buffer
+ * holds the other r, so the call does not allocate. */
+int tvfgp_run_f16(tvfgp_t h, const float *b, unsigned short *p, unsigned short *r, float lambda,
+                  int nsteps, double t0, tvfgp_stream_t stream, double *t_final);
+
+/* tvfgp_primal for a binary16 dual field. */
+int tvfgp_primal_f16(tvfgp_t h, const float *b, const unsigned short *dual, float lambda, float *z,
+                     tvfgp_stream_t stream);
 
 /* Host only: the momentum weights m[0..nsteps-1] of a run started at t0 (in
  * double; the kernels receive each rounded once to float) and t after the

@@ -79,6 +79,21 @@ def _load():
             f = getattr(lib, "oracle_fgp_run" + suf)
             f.argtypes = [c_int, c_int, c_int, vp, vp, vp, real, c_int, c_dbl, vp]
             f.restype = c_int
+        lib.oracle_half_to_float.argtypes = [ctypes.c_ushort]
+        lib.oracle_half_to_float.restype = ctypes.c_float
+        lib.oracle_float_to_half.argtypes = [ctypes.c_float]
+        lib.oracle_float_to_half.restype = ctypes.c_ushort
+        for name in ("oracle_half_to_float_array", "oracle_float_to_half_array"):
+            getattr(lib, name).argtypes = [vp, vp, ctypes.c_size_t]
+            getattr(lib, name).restype = None
+        lib.oracle_primal_h16.argtypes = [c_int, c_int, c_int, vp, vp, ctypes.c_float, vp]
+        lib.oracle_primal_h16.restype = None
+        lib.oracle_fgp_step_h16.argtypes = [c_int, c_int, c_int, vp, vp, vp, vp, ctypes.c_float,
+                                            ctypes.c_float]
+        lib.oracle_fgp_step_h16.restype = c_int
+        lib.oracle_fgp_run_h16.argtypes = [c_int, c_int, c_int, vp, vp, vp, ctypes.c_float, c_int,
+                                           c_dbl, vp]
+        lib.oracle_fgp_run_h16.restype = c_int
         _lib = lib
         return lib
 
@@ -183,6 +198,67 @@ def fgp_run(b, p, r, lam, nsteps, t0=1.0):
     tf = ctypes.c_double(0.0)
     rc = getattr(_load(), "oracle_fgp_run" + _suffix(b.dtype))(
         nx, ny, nz, _ptr(b), _ptr(p), _ptr(r), lam, int(nsteps), float(t0), ctypes.byref(tf))
+    if rc != 0:
+        raise MemoryError("oracle could not allocate its work buffers")
+    return tf.value
+
+
+# ---------------------------------------------------------------------------
+# binary16 storage of the dual (arrays of uint16 holding the IEEE bits)
+# ---------------------------------------------------------------------------
+
+def half_to_float(h: np.ndarray) -> np.ndarray:
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    out = np.empty(h.shape, dtype=np.float32)
+    _load().oracle_half_to_float_array(_ptr(h), _ptr(out), h.size)
+    return out
+
+
+def float_to_half(f: np.ndarray) -> np.ndarray:
+    """Round float32 values to binary16 (nearest, ties to even); uint16 bits."""
+    f = np.ascontiguousarray(f, dtype=np.float32)
+    out = np.empty(f.shape, dtype=np.uint16)
+    _load().oracle_float_to_half_array(_ptr(f), _ptr(out), f.size)
+    return out
+
+
+def _check_dual16(name, a, shape):
+    if not isinstance(a, np.ndarray) or a.shape != (3,) + tuple(shape) or a.dtype != np.uint16 \
+            or not a.flags.c_contiguous:
+        raise ValueError("%s must be a C-contiguous uint16 array of shape (3,)+%s" % (name, tuple(shape)))
+
+
+def primal_h16(b, dual16, lam):
+    _check_scalar("b", b, np.float32)
+    _check_dual16("dual", dual16, b.shape)
+    nz, ny, nx = b.shape
+    z = np.empty_like(b)
+    _load().oracle_primal_h16(nx, ny, nz, _ptr(b), _ptr(dual16), lam, _ptr(z))
+    return z
+
+
+def fgp_step_h16(b, p16, r_src16, lam, m):
+    """One step with binary16 storage; p16 updated in place; returns r_dst16."""
+    _check_scalar("b", b, np.float32)
+    _check_dual16("p", p16, b.shape)
+    _check_dual16("r_src", r_src16, b.shape)
+    nz, ny, nx = b.shape
+    r_dst = np.empty_like(r_src16)
+    rc = _load().oracle_fgp_step_h16(nx, ny, nz, _ptr(b), _ptr(p16), _ptr(r_src16), _ptr(r_dst), lam, m)
+    if rc != 0:
+        raise MemoryError("oracle could not allocate its work buffers")
+    return r_dst
+
+
+def fgp_run_h16(b, p16, r16, lam, nsteps, t0=1.0):
+    """nsteps steps with binary16 storage of p and r (updated in place)."""
+    _check_scalar("b", b, np.float32)
+    _check_dual16("p", p16, b.shape)
+    _check_dual16("r", r16, b.shape)
+    nz, ny, nx = b.shape
+    tf = ctypes.c_double(0.0)
+    rc = _load().oracle_fgp_run_h16(nx, ny, nz, _ptr(b), _ptr(p16), _ptr(r16), lam, int(nsteps),
+                                    float(t0), ctypes.byref(tf))
     if rc != 0:
         raise MemoryError("oracle could not allocate its work buffers")
     return tf.value
