@@ -170,13 +170,39 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _strip_comments(src: str) -> str:
+    """C++ source without comments and blank-line differences (string
+    literals kept), so that comment edits keep the hash."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"':
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (ln.rstrip() for ln in "".join(out).splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_hash() -> str:
-    """Hash of the device code of the step kernels (the files that hold the
-    kernels and their launch shapes); host-only changes keep it."""
+    """Hash of the device code of the step kernels (the headers that hold the
+    kernels and their launch shapes), comments excluded; host-only and
+    comment-only changes keep it."""
     h = hashlib.sha256()
-    for fn in ("fgp_kernels.cuh", "zmarch_tma.cuh"):
-        with open(os.path.join(ROOT, "fgp_dual_stencil_gb300", "csrc", fn), "rb") as f:
-            h.update(f.read())
+    for fn in ("fgp_kernels.cuh", "zmarch_tma.cuh", "zmarch2_tma.cuh"):
+        with open(os.path.join(ROOT, "fgp_dual_stencil_gb300", "csrc", fn)) as f:
+            h.update(_strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

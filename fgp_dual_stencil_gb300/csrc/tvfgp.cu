@@ -82,6 +82,7 @@ struct tvfgp_handle {
     float *zscratch;            // N floats, two-kernel variant only
     int *d_err;
     ZmarchPlan zplan;
+    ZmarchPlan zplan_h;            // the z-march over a binary16 dual
     Zmarch2Plan z2plan;
     GraphEntry graphs[kGraphSlots];
     unsigned long long graph_clock;
@@ -181,6 +182,7 @@ constexpr int kKernDualZScalar = 103;
 // One-step kernels on a dual stored as binary16.
 constexpr int kKernFusedH = 120;
 constexpr int kKernScalarH = 121;
+constexpr int kKernZmarchH = 122;
 
 // One kernel launch of a run: a single step (p updated in place, r_src ->
 // r_dst), a two-step launch (p_src -> p_dst and r_src -> r_dst), or a half
@@ -199,6 +201,7 @@ struct KArgs {
     StepArgs a;
     StepArgsT<__half> ah;
     ZmarchArgs za;
+    ZmarchArgsT<__half> zah;
     Zmarch2Args z2;
     PrimalArgs pa;
     DualArgs da;
@@ -215,6 +218,14 @@ LaunchCfg item_cfg(const tvfgp_handle *h, int kernel)
     if (kernel == kKernScalarH) {
         LaunchCfg c = step_cfg(h, TVFGP_VARIANT_SCALAR);
         c.func = reinterpret_cast<const void *>(&fgp_step_scalar<__half>);
+        return c;
+    }
+    if (kernel == kKernZmarchH) {
+        LaunchCfg c;
+        c.func = zmarch_kernel<__half>();
+        c.block = dim3(zmarch_threads<__half>(), 1, 1);
+        c.grid = zmarch_grid(h->zplan_h);
+        c.smem = zmarch_smem_bytes<__half>();
         return c;
     }
     if (kernel >= kKernPrimalZVec) {
@@ -243,7 +254,7 @@ LaunchCfg item_cfg(const tvfgp_handle *h, int kernel)
 
 bool fill_item(const tvfgp_handle *h, const Item &it, const float *b, float lam, KArgs &k)
 {
-    if (it.kernel == kKernFusedH || it.kernel == kKernScalarH) {
+    if (it.kernel == kKernFusedH || it.kernel == kKernScalarH || it.kernel == kKernZmarchH) {
         // the dual buffers of a binary16 run travel as float* in an Item
         k.ah.b = b;
         k.ah.p = reinterpret_cast<__half *>(it.p_dst);
@@ -256,6 +267,10 @@ bool fill_item(const tvfgp_handle *h, const Item &it, const float *b, float lam,
         k.ah.ny = h->ny;
         k.ah.nz = h->nz;
         k.ah.N = h->N;
+        if (it.kernel == kKernZmarchH) {
+            k.ptrs[0] = &k.zah;
+            return zmarch_fill(h->zplan_h, k.ah, h->d_err, k.zah);
+        }
         k.ptrs[0] = &k.ah;
         return true;
     }
@@ -586,6 +601,7 @@ int tvfgp_create_ex(int nx, int ny, int nz, int variant, unsigned flags, tvfgp_t
     if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(int));
     if (e == cudaSuccess) {
         if (zmarch_plan(nx, ny, nz, &h->zplan) != TVFGP_OK ||
+            zmarch_plan<__half>(nx, ny, nz, &h->zplan_h) != TVFGP_OK ||
             zmarch2_plan(nx, ny, nz, &h->z2plan) != TVFGP_OK)
             e = cudaErrorInvalidValue;
     }
@@ -799,7 +815,18 @@ int tvfgp_run_f16(tvfgp_t h, const float *b, unsigned short *p, unsigned short *
     }
     const bool vec_ok = (h->nx % 4 == 0) && aligned16(b) && (reinterpret_cast<uintptr_t>(p) & 7u) == 0 &&
                         (reinterpret_cast<uintptr_t>(r) & 7u) == 0;
-    const int kern = vec_ok ? kKernFusedH : kKernScalarH;
+    // The z-march moves rows of whole 16-byte units: nx % 8 == 0 and every
+    // component's base 16-byte aligned (N is then a multiple of 8).
+    const bool march_ok = zmarch_supported<__half>(h->nx, h->ny, h->nz) && zmarch_available() &&
+                          aligned16(b) && aligned16(p) && aligned16(r);
+    int kern = kKernScalarH, ran = TVFGP_VARIANT_SCALAR;
+    if (h->variant != TVFGP_VARIANT_SCALAR && h->variant != TVFGP_VARIANT_FUSED && march_ok) {
+        kern = kKernZmarchH;
+        ran = TVFGP_VARIANT_ZMARCH_TMA;
+    } else if (h->variant != TVFGP_VARIANT_SCALAR && vec_ok) {
+        kern = kKernFusedH;
+        ran = TVFGP_VARIANT_FUSED;
+    }
     float *pf = reinterpret_cast<float *>(p), *rf = reinterpret_cast<float *>(r);
     std::vector<Item> items;
     for (int k = 0; k < nsteps; ++k) {
@@ -823,7 +850,7 @@ int tvfgp_run_f16(tvfgp_t h, const float *b, unsigned short *p, unsigned short *
         }
     }
     if (rc == TVFGP_OK) {
-        h->last_variant = vec_ok ? TVFGP_VARIANT_FUSED : TVFGP_VARIANT_SCALAR;
+        h->last_variant = ran;
         if (t_final) *t_final = tf;
     }
     return rc;

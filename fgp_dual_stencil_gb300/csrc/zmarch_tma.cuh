@@ -22,6 +22,13 @@
 // TMA copy issued planes ahead, before any wait on it: the voxel's own p and
 // r arrive with their plane, and no thread issues a global load.
 //
+// The kernel is a template on the storage of p and r: fp32, or binary16
+// (TMA boxes of halves, widened exactly to fp32 on their way out of shared
+// memory; the step's arithmetic is the same fp32 sequence, and stored
+// values are rounded to nearest-even).  Half boxes start on 8-column
+// boundaries, so the r0 box then starts at x0-8 and the r1, r2 boxes span
+// x0..x0+TX+7.
+//
 // Every wait on a TMA barrier is bounded; on timeout the kernel sets the
 // caller's error word, drains its outstanding copies (again bounded) and
 // returns, so the context stays usable (tvfgp_check reports it).
@@ -34,77 +41,111 @@
 
 namespace tvfgp {
 
+// Tile shape of the fp32 march, and the _H twins for a binary16 dual.
 #ifndef TVFGP_ZM_TX
 #define TVFGP_ZM_TX 32
 #endif
 #ifndef TVFGP_ZM_ROWS
 #define TVFGP_ZM_ROWS 16
 #endif
+#ifndef TVFGP_ZM_STAGES
+#define TVFGP_ZM_STAGES 4
+#endif
 #ifndef TVFGP_ZM_MINB
 #define TVFGP_ZM_MINB 3
+#endif
+#ifndef TVFGP_ZM_TX_H
+#define TVFGP_ZM_TX_H 32
+#endif
+#ifndef TVFGP_ZM_ROWS_H
+#define TVFGP_ZM_ROWS_H 16
+#endif
+#ifndef TVFGP_ZM_STAGES_H
+#define TVFGP_ZM_STAGES_H 4
+#endif
+#ifndef TVFGP_ZM_MINB_H
+#define TVFGP_ZM_MINB_H 4
 #endif
 #ifndef TVFGP_ZM_L2PROMO
 #define TVFGP_ZM_L2PROMO CU_TENSOR_MAP_L2_PROMOTION_L2_256B
 #endif
-constexpr int ZM_TX = TVFGP_ZM_TX;        // tile width (voxels)
-constexpr int ZM_ROWS = TVFGP_ZM_ROWS;    // rows whose z is computed per plane
-constexpr int ZM_TY = ZM_ROWS - 1;        // rows whose dual is updated
-constexpr int ZM_QX = ZM_TX / 4;          // quads per row
-constexpr int ZM_THREADS = ZM_QX * ZM_ROWS;
-#ifndef TVFGP_ZM_STAGES
-#define TVFGP_ZM_STAGES 4
-#endif
-constexpr int ZM_STAGES = TVFGP_ZM_STAGES;   // TMA ring depth (planes in flight)
 constexpr int ZM_MAX_POLLS = 1 << 22;     // bound of every barrier wait
 
-constexpr int ZM_BW = ZM_TX + 4;          // width of the b, r1, r2 boxes
-constexpr int ZM_W0 = ZM_TX + 8;          // width of the r0 box
-constexpr int ZM_HB = ZM_ROWS;            // height of the b, r0, r2 boxes
-constexpr int ZM_H1 = ZM_ROWS + 1;        // height of the r1 box
-constexpr int ZM_ZP = ZM_TX + 4;          // row pitch of a z plane
-
 constexpr int zm_round128(int v) { return (v + 127) / 128 * 128; }
-constexpr int ZM_BYTES_B = ZM_BW * ZM_HB * 4;
-constexpr int ZM_BYTES_R0 = ZM_W0 * ZM_HB * 4;
-constexpr int ZM_BYTES_R1 = ZM_BW * ZM_H1 * 4;
-constexpr int ZM_BYTES_R2 = ZM_BW * ZM_HB * 4;
-constexpr int ZM_BYTES_P = ZM_TX * ZM_TY * 4;      // one component of p
-constexpr int ZM_OFF_B = 0;
-constexpr int ZM_OFF_R0 = zm_round128(ZM_OFF_B + ZM_BYTES_B);
-constexpr int ZM_OFF_R1 = zm_round128(ZM_OFF_R0 + ZM_BYTES_R0);
-constexpr int ZM_OFF_R2 = zm_round128(ZM_OFF_R1 + ZM_BYTES_R1);
-constexpr int ZM_OFF_P0 = zm_round128(ZM_OFF_R2 + ZM_BYTES_R2);
-constexpr int ZM_OFF_P1 = zm_round128(ZM_OFF_P0 + ZM_BYTES_P);
-constexpr int ZM_OFF_P2 = zm_round128(ZM_OFF_P1 + ZM_BYTES_P);
-constexpr int ZM_STAGE_STRIDE = zm_round128(ZM_OFF_P2 + ZM_BYTES_P);
-constexpr int ZM_STAGE_TX_BR = ZM_BYTES_B + ZM_BYTES_R0 + ZM_BYTES_R1 + ZM_BYTES_R2;
-constexpr int ZM_STAGE_TX = ZM_STAGE_TX_BR + 3 * ZM_BYTES_P;
-constexpr int ZM_OFF_PREV = ZM_STAGES * ZM_STAGE_STRIDE;               // r2 of plane z0-1
-constexpr int ZM_OFF_Z = zm_round128(ZM_OFF_PREV + ZM_BYTES_R2);       // 3 z planes
-constexpr int ZM_BYTES_Z = 3 * ZM_ROWS * ZM_ZP * 4;
-constexpr int ZM_OFF_BAR = zm_round128(ZM_OFF_Z + ZM_BYTES_Z);         // STAGES+1 barriers
-constexpr int ZM_OFF_FLAG = ZM_OFF_BAR + 8 * (ZM_STAGES + 1);
-constexpr int ZM_SMEM = ZM_OFF_FLAG + 16 + 128;                        // + base alignment
 
-static_assert(ZM_TX % 4 == 0 && ZM_W0 <= 256 && ZM_H1 <= 256, "TMA box limits");
-// Plane q's slot holds its p until the dual update of q, one iteration after
-// its b and r were consumed; the next plane is loaded into the slot of q-1,
-// so a plane is issued S-1 iterations before its wait: S >= 3.
-static_assert(ZM_STAGES >= 3, "the ring needs three slots");
-static_assert(ZM_SMEM * TVFGP_ZM_MINB <= 227 * 1024, "CTAs per SM must fit in shared memory");
+// Tile and shared-memory layout of one z-march for a dual stored as TS
+// (float or __half; b and z are always fp32).  A CTA owns TX columns and
+// computes z on ROWS rows of each plane, updating the dual on the first
+// TY = ROWS-1; a thread owns a quad of 4 x voxels of one row.  A TMA box
+// starts on a 16-byte column, so the r0 box starts XO = 16 / sizeof(TS)
+// columns left of the tile (its column XO-1 is r0(x0-1)) and the r1, r2
+// boxes are XO columns wider than the tile (their column TX is the x+1
+// halo): 4 columns for fp32, 8 for binary16.
+template <typename TS>
+struct ZmLayout {
+    static constexpr bool F32 = sizeof(TS) == 4;
+    static constexpr int TX = F32 ? TVFGP_ZM_TX : TVFGP_ZM_TX_H;          // tile width (voxels)
+    static constexpr int ROWS = F32 ? TVFGP_ZM_ROWS : TVFGP_ZM_ROWS_H;    // rows whose z is computed
+    static constexpr int TY = ROWS - 1;                                   // rows whose dual is updated
+    static constexpr int QX = TX / 4;                                     // quads per row
+    static constexpr int THREADS = QX * ROWS;
+    static constexpr int STAGES = F32 ? TVFGP_ZM_STAGES : TVFGP_ZM_STAGES_H;  // planes in flight
+    // resident CTAs per SM the registers are budgeted for
+    static constexpr int MINB = F32 ? TVFGP_ZM_MINB : TVFGP_ZM_MINB_H;
+    static constexpr int BW = TX + 4;           // width of the b box (fp32)
+    static constexpr int HB = ROWS;             // height of the b, r0, r2 boxes
+    static constexpr int H1 = ROWS + 1;         // height of the r1 box
+    static constexpr int ZP = TX + 4;           // row pitch of a z plane
+    static constexpr int ES = static_cast<int>(sizeof(TS));
+    static constexpr int XO = 16 / ES;
+    static constexpr int W0 = TX + 2 * XO;      // width of the r0 box
+    static constexpr int RW = TX + XO;          // width of the r1, r2 boxes
+    static constexpr int BYTES_B = BW * HB * 4;
+    static constexpr int BYTES_R0 = W0 * HB * ES;
+    static constexpr int BYTES_R1 = RW * H1 * ES;
+    static constexpr int BYTES_R2 = RW * HB * ES;
+    static constexpr int BYTES_P = TX * TY * ES;     // one component of p
+    static constexpr int OFF_B = 0;
+    static constexpr int OFF_R0 = zm_round128(OFF_B + BYTES_B);
+    static constexpr int OFF_R1 = zm_round128(OFF_R0 + BYTES_R0);
+    static constexpr int OFF_R2 = zm_round128(OFF_R1 + BYTES_R1);
+    static constexpr int OFF_P0 = zm_round128(OFF_R2 + BYTES_R2);
+    static constexpr int OFF_P1 = zm_round128(OFF_P0 + BYTES_P);
+    static constexpr int OFF_P2 = zm_round128(OFF_P1 + BYTES_P);
+    static constexpr int STAGE_STRIDE = zm_round128(OFF_P2 + BYTES_P);
+    static constexpr int STAGE_TX_BR = BYTES_B + BYTES_R0 + BYTES_R1 + BYTES_R2;
+    static constexpr int STAGE_TX = STAGE_TX_BR + 3 * BYTES_P;
+    static constexpr int OFF_PREV = STAGES * STAGE_STRIDE;               // r2 of plane z0-1
+    static constexpr int OFF_Z = zm_round128(OFF_PREV + BYTES_R2);       // 3 z planes
+    static constexpr int BYTES_Z = 3 * ROWS * ZP * 4;
+    static constexpr int OFF_BAR = zm_round128(OFF_Z + BYTES_Z);         // STAGES+1 barriers
+    static constexpr int OFF_FLAG = OFF_BAR + 8 * (STAGES + 1);
+    static constexpr int SMEM = OFF_FLAG + 16 + 128;                     // + base alignment
+
+    static_assert(TX % 4 == 0 && W0 <= 256 && H1 <= 256 && THREADS <= 1024, "TMA box limits");
+    static_assert((W0 * ES) % 16 == 0 && (RW * ES) % 16 == 0 && (TX * ES) % 16 == 0,
+                  "TMA box rows are whole 16-byte units");
+    static_assert(SMEM * MINB <= 227 * 1024, "CTAs per SM must fit in shared memory");
+    // Plane q's slot holds its p until the dual update of q, one iteration
+    // after its b and r were consumed; the next plane is loaded into the slot
+    // of q-1, so a plane is issued S-1 iterations before its wait: S >= 3.
+    static_assert(STAGES >= 3, "the ring needs three slots");
+};
 
 struct ZmarchPlan {
     dim3 grid;
     int zc;                       // planes per CTA
 };
 
-struct ZmarchArgs {
+template <typename TS>
+struct ZmarchArgsT {
     CUtensorMap tb, t0, t1, t2;   // b, r0, r1, r2 of the r read by this step
     CUtensorMap tp0, tp1, tp2;    // the three components of p
-    StepArgs a;
+    StepArgsT<TS> a;
     int *err;
     int zc;                       // planes per CTA (grid.z = ceil(nz / zc))
 };
+using ZmarchArgs = ZmarchArgsT<float>;
 
 // ---------------------------------------------------------------------------
 // device helpers (TMA, mbarrier)
@@ -148,63 +189,73 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
 }
 
 __device__ __forceinline__ float4 lds4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 lds4(const __half *p) { return widen4(*reinterpret_cast<const uint2 *>(p)); }
+__device__ __forceinline__ float lds1(const float *p) { return *p; }
+__device__ __forceinline__ float lds1(const __half *p) { return __half2float(*p); }
 
 // z of the quad (row, 4*qx) of a staged plane; r2lo is r2 of the plane below.
+template <typename TS>
 __device__ __forceinline__ void zm_quad(const unsigned char *st, int row, int qx, float4 r2lo,
                                         float lam, float4 &R0, float4 &R1, float4 &R2, float4 &Z)
 {
-    const float *B = reinterpret_cast<const float *>(st + ZM_OFF_B);
-    const float *S0 = reinterpret_cast<const float *>(st + ZM_OFF_R0);
-    const float *S1 = reinterpret_cast<const float *>(st + ZM_OFF_R1);
-    const float *S2 = reinterpret_cast<const float *>(st + ZM_OFF_R2);
+    using L = ZmLayout<TS>;
+    const float *B = reinterpret_cast<const float *>(st + L::OFF_B);
+    const TS *S0 = reinterpret_cast<const TS *>(st + L::OFF_R0);
+    const TS *S1 = reinterpret_cast<const TS *>(st + L::OFF_R1);
+    const TS *S2 = reinterpret_cast<const TS *>(st + L::OFF_R2);
     const int c = 4 * qx;
-    const float4 Bq = lds4(B + row * ZM_BW + c);
-    R0 = lds4(S0 + row * ZM_W0 + 4 + c);
-    const float left = S0[row * ZM_W0 + 3 + c];
-    R1 = lds4(S1 + (row + 1) * ZM_BW + c);
-    const float4 R1lo = lds4(S1 + row * ZM_BW + c);
-    R2 = lds4(S2 + row * ZM_BW + c);
+    const float4 Bq = lds4(B + row * L::BW + c);
+    R0 = lds4(S0 + row * L::W0 + L::XO + c);
+    const float left = lds1(S0 + row * L::W0 + L::XO - 1 + c);
+    R1 = lds4(S1 + (row + 1) * L::RW + c);
+    const float4 R1lo = lds4(S1 + row * L::RW + c);
+    R2 = lds4(S2 + row * L::RW + c);
     Z = zquad(Bq, R0, R1, R2, left, R1lo, r2lo, lam);
 }
 
 // z at column x0+TX of a row (the x+1 neighbour of the tile's last quad).
+template <typename TS>
 __device__ __forceinline__ float zm_halo(const unsigned char *st, int row, float r2lo, float lam,
                                          float &r2here)
 {
-    const float *B = reinterpret_cast<const float *>(st + ZM_OFF_B);
-    const float *S0 = reinterpret_cast<const float *>(st + ZM_OFF_R0);
-    const float *S1 = reinterpret_cast<const float *>(st + ZM_OFF_R1);
-    const float *S2 = reinterpret_cast<const float *>(st + ZM_OFF_R2);
-    r2here = S2[row * ZM_BW + ZM_TX];
-    return zval(B[row * ZM_BW + ZM_TX], lam,
-                __fsub_rn(S0[row * ZM_W0 + 4 + ZM_TX], S0[row * ZM_W0 + 3 + ZM_TX]),
-                __fsub_rn(S1[(row + 1) * ZM_BW + ZM_TX], S1[row * ZM_BW + ZM_TX]),
+    using L = ZmLayout<TS>;
+    const float *B = reinterpret_cast<const float *>(st + L::OFF_B);
+    const TS *S0 = reinterpret_cast<const TS *>(st + L::OFF_R0);
+    const TS *S1 = reinterpret_cast<const TS *>(st + L::OFF_R1);
+    const TS *S2 = reinterpret_cast<const TS *>(st + L::OFF_R2);
+    r2here = lds1(S2 + row * L::RW + L::TX);
+    return zval(B[row * L::BW + L::TX], lam,
+                __fsub_rn(lds1(S0 + row * L::W0 + L::XO + L::TX), lds1(S0 + row * L::W0 + L::XO - 1 + L::TX)),
+                __fsub_rn(lds1(S1 + (row + 1) * L::RW + L::TX), lds1(S1 + row * L::RW + L::TX)),
                 __fsub_rn(r2here, r2lo));
 }
 
-__global__ void __launch_bounds__(ZM_THREADS, TVFGP_ZM_MINB) fgp_step_zmarch_tma(const __grid_constant__ ZmarchArgs za)
+template <typename TS>
+__global__ void __launch_bounds__(ZmLayout<TS>::THREADS, ZmLayout<TS>::MINB)
+    fgp_step_zmarch_tma(const __grid_constant__ ZmarchArgsT<TS> za)
 {
+    using L = ZmLayout<TS>;
     extern __shared__ unsigned char zm_raw[];
     unsigned char *smem = zm_raw + ((128 - (smem_addr(zm_raw) & 127)) & 127);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + ZM_OFF_BAR);   // [STAGES] + prev
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + ZM_OFF_FLAG);
-    float *zpl = reinterpret_cast<float *>(smem + ZM_OFF_Z);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);   // [STAGES] + prev
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_FLAG);
+    float *zpl = reinterpret_cast<float *>(smem + L::OFF_Z);
 
-    const StepArgs &a = za.a;
+    const StepArgsT<TS> &a = za.a;
     const int nx = a.nx, ny = a.ny, nz = a.nz;
     const int tid = threadIdx.x;
-    const int qx = tid % ZM_QX, row = tid / ZM_QX;
-    const int x0 = blockIdx.x * ZM_TX, y0 = blockIdx.y * ZM_TY;
+    const int qx = tid % L::QX, row = tid / L::QX;
+    const int x0 = blockIdx.x * L::TX, y0 = blockIdx.y * L::TY;
     const int z0 = blockIdx.z * za.zc;
     const int ze = min(z0 + za.zc, nz);            // planes updated: [z0, ze)
     const int qmax = min(ze, nz - 1);              // last plane whose z is needed
     const int x = x0 + 4 * qx, y = y0 + row;
-    const bool upd = (row < ZM_TY) && (x < nx) && (y < ny);
+    const bool upd = (row < L::TY) && (x < nx) && (y < ny);
     const bool hasY = (y + 1 < ny);
     const float lam = a.lam, s = a.s, m = a.m;
 
     if (tid == 0) {
-        for (int k = 0; k <= ZM_STAGES; ++k) mbar_init(&bars[k], 1);
+        for (int k = 0; k <= L::STAGES; ++k) mbar_init(&bars[k], 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -212,32 +263,32 @@ __global__ void __launch_bounds__(ZM_THREADS, TVFGP_ZM_MINB) fgp_step_zmarch_tma
     __syncthreads();
 
     auto issue = [&](int q) {                       // thread 0 only
-        unsigned char *st = smem + ((q - z0) % ZM_STAGES) * ZM_STAGE_STRIDE;
-        uint64_t *bar = &bars[(q - z0) % ZM_STAGES];
+        unsigned char *st = smem + ((q - z0) % L::STAGES) * L::STAGE_STRIDE;
+        uint64_t *bar = &bars[(q - z0) % L::STAGES];
         const bool with_p = q < ze;                 // plane ze only feeds z(i+ez)
-        mbar_expect_tx(bar, with_p ? ZM_STAGE_TX : ZM_STAGE_TX_BR);
+        mbar_expect_tx(bar, with_p ? L::STAGE_TX : L::STAGE_TX_BR);
         if (with_p) {
-            tma_load_3d(st + ZM_OFF_P0, &za.tp0, x0, y0, q, bar);
-            tma_load_3d(st + ZM_OFF_P1, &za.tp1, x0, y0, q, bar);
-            tma_load_3d(st + ZM_OFF_P2, &za.tp2, x0, y0, q, bar);
+            tma_load_3d(st + L::OFF_P0, &za.tp0, x0, y0, q, bar);
+            tma_load_3d(st + L::OFF_P1, &za.tp1, x0, y0, q, bar);
+            tma_load_3d(st + L::OFF_P2, &za.tp2, x0, y0, q, bar);
         }
-        tma_load_3d(st + ZM_OFF_B, &za.tb, x0, y0, q, bar);
-        tma_load_3d(st + ZM_OFF_R0, &za.t0, x0 - 4, y0, q, bar);
-        tma_load_3d(st + ZM_OFF_R1, &za.t1, x0, y0 - 1, q, bar);
-        tma_load_3d(st + ZM_OFF_R2, &za.t2, x0, y0, q, bar);
+        tma_load_3d(st + L::OFF_B, &za.tb, x0, y0, q, bar);
+        tma_load_3d(st + L::OFF_R0, &za.t0, x0 - L::XO, y0, q, bar);
+        tma_load_3d(st + L::OFF_R1, &za.t1, x0, y0 - 1, q, bar);
+        tma_load_3d(st + L::OFF_R2, &za.t2, x0, y0, q, bar);
     };
     if (tid == 0) {
         if (z0 > 0) {
-            mbar_expect_tx(&bars[ZM_STAGES], ZM_BYTES_R2);
-            tma_load_3d(smem + ZM_OFF_PREV, &za.t2, x0, y0, z0 - 1, &bars[ZM_STAGES]);
+            mbar_expect_tx(&bars[L::STAGES], L::BYTES_R2);
+            tma_load_3d(smem + L::OFF_PREV, &za.t2, x0, y0, z0 - 1, &bars[L::STAGES]);
         }
-        for (int q = z0; q <= qmax && q < z0 + ZM_STAGES; ++q) issue(q);
+        for (int q = z0; q <= qmax && q < z0 + L::STAGES; ++q) issue(q);
     }
-    int next_issue = z0 + ZM_STAGES;               // next plane to load (thread 0)
+    int next_issue = z0 + L::STAGES;               // next plane to load (thread 0)
 
-    auto stage_of = [&](int q) { return smem + ((q - z0) % ZM_STAGES) * ZM_STAGE_STRIDE; };
-    auto parity_of = [&](int q) { return static_cast<uint32_t>(((q - z0) / ZM_STAGES) & 1); };
-    auto zrow = [&](int q, int rr) { return zpl + ((q % 3) * ZM_ROWS + rr) * ZM_ZP; };
+    auto stage_of = [&](int q) { return smem + ((q - z0) % L::STAGES) * L::STAGE_STRIDE; };
+    auto parity_of = [&](int q) { return static_cast<uint32_t>(((q - z0) / L::STAGES) & 1); };
+    auto zrow = [&](int q, int rr) { return zpl + ((q % 3) * L::ROWS + rr) * L::ZP; };
 
     // prologue: z of plane z0, own r at z0
     float4 Rc0, Rc1, Rc2, Zc;
@@ -247,26 +298,26 @@ __global__ void __launch_bounds__(ZM_THREADS, TVFGP_ZM_MINB) fgp_step_zmarch_tma
         float4 r2lo = f4zero();
         float r2lo_h = 0.0f;
         if (z0 > 0) {
-            ok = mbar_wait_tma(&bars[ZM_STAGES], 0);
-            const float *P2 = reinterpret_cast<const float *>(smem + ZM_OFF_PREV);
-            r2lo = lds4(P2 + row * ZM_BW + 4 * qx);
-            r2lo_h = P2[row * ZM_BW + ZM_TX];
+            ok = mbar_wait_tma(&bars[L::STAGES], 0);
+            const TS *P2 = reinterpret_cast<const TS *>(smem + L::OFF_PREV);
+            r2lo = lds4(P2 + row * L::RW + 4 * qx);
+            r2lo_h = lds1(P2 + row * L::RW + L::TX);
         }
         ok = ok && mbar_wait_tma(&bars[0], 0);
         if (ok) {
             const unsigned char *st = stage_of(z0);
-            zm_quad(st, row, qx, r2lo, lam, Rc0, Rc1, Rc2, Zc);
+            zm_quad<TS>(st, row, qx, r2lo, lam, Rc0, Rc1, Rc2, Zc);
             float *zr = zrow(z0, row);
             *reinterpret_cast<float4 *>(zr + 4 * qx) = Zc;
-            if (qx == ZM_QX - 1) zr[ZM_TX] = zm_halo(st, row, r2lo_h, lam, r2halo);
+            if (qx == L::QX - 1) zr[L::TX] = zm_halo<TS>(st, row, r2lo_h, lam, r2halo);
         } else {
             *abort_flag = 1;
         }
     }
     __syncthreads();
 
-    float *p0 = a.p, *p1 = a.p + a.N, *p2 = a.p + 2 * a.N;
-    float *o0 = a.rd, *o1 = a.rd + a.N, *o2 = a.rd + 2 * a.N;
+    TS *p0 = a.p, *p1 = a.p + a.N, *p2 = a.p + 2 * a.N;
+    TS *o0 = a.rd, *o1 = a.rd + a.N, *o2 = a.rd + 2 * a.N;
 
     int zlast = z0 - 1;                            // planes <= zlast+1 were waited for
     for (int z = z0; z < ze && *abort_flag == 0; ++z) {
@@ -278,12 +329,12 @@ __global__ void __launch_bounds__(ZM_THREADS, TVFGP_ZM_MINB) fgp_step_zmarch_tma
         float4 Rn0 = f4zero(), Rn1 = f4zero(), Rn2 = f4zero(), Zn = f4zero();
         float r2halo_n = 0.0f;
         if (hasZ) {
-            if (mbar_wait_tma(&bars[(z + 1 - z0) % ZM_STAGES], parity_of(z + 1))) {
+            if (mbar_wait_tma(&bars[(z + 1 - z0) % L::STAGES], parity_of(z + 1))) {
                 const unsigned char *st = stage_of(z + 1);
-                zm_quad(st, row, qx, Rc2, lam, Rn0, Rn1, Rn2, Zn);
+                zm_quad<TS>(st, row, qx, Rc2, lam, Rn0, Rn1, Rn2, Zn);
                 float *zr = zrow(z + 1, row);
                 *reinterpret_cast<float4 *>(zr + 4 * qx) = Zn;
-                if (qx == ZM_QX - 1) zr[ZM_TX] = zm_halo(st, row, r2halo, lam, r2halo_n);
+                if (qx == L::QX - 1) zr[L::TX] = zm_halo<TS>(st, row, r2halo, lam, r2halo_n);
             } else {
                 *abort_flag = 1;
             }
@@ -299,10 +350,10 @@ __global__ void __launch_bounds__(ZM_THREADS, TVFGP_ZM_MINB) fgp_step_zmarch_tma
         // (2) dual update of plane z, with its own p from the staged plane
         if (upd) {
             const unsigned char *stz = stage_of(z);
-            const int pofs = row * ZM_TX + 4 * qx;
-            float4 P0 = lds4(reinterpret_cast<const float *>(stz + ZM_OFF_P0) + pofs);
-            float4 P1 = lds4(reinterpret_cast<const float *>(stz + ZM_OFF_P1) + pofs);
-            float4 P2 = lds4(reinterpret_cast<const float *>(stz + ZM_OFF_P2) + pofs);
+            const int pofs = row * L::TX + 4 * qx;
+            float4 P0 = lds4(reinterpret_cast<const TS *>(stz + L::OFF_P0) + pofs);
+            float4 P1 = lds4(reinterpret_cast<const TS *>(stz + L::OFF_P1) + pofs);
+            float4 P2 = lds4(reinterpret_cast<const TS *>(stz + L::OFF_P2) + pofs);
             const float *zr = zrow(z, row);
             const float zx = zr[4 * qx + 4];
             const float4 ZY = hasY ? lds4(zrow(z, row + 1) + 4 * qx) : f4zero();
@@ -321,12 +372,12 @@ __global__ void __launch_bounds__(ZM_THREADS, TVFGP_ZM_MINB) fgp_step_zmarch_tma
             dual_update(N0.y, N1.y, N2.y, __fsub_rn(Zc.y, Zc.z), G1.y, G2.y, P0.y, P1.y, P2.y, s, m);
             dual_update(N0.z, N1.z, N2.z, __fsub_rn(Zc.z, Zc.w), G1.z, G2.z, P0.z, P1.z, P2.z, s, m);
             dual_update(N0.w, N1.w, N2.w, gx3, G1.w, G2.w, P0.w, P1.w, P2.w, s, m);
-            st4(p0 + i, P0);
-            st4(p1 + i, P1);
-            st4(p2 + i, P2);
-            st4(o0 + i, N0);
-            st4(o1 + i, N1);
-            st4(o2 + i, N2);
+            stv(p0 + i, P0);
+            stv(p1 + i, P1);
+            stv(p2 + i, P2);
+            stv(o0 + i, N0);
+            stv(o1 + i, N1);
+            stv(o2 + i, N2);
         }
         Rc0 = Rn0;
         Rc1 = Rn1;
@@ -342,9 +393,9 @@ __global__ void __launch_bounds__(ZM_THREADS, TVFGP_ZM_MINB) fgp_step_zmarch_tma
         __syncthreads();
         if (tid == 0) {
             atomicExch(za.err, kErrTimeout);
-            if (z0 > 0 && zlast < z0) mbar_wait_tma(&bars[ZM_STAGES], 0);
+            if (z0 > 0 && zlast < z0) mbar_wait_tma(&bars[L::STAGES], 0);
             for (int q = zlast + 1; q < next_issue && q <= qmax; ++q)
-                mbar_wait_tma(&bars[(q - z0) % ZM_STAGES], parity_of(q));
+                mbar_wait_tma(&bars[(q - z0) % L::STAGES], parity_of(q));
         }
         __syncthreads();
     }
@@ -368,7 +419,10 @@ inline PFN_cuTensorMapEncodeTiled_v12000 zm_encoder()
     return fn;
 }
 
-inline bool zmarch_supported(int nx, int, int) { return nx % 4 == 0; }
+// The fp32 march needs rows of whole 16-byte units (nx % 4 == 0), the
+// binary16 one nx % 8 == 0; both need 16-byte aligned base addresses.
+template <typename TS = float>
+inline bool zmarch_supported(int nx, int, int) { return nx % ZmLayout<TS>::XO == 0; }
 
 // The variant needs the driver's tensor-map encoder.
 inline bool zmarch_available() { return zm_encoder() != nullptr; }
@@ -386,22 +440,33 @@ inline int zmarch_pick_zc(int tiles_xy, int nz, int slots)
     return 8;
 }
 
+template <typename TS = float>
+inline const void *zmarch_kernel() { return reinterpret_cast<const void *>(&fgp_step_zmarch_tma<TS>); }
+template <typename TS = float>
+inline int zmarch_threads() { return ZmLayout<TS>::THREADS; }
+inline dim3 zmarch_grid(const ZmarchPlan &p) { return p.grid; }
+template <typename TS = float>
+inline size_t zmarch_smem_bytes() { return ZmLayout<TS>::SMEM; }
+
+template <typename TS = float>
 inline int zmarch_plan(int nx, int ny, int nz, ZmarchPlan *plan)
 {
-    const int tx = (nx + ZM_TX - 1) / ZM_TX, ty = (ny + ZM_TY - 1) / ZM_TY;
+    using L = ZmLayout<TS>;
+    const int tx = (nx + L::TX - 1) / L::TX, ty = (ny + L::TY - 1) / L::TY;
     plan->zc = 32;
     plan->grid = dim3(tx, ty, (nz + plan->zc - 1) / plan->zc);
-    if (!zmarch_supported(nx, ny, nz)) return 0;
+    if (!zmarch_supported<TS>(nx, ny, nz)) return 0;
     if (zm_encoder() == nullptr) return 3;
-    const void *fn = reinterpret_cast<const void *>(&fgp_step_zmarch_tma);
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ZM_SMEM) != cudaSuccess) {
+    const void *fn = zmarch_kernel<TS>();
+    const int smem = ZmLayout<TS>::SMEM;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
         cudaGetLastError();
         return 3;
     }
     int dev = 0, sms = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, ZM_THREADS, ZM_SMEM) != cudaSuccess) {
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, L::THREADS, smem) != cudaSuccess) {
         cudaGetLastError();
         return 3;
     }
@@ -410,37 +475,38 @@ inline int zmarch_plan(int nx, int ny, int nz, ZmarchPlan *plan)
     return 0;
 }
 
-inline const void *zmarch_kernel() { return reinterpret_cast<const void *>(&fgp_step_zmarch_tma); }
-inline int zmarch_threads() { return ZM_THREADS; }
-inline dim3 zmarch_grid(const ZmarchPlan &p) { return p.grid; }
-inline size_t zmarch_smem_bytes() { return ZM_SMEM; }
-
-inline bool zm_encode(CUtensorMap *map, const float *base, int nx, int ny, int nz, int bw, int bh)
+template <typename T>
+inline bool zm_encode(CUtensorMap *map, const T *base, int nx, int ny, int nz, int bw, int bh)
 {
+    constexpr cuuint64_t es = sizeof(T);
+    const CUtensorMapDataType dt = es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const cuuint64_t dims[3] = {(cuuint64_t)nx, (cuuint64_t)ny, (cuuint64_t)nz};
-    const cuuint64_t strides[2] = {(cuuint64_t)nx * 4, (cuuint64_t)nx * ny * 4};
+    const cuuint64_t strides[2] = {(cuuint64_t)nx * es, (cuuint64_t)nx * ny * es};
     const cuuint32_t box[3] = {(cuuint32_t)bw, (cuuint32_t)bh, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
-    return zm_encoder()(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides,
-                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                        TVFGP_ZM_L2PROMO, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return zm_encoder()(map, dt, 3, const_cast<T *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, TVFGP_ZM_L2PROMO,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Fill the kernel arguments of one step: tensor maps of b and of the three
-// components of r_src.  Returns false if an encoding fails.
-inline bool zmarch_fill(const ZmarchPlan &plan, const StepArgs &a, int *err, ZmarchArgs &za)
+// Fill the kernel arguments of one step: tensor maps of b, of the three
+// components of p and of the three components of r_src.  Returns false if
+// an encoding fails.
+template <typename TS>
+inline bool zmarch_fill(const ZmarchPlan &plan, const StepArgsT<TS> &a, int *err, ZmarchArgsT<TS> &za)
 {
+    using L = ZmLayout<TS>;
     za.a = a;
     za.err = err;
     za.zc = plan.zc;
-    const float *r = a.rs;
-    return zm_encode(&za.tp0, a.p, a.nx, a.ny, a.nz, ZM_TX, ZM_TY) &&
-           zm_encode(&za.tp1, a.p + a.N, a.nx, a.ny, a.nz, ZM_TX, ZM_TY) &&
-           zm_encode(&za.tp2, a.p + 2 * a.N, a.nx, a.ny, a.nz, ZM_TX, ZM_TY) &&
-           zm_encode(&za.tb, a.b, a.nx, a.ny, a.nz, ZM_BW, ZM_HB) &&
-           zm_encode(&za.t0, r, a.nx, a.ny, a.nz, ZM_W0, ZM_HB) &&
-           zm_encode(&za.t1, r + a.N, a.nx, a.ny, a.nz, ZM_BW, ZM_H1) &&
-           zm_encode(&za.t2, r + 2 * a.N, a.nx, a.ny, a.nz, ZM_BW, ZM_HB);
+    const TS *r = a.rs;
+    return zm_encode(&za.tp0, a.p, a.nx, a.ny, a.nz, L::TX, L::TY) &&
+           zm_encode(&za.tp1, a.p + a.N, a.nx, a.ny, a.nz, L::TX, L::TY) &&
+           zm_encode(&za.tp2, a.p + 2 * a.N, a.nx, a.ny, a.nz, L::TX, L::TY) &&
+           zm_encode(&za.tb, a.b, a.nx, a.ny, a.nz, L::BW, L::HB) &&
+           zm_encode(&za.t0, r, a.nx, a.ny, a.nz, L::W0, L::HB) &&
+           zm_encode(&za.t1, r + a.N, a.nx, a.ny, a.nz, L::RW, L::H1) &&
+           zm_encode(&za.t2, r + 2 * a.N, a.nx, a.ny, a.nz, L::RW, L::HB);
 }
 
 }  // namespace tvfgp

@@ -152,10 +152,14 @@ int tvfgp_primal(tvfgp_t h, const float *b, const float *dual, float lambda, flo
  * order, and rounds each stored result once to binary16 (nearest, ties to
  * even).  It moves 28 bytes per voxel and step instead of 52 and changes the
  * result: the page ("Profiler counters") counts a half-precision dual among
- * the ways to move fewer bytes.  The vector kernel runs when nx % 4 == 0, b
- * is 16-byte and p, r 8-byte aligned, the scalar kernel otherwise.  p and r
- * must be 2-byte aligned (TVFGP_ERR_ALIGN).  The handle's scratch buffer
- * holds the other r, so the call does not allocate. */
+ * the ways to move fewer bytes.  Kernel choice: on a handle set to
+ * TVFGP_VARIANT_SCALAR the scalar kernel; on FUSED the fused vector kernel
+ * when nx % 4 == 0, b is 16-byte and p, r 8-byte aligned (else scalar); on
+ * every other variant the TMA z-march when nx % 8 == 0 and b, p, r are
+ * 16-byte aligned, else as FUSED.  All three give the same bits;
+ * tvfgp_last_variant reports ZMARCH_TMA, FUSED or SCALAR.  p and r must be
+ * 2-byte aligned (TVFGP_ERR_ALIGN).  The handle's scratch buffer holds the
+ * other r, so the call does not allocate. */
 int tvfgp_run_f16(tvfgp_t h, const float *b, unsigned short *p, unsigned short *r, float lambda,
                   int nsteps, double t0, tvfgp_stream_t stream, double *t_final);
 

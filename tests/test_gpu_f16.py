@@ -51,7 +51,22 @@ def test_workloads_exact(T, key, graph):
     assert np.array_equal(z.cpu().numpy(), oracle.primal_h16(b, ph, w.lam))
 
 
-@pytest.mark.parametrize("shape", [(1, 1, 1), (5, 3, 7), (33, 17, 9), (36, 40, 3), (132, 9, 11)])
+F16_SHAPES = [(1, 1, 1), (5, 3, 7), (33, 17, 9), (36, 40, 3), (132, 9, 11),
+              (8, 1, 1), (8, 3, 2), (40, 17, 9), (72, 31, 37), (264, 5, 19), (16, 64, 64)]
+
+
+def expected_variant(T, nx, variant):
+    """The kernel run_f16 picks: the z-march when rows are whole 16-byte
+    units (nx % 8 == 0), else the fused kernel when nx % 4 == 0, else the
+    scalar one; FUSED and SCALAR handles keep to their own kernel."""
+    if variant == "scalar":
+        return T.TVFGP_VARIANT_SCALAR
+    if nx % 8 == 0 and variant != "fused":
+        return T.TVFGP_VARIANT_ZMARCH_TMA
+    return T.TVFGP_VARIANT_FUSED if nx % 4 == 0 else T.TVFGP_VARIANT_SCALAR
+
+
+@pytest.mark.parametrize("shape", F16_SHAPES)
 def test_odd_shapes_exact(T, shape):
     nx, ny, nz = shape
     b = synth.random_case(shape, 31)
@@ -61,13 +76,77 @@ def test_odd_shapes_exact(T, shape):
         p, r = dev16(p0), dev16(r0)
         with T.Tvfgp(nx, ny, nz) as h:
             h.run_f16(dev(b), p, r, 0.07, nsteps, 1.0)
-            assert h.last_variant == (T.TVFGP_VARIANT_SCALAR if nx % 4 else T.TVFGP_VARIANT_FUSED) \
-                or nsteps == 0
-            h.check()
+            assert h.last_variant == expected_variant(T, nx, "auto") or nsteps == 0
+            assert h.check() == 0
         ph, rh = p0.copy(), r0.copy()
         oracle.fgp_run_h16(b, ph, rh, 0.07, nsteps, 1.0)
         assert np.array_equal(bits(p), ph), (shape, nsteps)
         assert np.array_equal(bits(r), rh), (shape, nsteps)
+
+
+@pytest.mark.parametrize("variant", ["auto", "fused", "scalar"])
+def test_f16_kernels_agree_bitwise(T, variant):
+    """The three binary16 kernels on a volume where all three can run (64 x
+    45 x 40: several tiles in x and y, ragged in y, several march segments
+    in z) give the oracle's bits, eager and through a graph."""
+    shape = (64, 45, 40)
+    b = synth.random_case(shape, 41)
+    p0 = oracle.float_to_half(synth.random_dual(shape, 42, scale=0.5))
+    r0 = oracle.float_to_half(synth.random_dual(shape, 43, scale=0.7))
+    ph, rh = p0.copy(), r0.copy()
+    oracle.fgp_run_h16(b, ph, rh, 0.05, 5, 1.0)
+    for graph in (False, True):
+        p, r = dev16(p0), dev16(r0)
+        with T.Tvfgp(*shape, variant, graph) as h:
+            h.run_f16(dev(b), p, r, 0.05, 5, 1.0)
+            assert h.last_variant == expected_variant(T, shape[0], variant)
+            assert h.check() == 0
+        assert np.array_equal(bits(p), ph) and np.array_equal(bits(r), rh), (variant, graph)
+
+
+def test_f16_march_misaligned_falls_back(T):
+    """A dual whose base is 8- but not 16-byte aligned cannot feed the
+    tensor maps: the fused kernel runs, with the same bits."""
+    import torch
+    shape = (32, 8, 8)
+    n = 32 * 8 * 8
+    b = synth.random_case(shape, 51)
+    p0 = oracle.float_to_half(synth.random_dual(shape, 52, scale=0.5))
+    r0 = oracle.float_to_half(synth.random_dual(shape, 53, scale=0.7))
+    ph, rh = p0.copy(), r0.copy()
+    oracle.fgp_run_h16(b, ph, rh, 0.05, 3, 1.0)
+    pbuf = torch.zeros(3 * n + 4, dtype=torch.float16, device="cuda")
+    rbuf = torch.zeros(3 * n + 4, dtype=torch.float16, device="cuda")
+    p, r = pbuf[4:], rbuf[4:]                       # 8 bytes past a 256-byte boundary
+    p.copy_(dev16(p0).reshape(-1))
+    r.copy_(dev16(r0).reshape(-1))
+    with T.Tvfgp(*shape) as h:
+        h.run_f16(dev(b), p, r, 0.05, 3, 1.0)
+        assert h.last_variant == T.TVFGP_VARIANT_FUSED
+        assert h.check() == 0
+    assert np.array_equal(bits(p).reshape(ph.shape), ph) and np.array_equal(bits(r).reshape(rh.shape), rh)
+
+
+@pytest.mark.slow
+def test_f16_512_cubed_exact(T):
+    """The 512^3 workload with a binary16 dual, in the configuration the
+    bench times for it (graph replay of the z-march, a fresh b and t0 per
+    outer), against the oracle; the first 3 of its 20 outers, to bound the
+    oracle's time."""
+    w = synth.WORKLOADS["c4"]
+    base = synth.phantom(w)
+    shape = (3, w.nz, w.ny, w.nx)
+    ph = np.zeros(shape, np.uint16)
+    rh = np.zeros(shape, np.uint16)
+    p, r = dev16(ph), dev16(rh)
+    with T.Tvfgp(w.nx, w.ny, w.nz, "auto", True) as h:
+        for k in range(3):
+            b = synth.make_b(w, k, base)
+            h.run_f16(dev(b), p, r, w.lam, w.steps, w.t0)
+            oracle.fgp_run_h16(b, ph, rh, w.lam, w.steps, w.t0)
+        assert h.last_variant == T.TVFGP_VARIANT_ZMARCH_TMA
+        assert h.check() == 0
+    assert np.array_equal(bits(p), ph) and np.array_equal(bits(r), rh)
 
 
 def test_accuracy_against_fp32(T):
