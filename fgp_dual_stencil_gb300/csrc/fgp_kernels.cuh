@@ -16,7 +16,9 @@
 //   |q| = sqrt((q0*q0 + q1*q1) + q2*q2);  p'_a = q_a / max(1, |q|)
 //   r_a = p'_a + m*(p'_a - p_a)
 // Dividing by max(1,|q|) equals q itself when |q| <= 1, so the square root
-// and the division are only issued when |q|^2 > 1 (IEEE x/1 == x).
+// and the division are only issued when |q|^2 > 1 (IEEE x/1 == x); they are
+// then evaluated by a shorter sequence with the same correctly rounded
+// results (project_unit_ball below).
 #pragma once
 
 #include <cuda_fp16.h>
@@ -69,6 +71,104 @@ __device__ __forceinline__ float zval(float b, float lam, float d0, float d1, fl
     return fmaxf(__fsub_rn(b, __fmul_rn(lam, L)), 0.0f);
 }
 
+// ---------------------------------------------------------------------------
+// projection onto the unit ball, p' = q / max(1, |q|)
+// ---------------------------------------------------------------------------
+//
+// Where |q|^2 = nn > 1 the canonical result is n = RN(sqrt(nn)) followed by
+// RN(q_a / n) for each component (IEEE square root and division).  The fast
+// path reaches the same bits with one hardware estimate and fused
+// multiply-adds:
+//   k = rsqrt.approx(nn)                          estimate of 1/sqrt(nn)
+//   g = RN(nn k), e = RN(nn - g^2), n = RN(g + e k/2)
+//                                                 Newton correction of sqrt
+//   v = rcp.approx(n), t = RN(1 - n v), y = RN(v + t v)
+//                                                 Newton correction of 1/n
+//   c = RN(q y), w = RN(c n - q), d = RN(c - w y) corrected quotient
+// The last line is Markstein's FMA division (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990; the FMA-based division of Muller et al., "Handbook of
+// Floating-Point Arithmetic"): when y = RN(1/n) and c is within one ulp of
+// q/n, w is exact and d = RN(q/n), as long as nothing under- or overflows.
+// That n = RN(sqrt(nn)) and y = RN(1/n) for every float nn in (1, 2^100) is
+// not a theorem about the estimates but a measured fact (a reciprocal
+// corrected from k instead of from its own estimate misses 200 of them):
+// tvfgp_debug_projection_check compares all of them with __fsqrt_rn and
+// __frcp_rn, and compares whole projections with the IEEE ones on random
+// and near-binade-edge inputs.  Range guard: the fast path runs only for
+// nn < 2^100 and components that are zero or at least 2^-75 in magnitude,
+// which keeps every intermediate a normal number; other inputs take the IEEE
+// operations.  Forming w = c n - q (not q - c n) and d = c - w y returns a
+// zero component with its sign, as the IEEE division does.
+
+__device__ __forceinline__ float rsqrt_estimate(float x)
+{
+    float y;
+    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcp_estimate(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// n = RN(sqrt(nn)) and y = RN(1/n), for nn in (1, 2^100).
+__device__ __forceinline__ void sqrt_recip_rn(float nn, float &n, float &y)
+{
+    const float k = rsqrt_estimate(nn);
+    const float g = __fmul_rn(nn, k);
+    const float e = __fmaf_rn(-g, g, nn);
+    n = __fmaf_rn(e, __fmul_rn(0.5f, k), g);
+    const float v = rcp_estimate(n);
+    const float t = __fmaf_rn(-n, v, 1.0f);
+    y = __fmaf_rn(t, v, v);
+}
+
+// RN(q / n) given y = RN(1/n), in the range the guard admits.
+__device__ __forceinline__ float div_by_recip_rn(float q, float n, float y)
+{
+    const float c = __fmul_rn(q, y);
+    const float w = __fmaf_rn(c, n, -q);
+    return __fmaf_rn(-w, y, c);
+}
+
+// A component outside the fast path's range: non-zero and below 2^-75 in
+// magnitude.  (2|q| as bits) - 2 wraps to the top for q = +-0.
+__device__ __forceinline__ bool tiny_nonzero(float q)
+{
+    constexpr uint32_t kLim = 0x1a000000u * 2u - 2u;    // 2^-75 has the bits 0x1a000000
+    return (__float_as_uint(q) << 1) - 2u < kLim;
+}
+
+// The canonical IEEE projection (also the reference of the self-check).
+__device__ __forceinline__ void project_unit_ball_ieee(float &q0, float &q1, float &q2, float nn)
+{
+    if (nn > 1.0f) {
+        const float n = __fsqrt_rn(nn);
+        q0 = __fdiv_rn(q0, n);
+        q1 = __fdiv_rn(q1, n);
+        q2 = __fdiv_rn(q2, n);
+    }
+}
+
+__device__ __forceinline__ void project_unit_ball(float &q0, float &q1, float &q2, float nn)
+{
+    if (nn > 1.0f) {
+        if (nn < 0x1p100f && !(tiny_nonzero(q0) | tiny_nonzero(q1) | tiny_nonzero(q2))) {
+            float n, y;
+            sqrt_recip_rn(nn, n, y);
+            q0 = div_by_recip_rn(q0, n, y);
+            q1 = div_by_recip_rn(q1, n, y);
+            q2 = div_by_recip_rn(q2, n, y);
+        } else {
+            project_unit_ball_ieee(q0, q1, q2, nn);
+        }
+    }
+}
+
 // q = r + g*s, projection onto the unit ball, extrapolation.  Writes p' into
 // (p0,p1,p2) and the new r into (r0,r1,r2).
 __device__ __forceinline__ void dual_update(float &r0, float &r1, float &r2,
@@ -83,12 +183,7 @@ __device__ __forceinline__ void dual_update(float &r0, float &r1, float &r2,
     // max(1, |q|) > 1 exactly when |q|^2 > 1 (a correctly rounded square root
     // is monotone and sqrt(1) = 1); where |q|^2 > 1 but |q| rounds to 1, the
     // division by 1 leaves q unchanged, as the definition does.
-    if (nn > 1.0f) {
-        const float n = __fsqrt_rn(nn);
-        q0 = __fdiv_rn(q0, n);
-        q1 = __fdiv_rn(q1, n);
-        q2 = __fdiv_rn(q2, n);
-    }
+    project_unit_ball(q0, q1, q2, nn);
     r0 = __fadd_rn(q0, __fmul_rn(m, __fsub_rn(q0, p0)));
     r1 = __fadd_rn(q1, __fmul_rn(m, __fsub_rn(q1, p1)));
     r2 = __fadd_rn(q2, __fmul_rn(m, __fsub_rn(q2, p2)));

@@ -10,6 +10,7 @@
 #include "fgp_kernels.cuh"
 #include "zmarch_tma.cuh"
 #include "zmarch2_tma.cuh"
+#include "selfcheck.cuh"
 
 #include <cuda_runtime.h>
 
@@ -936,6 +937,22 @@ int tvfgp_host_free(void *p)
         return from_cuda(e);
     }
     return TVFGP_OK;
+}
+
+int tvfgp_debug_projection_check(int mode, unsigned long long count, unsigned long long seed,
+                                 unsigned long long *out, tvfgp_stream_t stream)
+{
+    if (mode < 0 || mode > 2 || out == nullptr || (reinterpret_cast<uintptr_t>(out) & 7u)) return TVFGP_ERR_ARG;
+    if (mode == 0) count = kNnEnd - kNnFirst;
+    else if (count > (1ull << 40)) return TVFGP_ERR_ARG;
+    if (count == 0) return TVFGP_OK;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return from_cuda(e);
+    projection_check<<<sms * 8, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(mode, count, seed, out);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? TVFGP_OK : from_cuda(e);
 }
 
 int tvfgp_debug_timeout_probe(tvfgp_t h, int spins, tvfgp_stream_t stream)

@@ -65,6 +65,7 @@ def _load():
         "tvfgp_last_variant": ([vp], i),
         "tvfgp_launch_count": ([vp], ll),
         "tvfgp_debug_timeout_probe": ([vp, i, vp], i),
+        "tvfgp_debug_projection_check": ([i, ctypes.c_ulonglong, ctypes.c_ulonglong, vp, vp], i),
         "tvfgp_run_noalloc": ([i, i, i, vp, vp, vp, f, i, d, vp, ctypes.POINTER(d)], i),
         "tvfgp_host_alloc": ([ctypes.c_size_t, i, ctypes.POINTER(vp)], i),
         "tvfgp_run_f16": ([vp, vp, vp, vp, f, i, d, vp, ctypes.POINTER(d)], i),
@@ -224,6 +225,16 @@ def tvfgp_last_variant(h: int) -> int:
 
 def tvfgp_launch_count(h: int) -> int:
     return int(_lib.tvfgp_launch_count(h))
+
+
+def tvfgp_debug_projection_check(mode: int, count: int, seed: int, out, stream=None) -> None:
+    """Enqueue the projection self-check (see the header); out is an int64
+    CUDA tensor of 2 elements set to (0, -1) by the caller."""
+    import torch
+    if not isinstance(out, torch.Tensor) or not out.is_cuda or out.dtype != torch.int64 or out.numel() != 2:
+        raise ValueError("out must be a CUDA int64 tensor of 2 elements")
+    _ok(_lib.tvfgp_debug_projection_check(int(mode), int(count), int(seed) & (2**64 - 1), out.data_ptr(),
+                                          _stream(stream)), "tvfgp_debug_projection_check")
 
 
 def tvfgp_debug_timeout_probe(h: int, spins: int, stream=None) -> None:

@@ -205,6 +205,25 @@ int tvfgp_host_free(void *p);
  * reports TVFGP_ERR_TIMEOUT.  1 <= spins <= 2^24. */
 int tvfgp_debug_timeout_probe(tvfgp_t h, int spins, tvfgp_stream_t stream);
 
+/* Self-check of the step kernels' projection onto the unit ball, which
+ * evaluates q / max(1, |q|) with a hardware square-root estimate and fused
+ * multiply-add corrections instead of IEEE square root and division, and
+ * must give the same bits (the page's step is defined by the exact
+ * operations; this check has no counterpart there).  Enqueues one kernel on
+ * `stream`:
+ *   mode 0: all floats nn in (1, 2^100): its square root and reciprocal
+ *           against __fsqrt_rn and __frcp_rn (count is ignored);
+ *   mode 1: `count` pseudo-random triples q (from `seed`): the whole
+ *           projection against the IEEE one;
+ *   mode 2: `count` quotients, half of them within a few ulps of a power of
+ *           two, against __fdiv_rn.
+ * out is a device array of two unsigned long long that the caller sets to
+ * {0, ULLONG_MAX}: out[0] receives the number of mismatches, out[1] the
+ * smallest mismatching sample index.  count <= 2^40; TVFGP_ERR_ARG on a bad
+ * mode, count or out (NULL or not 8-byte aligned). */
+int tvfgp_debug_projection_check(int mode, unsigned long long count, unsigned long long seed,
+                                 unsigned long long *out, tvfgp_stream_t stream);
+
 /* Capacity, in voxels, of tvfgp_run_noalloc's built-in scratch buffer
  * (2^21 voxels, e.g. 128^3: 3 * 2^21 floats = 24 MiB of device memory). */
 #define TVFGP_NOALLOC_MAX_VOXELS 2097152
