@@ -95,12 +95,19 @@ constexpr int Z2_TASKS_A = Z2_QA * (Z2_TY + 3);
 constexpr int Z2_TASKS_B = Z2_QA * (Z2_TY + 2);
 constexpr int Z2_TASKS_C = Z2_QC * (Z2_TY + 1);
 constexpr int Z2_TASKS_D = Z2_QD * Z2_TY;
-// One thread per z^k quad; the threads of the tile's quads also run z^{k+1}
-// and step k+1 on them, and the quads of z^{k+1}'s x+1 column and y+1 row go
-// to the threads past the step-k region.
+// One thread per z^k quad.  Threads are numbered so that the phases after
+// the first barrier run on as few warps as possible: threads
+// [0, TASKS_D) own the tile's quads (row-major, QD per row) and run all four
+// phases on them; threads [TASKS_D, TASKS_B) own the ring of the grown tile
+// (its first and last rows, then its left and right quad columns) and run z^k
+// and step k; threads [TASKS_B, TASKS_A) own z^k's extra last row.  The quads
+// of z^{k+1}'s x+1 column and y+1 row go to the threads from TASKS_D on, which
+// are free after the barrier.
 constexpr int Z2_THREADS = (Z2_TASKS_A + 31) / 32 * 32;
+constexpr int Z2_RING_B = Z2_TASKS_B - Z2_TASKS_D;        // 2 QA + 2 TY
 constexpr int Z2_HALO_C = (Z2_TY + 1) + Z2_QD;            // z^{k+1} quads outside the tile
-constexpr int Z2_HALO_T = Z2_THREADS - Z2_TASKS_B;        // threads that take them
+constexpr int Z2_HALO_T = Z2_THREADS - Z2_TASKS_D;        // threads that take them
+static_assert(Z2_RING_B == 2 * Z2_QA + 2 * Z2_TY && Z2_TASKS_A - Z2_TASKS_B == Z2_QA, "thread roles");
 static_assert(Z2_TASKS_B <= Z2_THREADS && Z2_HALO_T > 0, "thread roles");
 
 // shared rings, two slots each (a plane is written two iterations after the
@@ -187,10 +194,25 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     auto z1p = [&](int q) { return Z1 + (q & 1) * Z2_RING_Z1; };
 
     // this thread's quad in the z^k / step-k grid (c = lx + 4, row = ly + 1)
-    const int my_c = 4 * (tid % Z2_QA), my_row = tid / Z2_QA;
+    int my_c = 0, my_row = 0;
+    if (tid < Z2_TASKS_D) {                                      // tile
+        my_c = 4 + 4 * (tid % Z2_QD);
+        my_row = 1 + tid / Z2_QD;
+    } else if (tid < Z2_TASKS_D + 2 * Z2_QA) {                   // ring: rows ly = -1 and TY
+        const int j = tid - Z2_TASKS_D;
+        my_c = 4 * (j % Z2_QA);
+        my_row = j < Z2_QA ? 0 : Z2_TY + 1;
+    } else if (tid < Z2_TASKS_B) {                               // ring: quad columns 0 and QA-1
+        const int j = tid - Z2_TASKS_D - 2 * Z2_QA;
+        my_c = (j & 1) ? 4 * (Z2_QA - 1) : 0;
+        my_row = 1 + j / 2;
+    } else if (tid < Z2_TASKS_A) {                               // z^k only: row ly = TY+1
+        my_c = 4 * (tid - Z2_TASKS_B);
+        my_row = Z2_TY + 2;
+    }
     const bool doA = tid < Z2_TASKS_A;
     const bool doB = tid < Z2_TASKS_B;
-    const bool my_tile = doB && my_c >= 4 && my_c < Z2_TX + 4 && my_row >= 1 && my_row <= Z2_TY;
+    const bool my_tile = tid < Z2_TASKS_D;
 
     // z^k of plane q for this thread's quad, from the staged plane st and the
     // r2 of the plane below (lo: a staged r2 box, or nullptr at plane 0);
@@ -310,7 +332,7 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
         float4 Z1n = f4zero();
         if (q >= z0 && q <= uk_last) {
             if (my_tile) Z1n = z1_quad(q, my_c - 4, my_row - 1);
-            for (int h = tid - Z2_TASKS_B; h >= 0 && h < Z2_HALO_C; h += Z2_HALO_T) {
+            for (int h = tid - Z2_TASKS_D; h >= 0 && h < Z2_HALO_C; h += Z2_HALO_T) {
                 if (h <= Z2_TY)
                     z1_quad(q, Z2_TX, h);                            // x+1 column, rows 0..TY
                 else
