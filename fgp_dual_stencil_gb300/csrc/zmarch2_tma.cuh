@@ -300,21 +300,26 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
                    P2 = lds4(F(st, Z2_OFF_P2) + po);
             const bool yin = y >= 0 && y < ny;
             const bool gy = y < ny - 1;
-            float *r0 = &R0.x, *r1 = &R1.x, *r2 = &R2.x, *p0 = &P0.x, *p1 = &P1.x, *p2 = &P2.x;
             const float zcv[5] = {zc.x, zc.y, zc.z, zc.w, zx};
             const float zyv[4] = {zy.x, zy.y, zy.z, zy.w};
             const float zzv[4] = {zz.x, zz.y, zz.z, zz.w};
+            float4 G0, G1, G2;
+            float *g0 = &G0.x, *g1 = &G1.x, *g2 = &G2.x;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int xe = x + e;
-                if (yin && xe >= 0 && xe < nx) {
-                    const float g0 = (xe < nx - 1) ? __fsub_rn(zcv[e], zcv[e + 1]) : 0.0f;
-                    const float g1 = gy ? __fsub_rn(zcv[e], zyv[e]) : 0.0f;
-                    const float g2 = hasZ ? __fsub_rn(zcv[e], zzv[e]) : 0.0f;
-                    dual_update(r0[e], r1[e], r2[e], g0, g1, g2, p0[e], p1[e], p2[e], s, m0);
-                } else {
-                    r0[e] = r1[e] = r2[e] = 0.0f;            // the r(-1) = 0 boundary of step k+1
-                }
+                g0[e] = (xe < nx - 1) ? __fsub_rn(zcv[e], zcv[e + 1]) : 0.0f;
+                g1[e] = gy ? __fsub_rn(zcv[e], zyv[e]) : 0.0f;
+                g2[e] = hasZ ? __fsub_rn(zcv[e], zzv[e]) : 0.0f;
+            }
+            dual_update4(R0, R1, R2, G0, G1, G2, P0, P1, P2, s, m0);
+            // voxels of the ring outside the volume: r^{k+1} = 0, the r(-1) = 0
+            // boundary of step k+1 (their p is never used)
+            float *r0 = &R0.x, *r1 = &R1.x, *r2 = &R2.x;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int xe = x + e;
+                if (!(yin && xe >= 0 && xe < nx)) r0[e] = r1[e] = r2[e] = 0.0f;
             }
             const int mo = row * Z2_PK + c;
             *reinterpret_cast<float4 *>(mrp(q, 0) + mo) = R0;
@@ -366,10 +371,8 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
                     G2.z = __fsub_rn(zc.z, zz.z); G2.w = __fsub_rn(zc.w, zz.w);
                 }
                 const float gx3 = (x + 3 < nx - 1) ? __fsub_rn(zc.w, zx) : 0.0f;
-                dual_update(R0.x, R1.x, R2.x, __fsub_rn(zc.x, zc.y), G1.x, G2.x, P0.x, P1.x, P2.x, s, m1);
-                dual_update(R0.y, R1.y, R2.y, __fsub_rn(zc.y, zc.z), G1.y, G2.y, P0.y, P1.y, P2.y, s, m1);
-                dual_update(R0.z, R1.z, R2.z, __fsub_rn(zc.z, zc.w), G1.z, G2.z, P0.z, P1.z, P2.z, s, m1);
-                dual_update(R0.w, R1.w, R2.w, gx3, G1.w, G2.w, P0.w, P1.w, P2.w, s, m1);
+                const float4 G0 = make_float4(__fsub_rn(zc.x, zc.y), __fsub_rn(zc.y, zc.z), __fsub_rn(zc.z, zc.w), gx3);
+                dual_update4(R0, R1, R2, G0, G1, G2, P0, P1, P2, s, m1);
                 const long long i = x + (long long)nx * (y + (long long)ny * qd);
                 st4(p0d + i, P0);
                 st4(p1d + i, P1);
