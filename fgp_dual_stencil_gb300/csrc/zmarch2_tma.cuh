@@ -57,6 +57,12 @@ namespace tvfgp {
 #ifndef TVFGP_Z2_MINB
 #define TVFGP_Z2_MINB 3
 #endif
+#ifndef TVFGP_Z2_ZC_MAX
+#define TVFGP_Z2_ZC_MAX 64        // most output planes per CTA
+#endif
+#ifndef TVFGP_Z2_WAVES
+#define TVFGP_Z2_WAVES 2          // fewest waves of CTAs over the resident slots
+#endif
 
 constexpr int Z2_TX = TVFGP_Z2_TX;          // output tile width
 constexpr int Z2_TY = TVFGP_Z2_TY;          // output tile height
@@ -434,7 +440,7 @@ inline int zmarch2_plan(int nx, int ny, int nz, Zmarch2Plan *plan)
         cudaGetLastError();
         return 3;
     }
-    plan->zc = zmarch_pick_zc(tx * ty, nz, sms * (per_sm > 0 ? per_sm : 1));
+    plan->zc = zmarch_pick_zc(tx * ty, nz, sms * (per_sm > 0 ? per_sm : 1), TVFGP_Z2_ZC_MAX, TVFGP_Z2_WAVES);
     plan->grid = dim3(tx, ty, (nz + plan->zc - 1) / plan->zc);
     return 0;
 }

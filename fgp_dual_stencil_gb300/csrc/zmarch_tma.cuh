@@ -66,6 +66,12 @@ namespace tvfgp {
 #ifndef TVFGP_ZM_MINB_H
 #define TVFGP_ZM_MINB_H 4
 #endif
+#ifndef TVFGP_ZM_ZC_MAX
+#define TVFGP_ZM_ZC_MAX 32        // most planes per CTA
+#endif
+#ifndef TVFGP_ZM_WAVES
+#define TVFGP_ZM_WAVES 4          // fewest waves of CTAs over the resident slots
+#endif
 #ifndef TVFGP_ZM_L2PROMO
 #define TVFGP_ZM_L2PROMO CU_TENSOR_MAP_L2_PROMOTION_L2_256B
 #endif
@@ -425,15 +431,16 @@ inline bool zmarch_supported(int nx, int, int) { return nx % ZmLayout<TS>::XO ==
 // The variant needs the driver's tensor-map encoder.
 inline bool zmarch_available() { return zm_encoder() != nullptr; }
 
-// Planes per CTA: the deepest march (fewest repeated prologue planes) that
-// still gives at least four waves of CTAs over the GPU's resident slots, so
-// the last partial wave costs little.
-inline int zmarch_pick_zc(int tiles_xy, int nz, int slots)
+// Planes per CTA: the deepest march, up to zc_max planes (fewest repeated
+// prologue planes), that still gives at least `waves` waves of CTAs over the
+// GPU's resident slots, so the last partial wave costs little.
+inline int zmarch_pick_zc(int tiles_xy, int nz, int slots, int zc_max = 32, int waves = 4)
 {
-    static const int cand[] = {32, 24, 16, 12, 8};
+    static const int cand[] = {128, 96, 64, 48, 32, 24, 16, 12, 8};
     for (int zc : cand) {
+        if (zc > zc_max) continue;
         const long long ctas = static_cast<long long>(tiles_xy) * ((nz + zc - 1) / zc);
-        if (ctas >= 4LL * slots) return zc;
+        if (ctas >= static_cast<long long>(waves) * slots) return zc;
     }
     return 8;
 }
@@ -468,7 +475,7 @@ inline int zmarch_plan(int nx, int ny, int nz, ZmarchPlan *plan)
         cudaGetLastError();
         return 3;
     }
-    plan->zc = zmarch_pick_zc(tx * ty, nz, sms * (per_sm > 0 ? per_sm : 1));
+    plan->zc = zmarch_pick_zc(tx * ty, nz, sms * (per_sm > 0 ? per_sm : 1), TVFGP_ZM_ZC_MAX, TVFGP_ZM_WAVES);
     plan->grid = dim3(tx, ty, (nz + plan->zc - 1) / plan->zc);
     return 0;
 }
