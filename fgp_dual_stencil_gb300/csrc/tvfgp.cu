@@ -942,7 +942,7 @@ int tvfgp_host_free(void *p)
 int tvfgp_debug_projection_check(int mode, unsigned long long count, unsigned long long seed,
                                  unsigned long long *out, tvfgp_stream_t stream)
 {
-    if (mode < 0 || mode > 2 || out == nullptr || (reinterpret_cast<uintptr_t>(out) & 7u)) return TVFGP_ERR_ARG;
+    if (mode < 0 || mode > 3 || out == nullptr || (reinterpret_cast<uintptr_t>(out) & 7u)) return TVFGP_ERR_ARG;
     if (mode == 0) count = kNnEnd - kNnFirst;
     else if (count > (1ull << 40)) return TVFGP_ERR_ARG;
     if (count == 0) return TVFGP_OK;

@@ -217,6 +217,8 @@ int tvfgp_debug_timeout_probe(tvfgp_t h, int spins, tvfgp_stream_t stream);
  *           projection against the IEEE one;
  *   mode 2: `count` quotients, half of them within a few ulps of a power of
  *           two, against __fdiv_rn.
+ *   mode 3: `count` quads through the kernels' four-voxel update against
+ *           four updates built on the IEEE projection.
  * out is a device array of two unsigned long long that the caller sets to
  * {0, ULLONG_MAX}: out[0] receives the number of mismatches, out[1] the
  * smallest mismatching sample index.  count <= 2^40; TVFGP_ERR_ARG on a bad

@@ -3,7 +3,8 @@ and fused multiply-add corrections; the step is defined by the IEEE square
 root and division (the oracle uses them), so the fast path must return the
 same bits.  These tests run its self-check on the GPU: exhaustively for the
 square root and reciprocal, on 2^32 random triples for the whole projection,
-and on 2^32 quotients, half of them next to a power of two."""
+on 2^32 quotients, half of them next to a power of two, and on 2^28
+random quads through the kernels' four-voxel update."""
 import pytest
 
 pytestmark = pytest.mark.gpu
@@ -42,10 +43,16 @@ def test_quotients_near_binade_edges(T, seed):
     assert bad == 0, "%d of 2^32 quotients differ (first sample %d)" % (bad, first)
 
 
+@pytest.mark.parametrize("seed", [3, 0xface])
+def test_quad_update_random(T, seed):
+    bad, first = run_check(T, 3, 1 << 28, seed)
+    assert bad == 0, "%d of 2^28 quads differ (first sample %d)" % (bad, first)
+
+
 def test_check_argument_errors(T):
     import torch
     out = torch.zeros(2, dtype=torch.int64, device="cuda")
-    assert T.raw_call("tvfgp_debug_projection_check", 3, 10, 0, out.data_ptr(), None) == T.TVFGP_ERR_ARG
+    assert T.raw_call("tvfgp_debug_projection_check", 4, 10, 0, out.data_ptr(), None) == T.TVFGP_ERR_ARG
     assert T.raw_call("tvfgp_debug_projection_check", 1, (1 << 40) + 1, 0, out.data_ptr(), None) == T.TVFGP_ERR_ARG
     assert T.raw_call("tvfgp_debug_projection_check", 1, 10, 0, None, None) == T.TVFGP_ERR_ARG
     assert T.raw_call("tvfgp_debug_projection_check", 1, 10, 0, out.data_ptr() + 4, None) == T.TVFGP_ERR_ARG
