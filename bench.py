@@ -51,7 +51,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", default="c4", help="c1..c5 (default c4: 512^3)")
-    ap.add_argument("--variant", default="auto", choices=["auto", "fused", "scalar", "zmarch", "zmarch2", "separate"])
+    ap.add_argument("--variant", default="auto", choices=["auto", "fused", "scalar", "zmarch", "zmarch2", "separate", "cube"])
     ap.add_argument("--eager", action="store_true", help="launch eagerly instead of graph replay")
     ap.add_argument("--dual", default="f32", choices=["f32", "f16"],
                     help="storage of p and r (f16: binary16, fp32 arithmetic; changes the result)")
@@ -317,7 +317,8 @@ def gpu_arm(args, world, rank, local_rank, dist):
     kname = {T.TVFGP_VARIANT_FUSED: "fgp_step_fused4", T.TVFGP_VARIANT_SCALAR: "fgp_step_scalar",
              T.TVFGP_VARIANT_ZMARCH_TMA: "fgp_step_zmarch_tma",
              T.TVFGP_VARIANT_ZMARCH2_TMA: "fgp_step2_zmarch_tma",
-             T.TVFGP_VARIANT_SEPARATE: "primal_vec4 + dual_from_z_vec4"}.get(variant_used, "?")
+             T.TVFGP_VARIANT_SEPARATE: "primal_vec4 + dual_from_z_vec4",
+             T.TVFGP_VARIANT_CUBE_TMA: "fgp_step_cube_tma"}.get(variant_used, "?")
     if f16:
         kname += "<__half>"
     traffic = ncu_traffic(kname, N)             # DRAM bytes per launch (ncu), or None
@@ -345,7 +346,7 @@ def gpu_arm(args, world, rank, local_rank, dist):
     h.close()
     names = {T.TVFGP_VARIANT_FUSED: "fused", T.TVFGP_VARIANT_SCALAR: "scalar",
              T.TVFGP_VARIANT_ZMARCH_TMA: "zmarch", T.TVFGP_VARIANT_ZMARCH2_TMA: "zmarch2",
-             T.TVFGP_VARIANT_SEPARATE: "separate"}
+             T.TVFGP_VARIANT_SEPARATE: "separate", T.TVFGP_VARIANT_CUBE_TMA: "cube"}
     out = {
         "metric": METRIC,
         "value": round(value, 3),

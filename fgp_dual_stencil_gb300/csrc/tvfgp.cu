@@ -11,6 +11,7 @@
 #include "zmarch_tma.cuh"
 #include "zmarch2_tma.cuh"
 #include "selfcheck.cuh"
+#include "cube_tma.cuh"
 
 #include <cuda_runtime.h>
 
@@ -129,7 +130,8 @@ float step_of(float lam) { return static_cast<float>(1.0 / (12.0 * static_cast<d
 int resolve_variant(const tvfgp_handle *h, int requested, bool vec_ok)
 {
     int v = requested == TVFGP_VARIANT_AUTO ? kAutoVariant : requested;
-    if (v == TVFGP_VARIANT_FUSED || v == TVFGP_VARIANT_ZMARCH_TMA || v == TVFGP_VARIANT_ZMARCH2_TMA) {
+    if (v == TVFGP_VARIANT_FUSED || v == TVFGP_VARIANT_ZMARCH_TMA || v == TVFGP_VARIANT_ZMARCH2_TMA ||
+        v == TVFGP_VARIANT_CUBE_TMA) {
         if (!vec_ok) return TVFGP_VARIANT_SCALAR;
     }
     return v;
@@ -167,6 +169,11 @@ LaunchCfg step_cfg(const tvfgp_handle *h, int variant)
         c.block = dim3(zmarch_threads(), 1, 1);
         c.grid = zmarch_grid(h->zplan);
         c.smem = zmarch_smem_bytes();
+    } else if (variant == TVFGP_VARIANT_CUBE_TMA) {
+        c.func = cube_kernel();
+        c.block = dim3(cube_threads(), 1, 1);
+        c.grid = cube_grid(h->nx, h->ny, h->nz);
+        c.smem = cube_smem_bytes();
     } else {
         c.func = reinterpret_cast<const void *>(&fgp_step_scalar<float>);
         c.block = dim3(32, 8, 1);
@@ -203,6 +210,7 @@ struct KArgs {
     StepArgsT<__half> ah;
     ZmarchArgs za;
     ZmarchArgsT<__half> zah;
+    CubeArgs cb;
     Zmarch2Args z2;
     PrimalArgs pa;
     DualArgs da;
@@ -310,6 +318,10 @@ bool fill_item(const tvfgp_handle *h, const Item &it, const float *b, float lam,
     if (it.kernel == TVFGP_VARIANT_ZMARCH_TMA) {
         k.ptrs[0] = &k.za;
         return zmarch_fill(h->zplan, k.a, h->d_err, k.za);
+    }
+    if (it.kernel == TVFGP_VARIANT_CUBE_TMA) {
+        k.ptrs[0] = &k.cb;
+        return cube_fill(k.a, h->d_err, k.cb);
     }
     k.ptrs[0] = &k.a;
     return true;
@@ -576,9 +588,10 @@ int tvfgp_create_ex(int nx, int ny, int nz, int variant, unsigned flags, tvfgp_t
     *out = nullptr;
     if (nx < 1 || ny < 1 || nz < 1 || nx > 65535 || ny > 65535 || nz > 65535) return TVFGP_ERR_ARG;
     if (static_cast<long long>(nx) * ny * (static_cast<long long>(nz) + 1) > INT_MAX) return TVFGP_ERR_ARG;
-    if (variant < TVFGP_VARIANT_AUTO || variant > TVFGP_VARIANT_SEPARATE || flags != 0)
+    if (variant < TVFGP_VARIANT_AUTO || variant > TVFGP_VARIANT_CUBE_TMA || flags != 0)
         return TVFGP_ERR_ARG;
-    if ((variant == TVFGP_VARIANT_ZMARCH_TMA || variant == TVFGP_VARIANT_ZMARCH2_TMA) &&
+    if ((variant == TVFGP_VARIANT_ZMARCH_TMA || variant == TVFGP_VARIANT_ZMARCH2_TMA ||
+         variant == TVFGP_VARIANT_CUBE_TMA) &&
         !zmarch_available())
         return TVFGP_ERR_UNSUPPORTED;
     tvfgp_handle *h = new (std::nothrow) tvfgp_handle();
@@ -647,13 +660,14 @@ int tvfgp_destroy(tvfgp_t h)
 
 int tvfgp_set_variant(tvfgp_t h, int variant)
 {
-    if (!valid(h) || variant < TVFGP_VARIANT_AUTO || variant > TVFGP_VARIANT_SEPARATE)
+    if (!valid(h) || variant < TVFGP_VARIANT_AUTO || variant > TVFGP_VARIANT_CUBE_TMA)
         return TVFGP_ERR_ARG;
     if (variant == TVFGP_VARIANT_SEPARATE) {
         const int rc = ensure_z_scratch(h);
         if (rc != TVFGP_OK) return rc;
     }
-    if ((variant == TVFGP_VARIANT_ZMARCH_TMA || variant == TVFGP_VARIANT_ZMARCH2_TMA) &&
+    if ((variant == TVFGP_VARIANT_ZMARCH_TMA || variant == TVFGP_VARIANT_ZMARCH2_TMA ||
+         variant == TVFGP_VARIANT_CUBE_TMA) &&
         !zmarch_available())
         return TVFGP_ERR_UNSUPPORTED;
     const int want_pairs = variant == TVFGP_VARIANT_ZMARCH2_TMA ||

@@ -32,10 +32,12 @@ TVFGP_VARIANT_SCALAR = 2
 TVFGP_VARIANT_ZMARCH_TMA = 3
 TVFGP_VARIANT_ZMARCH2_TMA = 4
 TVFGP_VARIANT_SEPARATE = 5
+TVFGP_VARIANT_CUBE_TMA = 6
 
 VARIANTS = {"auto": TVFGP_VARIANT_AUTO, "fused": TVFGP_VARIANT_FUSED,
             "scalar": TVFGP_VARIANT_SCALAR, "zmarch": TVFGP_VARIANT_ZMARCH_TMA,
-            "zmarch2": TVFGP_VARIANT_ZMARCH2_TMA, "separate": TVFGP_VARIANT_SEPARATE}
+            "zmarch2": TVFGP_VARIANT_ZMARCH2_TMA, "separate": TVFGP_VARIANT_SEPARATE,
+            "cube": TVFGP_VARIANT_CUBE_TMA}
 
 
 class TvfgpError(RuntimeError):

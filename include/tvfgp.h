@@ -87,10 +87,14 @@ enum tvfgp_variant {
                                      buffer sets (9*nx*ny*nz more floats), allocated by
                                      tvfgp_create_ex / tvfgp_set_variant.  Same requirements
                                      as ZMARCH_TMA. */
-    TVFGP_VARIANT_SEPARATE = 5     /* the page's two-kernel step ("Variants", first row): one
+    TVFGP_VARIANT_SEPARATE = 5,    /* the page's two-kernel step ("Variants", first row): one
                                      kernel writes z, the next reads it (18 volumes per step
                                      instead of 13); for comparison.  Any shape; the handle
                                      then owns an N-float z buffer. */
+    TVFGP_VARIANT_CUBE_TMA = 6     /* the page's cube-tiled step ("Variants", 16 x 8 x 4 tile
+                                     row): b and r of a 16 x 8 x 4 tile and its one-voxel halo
+                                     staged in shared memory by TMA, z computed once per tile
+                                     voxel; for comparison.  Same requirements as ZMARCH_TMA. */
 };
 
 /* Create a handle for an nx x ny x nz volume on the current CUDA device.

@@ -21,7 +21,7 @@ def T():
     return tvfgp
 
 
-VEC_VARIANTS = ["fused", "zmarch", "zmarch2", "scalar", "separate"]
+VEC_VARIANTS = ["fused", "zmarch", "zmarch2", "scalar", "separate", "cube"]
 
 
 # ---------------------------------------------------------------------------
@@ -41,11 +41,12 @@ def test_small_workloads_exact(T, key, variant):
     assert launched == w.outers * per_outer + 2
 
 
-def test_256_warm_started_outers_graph(T):
+@pytest.mark.parametrize("variant", ["auto", "cube"])
+def test_256_warm_started_outers_graph(T, variant):
     """20 outers x 10 steps, fresh noise per outer, t0 reset, graph replay
     re-parameterised with every new b."""
     w = synth.WORKLOADS["c3"]
-    b, *gpu, _ = run_workload_gpu(w, "auto", graph=True)
+    b, *gpu, _ = run_workload_gpu(w, variant, graph=True)
     ref = run_workload_oracle(w)
     assert_parity(gpu, ref[1:], float(np.abs(b).max()), exact=True, what="c3")
 
