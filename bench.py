@@ -55,6 +55,9 @@ def parse_args():
     ap.add_argument("--eager", action="store_true", help="launch eagerly instead of graph replay")
     ap.add_argument("--dual", default="f32", choices=["f32", "f16"],
                     help="storage of p and r (f16: binary16, fp32 arithmetic; changes the result)")
+    ap.add_argument("--pitch", default="dense", choices=["dense", "fft"],
+                    help="row layout of every volume: dense, or padded to 2*(nx/2+1) floats "
+                         "(in-place real-to-complex FFT layout; runs the scalar kernels)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -239,22 +242,30 @@ def gpu_arm(args, world, rank, local_rank, dist):
     n_b = max(1, min(w.outers, W + K))
 
     base = synth.phantom(w)
+    pitch = T.fft_pitch(w.nx) if args.pitch == "fft" else w.nx
     # inputs staged in the library's write-combined page-locked memory: the
     # GPU reads it at a steady rate (CPU-cached pinned pages on a coherent
     # host showed copy times varying several-fold from copy to copy)
     b_host = []
     for k in range(n_b):
-        t = T.host_tensor((w.nz, w.ny, w.nx), write_combined=True)
-        t.numpy()[...] = synth.make_b(w, k, base)
+        t = T.host_tensor((w.nz, w.ny, pitch), write_combined=True)
+        bk = synth.make_b(w, k, base)
+        if pitch == w.nx:
+            t.numpy()[...] = bk
+        else:
+            full = np.zeros((w.nz, w.ny, pitch), np.float32)
+            full[..., :w.nx] = bk
+            t.numpy()[...] = full
         b_host.append(t)
     b_dev = [x.to(dev) for x in b_host]
-    shape = (3, w.nz, w.ny, w.nx)
+    shape = (3, w.nz, w.ny, pitch)
     f16 = args.dual == "f16"
     ddt = torch.float16 if f16 else torch.float32
     p = torch.zeros(shape, dtype=ddt, device=dev)
     r = torch.zeros(shape, dtype=ddt, device=dev)
-    z = torch.empty((w.nz, w.ny, w.nx), device=dev)
-    h = T.Tvfgp(w.nx, w.ny, w.nz, args.variant, graph=not args.eager)
+    z = torch.empty((w.nz, w.ny, pitch), device=dev)
+    h = T.Tvfgp(w.nx, w.ny, w.nz, args.variant, graph=not args.eager,
+                pitch=None if pitch == w.nx else pitch)
     stream = torch.cuda.current_stream(dev)
     run = h.run_f16 if f16 else h.run
     primal = h.primal_f16 if f16 else h.primal
@@ -330,7 +341,7 @@ def gpu_arm(args, world, rank, local_rank, dist):
     if not args.no_e2e:
         e2e_s = end_to_end(torch, h, w, b_host, p, r, stream, dev, K, dist, run, primal)
         e2e = {"value": round(world * N * w.steps * K / e2e_s / 1e9, 3), "unit": UNIT,
-               "h2d_bytes_per_step": 4 * N, "d2h_bytes_per_step": 4 * N,
+               "h2d_bytes_per_step": 4 * w.ny * w.nz * pitch, "d2h_bytes_per_step": 4 * w.ny * w.nz * pitch,
                "ms_per_step": round(e2e_s * 1e3 / K, 4),
                "overlap": "H2D of step j+1 and D2H of step j on two copy streams, double-buffered",
                "host_memory": "b from write-combined page-locked memory, z to page-locked memory "
@@ -372,6 +383,7 @@ def gpu_arm(args, world, rank, local_rank, dist):
             "nx": w.nx, "ny": w.ny, "nz": w.nz, "fgp_steps_per_bench_step": w.steps,
             "variant": names.get(variant_used, str(variant_used)),
             "launch": "eager" if args.eager else "cuda_graph",
+            "row_pitch": pitch,
             "l2": "inputs larger than L2 (%.1f GB of live buffers vs 126 MB L2)" % (11 * 4 * N / 1e9)
             if 4 * N > 129e6 else "working set fits in L2: GB/s is not an HBM figure",
             "parallelism": "replicas" if world > 1 else "single_gpu",
@@ -404,7 +416,7 @@ def end_to_end(torch, h, w, b_host, p, r, stream, dev, K, dist, run, primal):
     """Wall time of K outer iterations where each step's b comes from pinned
     host memory and its z goes back to pinned host memory."""
     n_b = len(b_host)
-    shape = (w.nz, w.ny, w.nx)
+    shape = tuple(b_host[0].shape)
     b_in = [torch.empty(shape, device=dev) for _ in range(2)]
     z_out = [torch.empty(shape, device=dev) for _ in range(2)]
     from fgp_dual_stencil_gb300 import tvfgp as T

@@ -42,7 +42,8 @@ struct StepArgsT {
     float s;           // 1/(12 lambda) rounded once to float
     float m;           // momentum weight of this step
     int nx, ny, nz;
-    long long N;       // nx*ny*nz
+    long long N;       // elements per volume: px*ny*nz
+    int px = 0;        // row pitch in elements (0: nx); only the scalar kernels take px != nx
 };
 using StepArgs = StepArgsT<float>;
 
@@ -53,7 +54,8 @@ struct PrimalArgsT {
     float *z;
     float lam;
     int nx, ny, nz;
-    long long N;
+    long long N;       // elements per volume: px*ny*nz
+    int px = 0;        // row pitch in elements (0: nx); only the scalar kernels take px != nx
 };
 using PrimalArgs = PrimalArgsT<float>;
 
@@ -470,11 +472,11 @@ __global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(con
 template <typename TS>
 __device__ __forceinline__ float zpoint(const float *__restrict__ b, const TS *__restrict__ r0,
                                         const TS *__restrict__ r1, const TS *__restrict__ r2,
-                                        int x, int y, int z, long long j, int nx, long long sz,
+                                        int x, int y, int z, long long j, int px, long long sz,
                                         float lam)
 {
     const float d0 = __fsub_rn(ld1_ro(r0 + j), x > 0 ? ld1_ro(r0 + j - 1) : 0.0f);
-    const float d1 = __fsub_rn(ld1_ro(r1 + j), y > 0 ? ld1_ro(r1 + j - nx) : 0.0f);
+    const float d1 = __fsub_rn(ld1_ro(r1 + j), y > 0 ? ld1_ro(r1 + j - px) : 0.0f);
     const float d2 = __fsub_rn(ld1_ro(r2 + j), z > 0 ? ld1_ro(r2 + j - sz) : 0.0f);
     return zval(__ldg(b + j), lam, d0, d1, d2);
 }
@@ -486,19 +488,20 @@ __global__ void __launch_bounds__(256) fgp_step_scalar(const StepArgsT<TS> a)
     const int y = blockIdx.y * 8 + threadIdx.y;
     const int z = blockIdx.z;
     const int nx = a.nx, ny = a.ny, nz = a.nz;
+    const int px = a.px > 0 ? a.px : nx;             // row pitch
     if (x >= nx || y >= ny) return;
-    const long long sz = (long long)nx * ny;
-    const long long i = x + (long long)nx * y + sz * z;
+    const long long sz = (long long)px * ny;
+    const long long i = x + (long long)px * y + sz * z;
     const TS *r0 = a.rs, *r1 = a.rs + a.N, *r2 = a.rs + 2 * a.N;
 
     // the voxel's own p and r first
     float P0 = ld1_once(a.p + i), P1 = ld1_once(a.p + a.N + i), P2 = ld1_once(a.p + 2 * a.N + i);
     float R0 = ld1_ro(r0 + i), R1 = ld1_ro(r1 + i), R2 = ld1_ro(r2 + i);
 
-    const float zc = zpoint(a.b, r0, r1, r2, x, y, z, i, nx, sz, a.lam);
-    const float g0 = (x < nx - 1) ? __fsub_rn(zc, zpoint(a.b, r0, r1, r2, x + 1, y, z, i + 1, nx, sz, a.lam)) : 0.0f;
-    const float g1 = (y < ny - 1) ? __fsub_rn(zc, zpoint(a.b, r0, r1, r2, x, y + 1, z, i + nx, nx, sz, a.lam)) : 0.0f;
-    const float g2 = (z < nz - 1) ? __fsub_rn(zc, zpoint(a.b, r0, r1, r2, x, y, z + 1, i + sz, nx, sz, a.lam)) : 0.0f;
+    const float zc = zpoint(a.b, r0, r1, r2, x, y, z, i, px, sz, a.lam);
+    const float g0 = (x < nx - 1) ? __fsub_rn(zc, zpoint(a.b, r0, r1, r2, x + 1, y, z, i + 1, px, sz, a.lam)) : 0.0f;
+    const float g1 = (y < ny - 1) ? __fsub_rn(zc, zpoint(a.b, r0, r1, r2, x, y + 1, z, i + px, px, sz, a.lam)) : 0.0f;
+    const float g2 = (z < nz - 1) ? __fsub_rn(zc, zpoint(a.b, r0, r1, r2, x, y, z + 1, i + sz, px, sz, a.lam)) : 0.0f;
     dual_update(R0, R1, R2, g0, g1, g2, P0, P1, P2, a.s, a.m);
     st1(a.p + i, P0);
     st1(a.p + a.N + i, P1);
@@ -547,10 +550,11 @@ __global__ void __launch_bounds__(256) primal_scalar(const PrimalArgsT<TS> a)
     const int y = blockIdx.y * 8 + threadIdx.y;
     const int z = blockIdx.z;
     const int nx = a.nx, ny = a.ny;
+    const int px = a.px > 0 ? a.px : nx;             // row pitch
     if (x >= nx || y >= ny) return;
-    const long long sz = (long long)nx * ny;
-    const long long i = x + (long long)nx * y + sz * z;
-    a.z[i] = zpoint(a.b, a.d, a.d + a.N, a.d + 2 * a.N, x, y, z, i, nx, sz, a.lam);
+    const long long sz = (long long)px * ny;
+    const long long i = x + (long long)px * y + sz * z;
+    a.z[i] = zpoint(a.b, a.d, a.d + a.N, a.d + 2 * a.N, x, y, z, i, px, sz, a.lam);
 }
 
 // ---------------------------------------------------------------------------
@@ -567,7 +571,8 @@ struct DualArgs {
     float *rd;
     float s, m;
     int nx, ny, nz;
-    long long N;
+    long long N;       // elements per volume: px*ny*nz
+    int px = 0;        // row pitch in elements (0: nx); only the scalar kernel takes px != nx
 };
 
 template <int BY>
@@ -628,14 +633,15 @@ __global__ void __launch_bounds__(256) dual_from_z_scalar(const DualArgs a)
     const int y = blockIdx.y * 8 + threadIdx.y;
     const int z = blockIdx.z;
     const int nx = a.nx, ny = a.ny, nz = a.nz;
+    const int px = a.px > 0 ? a.px : nx;             // row pitch
     if (x >= nx || y >= ny) return;
-    const long long sz = (long long)nx * ny;
-    const long long i = x + (long long)nx * y + sz * z;
+    const long long sz = (long long)px * ny;
+    const long long i = x + (long long)px * y + sz * z;
     float P0 = __ldcs(a.p + i), P1 = __ldcs(a.p + a.N + i), P2 = __ldcs(a.p + 2 * a.N + i);
     float R0 = __ldg(a.rs + i), R1 = __ldg(a.rs + a.N + i), R2 = __ldg(a.rs + 2 * a.N + i);
     const float zc = __ldg(a.z + i);
     const float g0 = (x < nx - 1) ? __fsub_rn(zc, __ldg(a.z + i + 1)) : 0.0f;
-    const float g1 = (y < ny - 1) ? __fsub_rn(zc, __ldg(a.z + i + nx)) : 0.0f;
+    const float g1 = (y < ny - 1) ? __fsub_rn(zc, __ldg(a.z + i + px)) : 0.0f;
     const float g2 = (z < nz - 1) ? __fsub_rn(zc, __ldg(a.z + i + sz)) : 0.0f;
     dual_update(R0, R1, R2, g0, g1, g2, P0, P1, P2, a.s, a.m);
     a.p[i] = P0;

@@ -51,6 +51,29 @@ struct LaunchCfg {
     size_t smem;
 };
 
+// The copy of the final r back from the scratch dual: one contiguous copy of
+// `width` bytes, or (pitch != 0, padded rows) `height` rows of `width`
+// bytes at a row pitch of `pitch` bytes, leaving the padding untouched.
+struct CopySpec {
+    size_t width = 0, height = 1, pitch = 0;
+};
+
+cudaMemcpy3DParms copy_params(const CopySpec &c, void *dst, const void *src)
+{
+    cudaMemcpy3DParms q = {};
+    q.srcPtr = make_cudaPitchedPtr(const_cast<void *>(src), c.pitch, c.width, c.height);
+    q.dstPtr = make_cudaPitchedPtr(dst, c.pitch, c.width, c.height);
+    q.extent = make_cudaExtent(c.width, c.height, 1);
+    q.kind = cudaMemcpyDeviceToDevice;
+    return q;
+}
+
+cudaError_t enqueue_copy(const CopySpec &c, void *dst, const void *src, cudaStream_t st)
+{
+    if (c.pitch == 0) return cudaMemcpyAsync(dst, src, c.width, cudaMemcpyDeviceToDevice, st);
+    return cudaMemcpy2DAsync(dst, c.pitch, src, c.pitch, c.width, c.height, cudaMemcpyDeviceToDevice, st);
+}
+
 struct GraphEntry {
     int nsteps = -1;
     int variant = -1;
@@ -58,7 +81,7 @@ struct GraphEntry {
     cudaGraphExec_t exec = nullptr;
     std::vector<cudaGraphNode_t> knodes;
     cudaGraphNode_t cnode = nullptr;
-    size_t copy_bytes = 0;
+    CopySpec copy;
     // parameters the instantiated graph currently holds
     const float *b = nullptr;
     float *p = nullptr, *r = nullptr;
@@ -74,7 +97,8 @@ constexpr int kGraphSlots = 4;
 struct tvfgp_handle {
     int magic;
     int nx, ny, nz;
-    long long N;
+    int px;                        // row pitch of every volume (nx unless created pitched)
+    long long N;                   // elements per volume: px*ny*nz
     int variant;
     int graph_on;
     int last_variant;
@@ -108,6 +132,24 @@ int check_ptr(const void *p)
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Rows stored without padding: the vector and TMA kernels need it.
+bool dense(const tvfgp_handle *h) { return h->px == h->nx; }
+
+// The copy of a whole dual field (3 components) with elements of es bytes:
+// contiguous, or only the x < nx part of every padded row.
+CopySpec dual_copy(const tvfgp_handle *h, size_t es)
+{
+    CopySpec c;
+    if (dense(h)) {
+        c.width = 3 * static_cast<size_t>(h->N) * es;
+    } else {
+        c.width = static_cast<size_t>(h->nx) * es;
+        c.height = 3 * static_cast<size_t>(h->ny) * static_cast<size_t>(h->nz);
+        c.pitch = static_cast<size_t>(h->px) * es;
+    }
+    return c;
+}
 
 bool overlap(const void *a, size_t na, const void *b, size_t nb)
 {
@@ -152,6 +194,7 @@ StepArgs make_args(const tvfgp_handle *h, const float *b, float *p, const float 
     a.ny = h->ny;
     a.nz = h->nz;
     a.N = h->N;
+    a.px = h->px;
     return a;
 }
 
@@ -276,6 +319,7 @@ bool fill_item(const tvfgp_handle *h, const Item &it, const float *b, float lam,
         k.ah.ny = h->ny;
         k.ah.nz = h->nz;
         k.ah.N = h->N;
+        k.ah.px = h->px;
         if (it.kernel == kKernZmarchH) {
             k.ptrs[0] = &k.zah;
             return zmarch_fill(h->zplan_h, k.ah, h->d_err, k.zah);
@@ -292,6 +336,7 @@ bool fill_item(const tvfgp_handle *h, const Item &it, const float *b, float lam,
         k.pa.ny = h->ny;
         k.pa.nz = h->nz;
         k.pa.N = h->N;
+        k.pa.px = h->px;
         k.ptrs[0] = &k.pa;
         return h->zscratch != nullptr;
     }
@@ -306,6 +351,7 @@ bool fill_item(const tvfgp_handle *h, const Item &it, const float *b, float lam,
         k.da.ny = h->ny;
         k.da.nz = h->nz;
         k.da.N = h->N;
+        k.da.px = h->px;
         k.ptrs[0] = &k.da;
         return h->zscratch != nullptr;
     }
@@ -427,7 +473,7 @@ bool node_params(tvfgp_handle *h, const Item &it, const float *b, float lam, KAr
 
 int build_graph(tvfgp_handle *h, GraphEntry &g, int variant, const float *b, float *p, float *r,
                 float lam, int nsteps, double t0, const std::vector<Item> &items, bool copy_back,
-                size_t copy_bytes)
+                const CopySpec &copy)
 {
     destroy_graph(g);
     cudaError_t e = cudaGraphCreate(&g.graph, 0);
@@ -445,9 +491,15 @@ int build_graph(tvfgp_handle *h, GraphEntry &g, int variant, const float *b, flo
         if (e != cudaSuccess) break;
         prev = g.knodes[k];
     }
-    if (e == cudaSuccess && copy_back)
-        e = cudaGraphAddMemcpyNode1D(&g.cnode, g.graph, &prev, 1, r, h->scratch, copy_bytes,
-                                     cudaMemcpyDeviceToDevice);
+    if (e == cudaSuccess && copy_back) {
+        if (copy.pitch == 0) {
+            e = cudaGraphAddMemcpyNode1D(&g.cnode, g.graph, &prev, 1, r, h->scratch, copy.width,
+                                         cudaMemcpyDeviceToDevice);
+        } else {
+            const cudaMemcpy3DParms q = copy_params(copy, r, h->scratch);
+            e = cudaGraphAddMemcpyNode(&g.cnode, g.graph, &prev, 1, &q);
+        }
+    }
     if (e == cudaSuccess) e = cudaGraphInstantiate(&g.exec, g.graph, 0);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -456,7 +508,7 @@ int build_graph(tvfgp_handle *h, GraphEntry &g, int variant, const float *b, flo
     }
     g.nsteps = nsteps;
     g.variant = variant;
-    g.copy_bytes = copy_bytes;
+    g.copy = copy;
     g.b = b;
     g.p = p;
     g.r = r;
@@ -478,9 +530,15 @@ int update_graph(tvfgp_handle *h, GraphEntry &g, const float *b, float *p, float
         }
         e = cudaGraphExecKernelNodeSetParams(g.exec, g.knodes[k], &kp);
     }
-    if (e == cudaSuccess && g.cnode)
-        e = cudaGraphExecMemcpyNodeSetParams1D(g.exec, g.cnode, r, h->scratch, g.copy_bytes,
-                                               cudaMemcpyDeviceToDevice);
+    if (e == cudaSuccess && g.cnode) {
+        if (g.copy.pitch == 0) {
+            e = cudaGraphExecMemcpyNodeSetParams1D(g.exec, g.cnode, r, h->scratch, g.copy.width,
+                                                   cudaMemcpyDeviceToDevice);
+        } else {
+            const cudaMemcpy3DParms q = copy_params(g.copy, r, h->scratch);
+            e = cudaGraphExecMemcpyNodeSetParams(g.exec, g.cnode, &q);
+        }
+    }
     if (e != cudaSuccess) {
         cudaGetLastError();
         return from_cuda(e);
@@ -495,7 +553,7 @@ int update_graph(tvfgp_handle *h, GraphEntry &g, const float *b, float *p, float
 
 int run_graph(tvfgp_handle *h, int variant, const float *b, float *p, float *r, float lam,
               int nsteps, double t0, const std::vector<Item> &items, bool copy_back,
-              size_t copy_bytes, cudaStream_t st)
+              const CopySpec &copy, cudaStream_t st)
 {
     GraphEntry *g = nullptr;
     for (auto &e : h->graphs)
@@ -506,7 +564,7 @@ int run_graph(tvfgp_handle *h, int variant, const float *b, float *p, float *r, 
         for (auto &e : h->graphs)
             if (!e.exec || e.use < victim->use) victim = &e;
         g = victim;
-        rc = build_graph(h, *g, variant, b, p, r, lam, nsteps, t0, items, copy_back, copy_bytes);
+        rc = build_graph(h, *g, variant, b, p, r, lam, nsteps, t0, items, copy_back, copy);
     } else if (g->b != b || g->p != p || g->r != r || g->lam != lam || g->t0 != t0) {
         rc = update_graph(h, *g, b, p, r, lam, t0, items);
     }
@@ -582,12 +640,13 @@ int tvfgp_momentum(double t0, int nsteps, double *m, double *t_final)
     return TVFGP_OK;
 }
 
-int tvfgp_create_ex(int nx, int ny, int nz, int variant, unsigned flags, tvfgp_t *out)
+static int create_impl(int nx, int ny, int nz, int px, int variant, unsigned flags, tvfgp_t *out)
 {
     if (out == nullptr) return TVFGP_ERR_ARG;
     *out = nullptr;
     if (nx < 1 || ny < 1 || nz < 1 || nx > 65535 || ny > 65535 || nz > 65535) return TVFGP_ERR_ARG;
-    if (static_cast<long long>(nx) * ny * (static_cast<long long>(nz) + 1) > INT_MAX) return TVFGP_ERR_ARG;
+    if (px < nx || px > 65535) return TVFGP_ERR_ARG;
+    if (static_cast<long long>(px) * ny * (static_cast<long long>(nz) + 1) > INT_MAX) return TVFGP_ERR_ARG;
     if (variant < TVFGP_VARIANT_AUTO || variant > TVFGP_VARIANT_CUBE_TMA || flags != 0)
         return TVFGP_ERR_ARG;
     if ((variant == TVFGP_VARIANT_ZMARCH_TMA || variant == TVFGP_VARIANT_ZMARCH2_TMA ||
@@ -600,7 +659,8 @@ int tvfgp_create_ex(int nx, int ny, int nz, int variant, unsigned flags, tvfgp_t
     h->nx = nx;
     h->ny = ny;
     h->nz = nz;
-    h->N = static_cast<long long>(nx) * ny * nz;
+    h->px = px;
+    h->N = static_cast<long long>(px) * ny * nz;
     h->variant = variant;
     h->graph_on = 0;
     h->last_variant = -1;
@@ -621,7 +681,7 @@ int tvfgp_create_ex(int nx, int ny, int nz, int variant, unsigned flags, tvfgp_t
     }
     const int want_pairs = variant == TVFGP_VARIANT_ZMARCH2_TMA ||
                            (variant == TVFGP_VARIANT_AUTO && kAutoVariant == TVFGP_VARIANT_ZMARCH2_TMA);
-    if (e == cudaSuccess && want_pairs && nx % 4 == 0 && ensure_pair_scratch(h) != TVFGP_OK)
+    if (e == cudaSuccess && want_pairs && nx % 4 == 0 && px == nx && ensure_pair_scratch(h) != TVFGP_OK)
         e = cudaErrorMemoryAllocation;
     if (e == cudaSuccess && variant == TVFGP_VARIANT_SEPARATE && ensure_z_scratch(h) != TVFGP_OK)
         e = cudaErrorMemoryAllocation;
@@ -637,6 +697,16 @@ int tvfgp_create_ex(int nx, int ny, int nz, int variant, unsigned flags, tvfgp_t
     }
     *out = h;
     return TVFGP_OK;
+}
+
+int tvfgp_create_ex(int nx, int ny, int nz, int variant, unsigned flags, tvfgp_t *out)
+{
+    return create_impl(nx, ny, nz, nx, variant, flags, out);
+}
+
+int tvfgp_create_pitched(int nx, int ny, int nz, int pitch, tvfgp_t *out)
+{
+    return create_impl(nx, ny, nz, pitch, TVFGP_VARIANT_AUTO, 0u, out);
 }
 
 int tvfgp_create(int nx, int ny, int nz, tvfgp_t *out)
@@ -672,7 +742,7 @@ int tvfgp_set_variant(tvfgp_t h, int variant)
         return TVFGP_ERR_UNSUPPORTED;
     const int want_pairs = variant == TVFGP_VARIANT_ZMARCH2_TMA ||
                            (variant == TVFGP_VARIANT_AUTO && kAutoVariant == TVFGP_VARIANT_ZMARCH2_TMA);
-    if (want_pairs && h->nx % 4 == 0) {
+    if (want_pairs && h->nx % 4 == 0 && dense(h)) {
         const int rc = ensure_pair_scratch(h);
         if (rc != TVFGP_OK) return rc;
     }
@@ -705,7 +775,7 @@ int tvfgp_step(tvfgp_t h, const float *b, float *p, const float *r_src, float *r
         overlap(p, 3 * v, r_src, 3 * v) || overlap(p, 3 * v, r_dst, 3 * v) ||
         overlap(r_src, 3 * v, r_dst, 3 * v))
         return TVFGP_ERR_ARG;
-    const bool vec_ok = (h->nx % 4 == 0) && aligned16(b) && aligned16(p) && aligned16(r_src) &&
+    const bool vec_ok = dense(h) && (h->nx % 4 == 0) && aligned16(b) && aligned16(p) && aligned16(r_src) &&
                         aligned16(r_dst);
     int variant = resolve_variant(h, h->variant, vec_ok);
     if (variant == TVFGP_VARIANT_ZMARCH2_TMA) variant = TVFGP_VARIANT_ZMARCH_TMA;   // one step only
@@ -745,19 +815,19 @@ int tvfgp_run(tvfgp_t h, const float *b, float *p, float *r, float lambda, int n
         if (t_final) *t_final = tf;
         return TVFGP_OK;
     }
-    const bool vec_ok = (h->nx % 4 == 0) && aligned16(b) && aligned16(p) && aligned16(r);
+    const bool vec_ok = dense(h) && (h->nx % 4 == 0) && aligned16(b) && aligned16(p) && aligned16(r);
     const int variant = resolve_variant(h, h->variant, vec_ok);
     std::vector<Item> items;
     bool copy_back = false;
     plan_run(h, variant, vec_ok, p, r, m, items, &copy_back);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (h->graph_on) {
-        rc = run_graph(h, variant, b, p, r, lambda, nsteps, t0, items, copy_back, 3 * v, st);
+        rc = run_graph(h, variant, b, p, r, lambda, nsteps, t0, items, copy_back, dual_copy(h, 4), st);
     } else {
         for (size_t k = 0; k < items.size() && rc == TVFGP_OK; ++k)
             rc = launch_item(h, items[k], b, lambda, st);
         if (rc == TVFGP_OK && copy_back) {
-            cudaError_t e = cudaMemcpyAsync(r, h->scratch, 3 * v, cudaMemcpyDeviceToDevice, st);
+            cudaError_t e = enqueue_copy(dual_copy(h, 4), r, h->scratch, st);
             if (e != cudaSuccess) {
                 cudaGetLastError();
                 rc = from_cuda(e);
@@ -790,7 +860,8 @@ int tvfgp_primal(tvfgp_t h, const float *b, const float *dual, float lambda, flo
     a.ny = h->ny;
     a.nz = h->nz;
     a.N = h->N;
-    const bool vec_ok = (h->nx % 4 == 0) && aligned16(b) && aligned16(dual) && aligned16(z);
+    a.px = h->px;
+    const bool vec_ok = dense(h) && (h->nx % 4 == 0) && aligned16(b) && aligned16(dual) && aligned16(z);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (vec_ok) {
         dim3 grid((h->nx / 4 + 31) / 32, (h->ny + kPrimalBY - 1) / kPrimalBY, h->nz);
@@ -828,11 +899,11 @@ int tvfgp_run_f16(tvfgp_t h, const float *b, unsigned short *p, unsigned short *
         if (t_final) *t_final = tf;
         return TVFGP_OK;
     }
-    const bool vec_ok = (h->nx % 4 == 0) && aligned16(b) && (reinterpret_cast<uintptr_t>(p) & 7u) == 0 &&
+    const bool vec_ok = dense(h) && (h->nx % 4 == 0) && aligned16(b) && (reinterpret_cast<uintptr_t>(p) & 7u) == 0 &&
                         (reinterpret_cast<uintptr_t>(r) & 7u) == 0;
     // The z-march moves rows of whole 16-byte units: nx % 8 == 0 and every
     // component's base 16-byte aligned (N is then a multiple of 8).
-    const bool march_ok = zmarch_supported<__half>(h->nx, h->ny, h->nz) && zmarch_available() &&
+    const bool march_ok = dense(h) && zmarch_supported<__half>(h->nx, h->ny, h->nz) && zmarch_available() &&
                           aligned16(b) && aligned16(p) && aligned16(r);
     int kern = kKernScalarH, ran = TVFGP_VARIANT_SCALAR;
     if (h->variant != TVFGP_VARIANT_SCALAR && h->variant != TVFGP_VARIANT_FUSED && march_ok) {
@@ -852,12 +923,12 @@ int tvfgp_run_f16(tvfgp_t h, const float *b, unsigned short *p, unsigned short *
     const bool copy_back = (nsteps % 2) == 1;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (h->graph_on) {
-        rc = run_graph(h, kern, b, pf, rf, lambda, nsteps, t0, items, copy_back, d, st);
+        rc = run_graph(h, kern, b, pf, rf, lambda, nsteps, t0, items, copy_back, dual_copy(h, 2), st);
     } else {
         for (size_t k = 0; k < items.size() && rc == TVFGP_OK; ++k)
             rc = launch_item(h, items[k], b, lambda, st);
         if (rc == TVFGP_OK && copy_back) {
-            cudaError_t e = cudaMemcpyAsync(r, h->scratch, d, cudaMemcpyDeviceToDevice, st);
+            cudaError_t e = enqueue_copy(dual_copy(h, 2), r, h->scratch, st);
             if (e != cudaSuccess) {
                 cudaGetLastError();
                 rc = from_cuda(e);
@@ -892,7 +963,8 @@ int tvfgp_primal_f16(tvfgp_t h, const float *b, const unsigned short *dual, floa
     a.ny = h->ny;
     a.nz = h->nz;
     a.N = h->N;
-    const bool vec_ok = (h->nx % 4 == 0) && aligned16(b) && aligned16(z) &&
+    a.px = h->px;
+    const bool vec_ok = dense(h) && (h->nx % 4 == 0) && aligned16(b) && aligned16(z) &&
                         (reinterpret_cast<uintptr_t>(dual) & 7u) == 0;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (vec_ok) {
@@ -1058,6 +1130,7 @@ extern "C" int tvfgp_run_noalloc(int nx, int ny, int nz, const float *b, float *
     a.ny = ny;
     a.nz = nz;
     a.N = N;
+    a.px = nx;
     dim3 grid, block;
     const void *fn;
     if (vec_ok) {

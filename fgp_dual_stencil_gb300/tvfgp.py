@@ -56,6 +56,7 @@ def _load():
     sig = {
         "tvfgp_create": ([i, i, i, ctypes.POINTER(vp)], i),
         "tvfgp_create_ex": ([i, i, i, i, u, ctypes.POINTER(vp)], i),
+        "tvfgp_create_pitched": ([i, i, i, i, ctypes.POINTER(vp)], i),
         "tvfgp_destroy": ([vp], i),
         "tvfgp_set_variant": ([vp, i], i),
         "tvfgp_set_graph": ([vp, i], i),
@@ -158,6 +159,21 @@ def tvfgp_create(nx: int, ny: int, nz: int, variant: int | str = TVFGP_VARIANT_A
     _ok(_lib.tvfgp_create_ex(int(nx), int(ny), int(nz), int(variant), int(flags), ctypes.byref(h)),
         "tvfgp_create")
     return h.value
+
+
+def tvfgp_create_pitched(nx: int, ny: int, nz: int, pitch: int) -> int:
+    """Create a handle for volumes whose rows hold `pitch` elements (x < nx
+    used), e.g. pitch = 2 * (nx // 2 + 1), the in-place real-to-complex FFT
+    layout."""
+    h = ctypes.c_void_p()
+    _ok(_lib.tvfgp_create_pitched(int(nx), int(ny), int(nz), int(pitch), ctypes.byref(h)),
+        "tvfgp_create_pitched")
+    return h.value
+
+
+def fft_pitch(nx: int) -> int:
+    """Row pitch of an in-place real-to-complex FFT of length nx: 2*(nx/2+1)."""
+    return 2 * (int(nx) // 2 + 1)
 
 
 def tvfgp_destroy(h: int) -> None:
@@ -296,13 +312,21 @@ def raw_call(name: str, *args) -> int:
 
 
 class Tvfgp:
-    """Owns one handle.  Tensors: b (nz, ny, nx), p and r (3, nz, ny, nx)."""
+    """Owns one handle.  Tensors: b (nz, ny, nx), p and r (3, nz, ny, nx); with
+    a row pitch, b (nz, ny, pitch) and p, r (3, nz, ny, pitch), of which only
+    x < nx is read or written."""
 
     def __init__(self, nx: int, ny: int, nz: int, variant: int | str = TVFGP_VARIANT_AUTO,
-                 graph: bool = False):
+                 graph: bool = False, pitch: int | None = None):
         self.shape = (int(nx), int(ny), int(nz))
-        self.n = int(nx) * int(ny) * int(nz)
-        self.h = tvfgp_create(nx, ny, nz, variant)
+        self.pitch = int(nx) if pitch is None else int(pitch)
+        self.n = self.pitch * int(ny) * int(nz)
+        if pitch is None:
+            self.h = tvfgp_create(nx, ny, nz, variant)
+        else:
+            self.h = tvfgp_create_pitched(nx, ny, nz, pitch)
+            if variant not in (TVFGP_VARIANT_AUTO, "auto"):
+                tvfgp_set_variant(self.h, variant)
         if graph:
             tvfgp_set_graph(self.h, True)
 

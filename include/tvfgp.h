@@ -103,6 +103,19 @@ enum tvfgp_variant {
  * TVFGP_ERR_ARG.  *out receives the handle (NULL on failure). */
 int tvfgp_create(int nx, int ny, int nz, tvfgp_t *out);
 
+/* A handle for volumes whose rows are padded: element (x, y, z) of b, of z
+ * and of each component of p and r sits at x + pitch*(y + ny*z), and every
+ * volume holds pitch*ny*nz elements (a dual field 3*pitch*ny*nz, component
+ * a at a*pitch*ny*nz).  pitch = 2*(nx/2 + 1) is the layout of an in-place
+ * real-to-complex FFT, the padded volumes of the page's solver ("Profiler
+ * counters": a 256³ volume takes 64.5 MiB).  The calls read and write only
+ * x < nx; the padding is never touched.  nx <= pitch <= 65535, else
+ * TVFGP_ERR_ARG.  Padded rows are in general not 16-byte aligned, so every
+ * call on such a handle runs the scalar kernels (last_variant reports
+ * SCALAR), whatever variant is set.  The scratch dual is 3*pitch*ny*nz
+ * floats.  tvfgp_run_noalloc has no pitched form. */
+int tvfgp_create_pitched(int nx, int ny, int nz, int pitch, tvfgp_t *out);
+
 /* As tvfgp_create, choosing the kernel variant (enum tvfgp_variant).  flags
  * must be 0. */
 int tvfgp_create_ex(int nx, int ny, int nz, int variant, unsigned flags, tvfgp_t *out);

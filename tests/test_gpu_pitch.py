@@ -1,0 +1,164 @@
+"""Volumes with padded rows (tvfgp_create_pitched), such as the in-place
+real-to-complex FFT layout with rows of 2*(nx/2+1) floats.  The padding is
+filled with garbage; on x < nx the results must equal the oracle's on the
+dense volume bit for bit, and the padding must come back untouched."""
+import numpy as np
+import pytest
+
+import oracle
+from fgp_dual_stencil_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def T():
+    import torch
+    assert torch.cuda.is_available()
+    from fgp_dual_stencil_gb300 import tvfgp
+    return tvfgp
+
+
+def pad(a, pitch, seed):
+    """a (..., nx) -> (..., pitch) with pseudo-random values in x >= nx."""
+    out = np.random.default_rng(seed).uniform(-7, 7, a.shape[:-1] + (pitch,)).astype(a.dtype)
+    out[..., :a.shape[-1]] = a
+    return out
+
+
+def dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def check(got, want, padded_before, nx, what):
+    g = got.detach().cpu().numpy()
+    assert np.array_equal(g[..., :nx], want), "%s differs from the oracle" % what
+    assert np.array_equal(g[..., nx:], padded_before[..., nx:]), "%s: padding was written" % what
+
+
+CASES = [((32, 8, 6), None), ((33, 5, 7), None), ((64, 17, 9), None), ((130, 9, 11), None),
+         ((7, 3, 2), None), ((40, 6, 5), 45), ((1, 1, 1), 2)]
+
+
+@pytest.mark.parametrize("graph", [False, True])
+@pytest.mark.parametrize("shape,pitch", CASES)
+def test_pitched_equals_dense_oracle(T, shape, pitch, graph):
+    nx, ny, nz = shape
+    pitch = pitch or T.fft_pitch(nx)
+    b = synth.random_case(shape, 61)
+    p0 = synth.random_dual(shape, 62, scale=0.4)
+    r0 = synth.random_dual(shape, 63, scale=0.6)
+    bp, pp, rp = pad(b, pitch, 1), pad(p0, pitch, 2), pad(r0, pitch, 3)
+    zp = pad(np.zeros_like(b), pitch, 4)
+    for nsteps in (0, 1, 2, 5):
+        p, r, z = dev(pp), dev(rp), dev(zp)
+        with T.Tvfgp(nx, ny, nz, "auto", graph, pitch=pitch) as h:
+            h.run(dev(bp), p, r, 0.07, nsteps, 1.0)
+            h.primal(dev(bp), p, 0.07, z=z)
+            assert h.last_variant == T.TVFGP_VARIANT_SCALAR or nsteps == 0
+            assert h.check() == 0
+        po, ro = p0.copy(), r0.copy()
+        oracle.fgp_run(b, po, ro, 0.07, nsteps, 1.0)
+        check(p, po, pp, nx, "p")
+        check(r, ro, rp, nx, "r")
+        check(z, oracle.primal(b, po, 0.07), zp, nx, "z")
+
+
+@pytest.mark.parametrize("variant", ["separate", "zmarch2", "fused"])
+def test_pitched_any_variant_runs_scalar(T, variant):
+    """Every variant set on a pitched handle runs the scalar kernels (the two-
+    kernel variant its scalar pair), with the same bits."""
+    shape = (48, 11, 9)
+    nx, ny, nz = shape
+    pitch = T.fft_pitch(nx)
+    b = synth.random_case(shape, 71)
+    p0 = synth.random_dual(shape, 72, scale=0.4)
+    r0 = synth.random_dual(shape, 73, scale=0.6)
+    bp, pp, rp = pad(b, pitch, 5), pad(p0, pitch, 6), pad(r0, pitch, 7)
+    p, r = dev(pp), dev(rp)
+    with T.Tvfgp(nx, ny, nz, variant, False, pitch=pitch) as h:
+        h.run(dev(bp), p, r, 0.05, 6, 1.0)
+        want = T.TVFGP_VARIANT_SEPARATE if variant == "separate" else T.TVFGP_VARIANT_SCALAR
+        assert h.last_variant == want
+        assert h.check() == 0
+    oracle.fgp_run(b, p0, r0, 0.05, 6, 1.0)
+    check(p, p0, pp, nx, "p")
+    check(r, r0, rp, nx, "r")
+
+
+def test_pitched_binary16(T):
+    import torch
+    shape = (62, 7, 5)
+    nx, ny, nz = shape
+    pitch = T.fft_pitch(nx)
+    b = synth.random_case(shape, 81)
+    p0 = oracle.float_to_half(synth.random_dual(shape, 82, scale=0.4))
+    r0 = oracle.float_to_half(synth.random_dual(shape, 83, scale=0.6))
+    bp = pad(b, pitch, 8)
+    pp = pad(p0.view(np.float16), pitch, 9)
+    rp = pad(r0.view(np.float16), pitch, 10)
+    p, r = dev(pp), dev(rp)
+    z = torch.zeros((nz, ny, pitch), device="cuda")
+    with T.Tvfgp(nx, ny, nz, pitch=pitch) as h:
+        h.run_f16(dev(bp), p, r, 0.05, 5, 1.0)
+        h.primal_f16(dev(bp), p, 0.05, z=z)
+        assert h.last_variant == T.TVFGP_VARIANT_SCALAR
+        assert h.check() == 0
+    ph, rh = p0.copy(), r0.copy()
+    oracle.fgp_run_h16(b, ph, rh, 0.05, 5, 1.0)
+    check(p, ph.view(np.float16), pp, nx, "p (binary16)")
+    check(r, rh.view(np.float16), rp, nx, "r (binary16)")
+    assert np.array_equal(z.cpu().numpy()[..., :nx], oracle.primal_h16(b, ph, 0.05))
+
+
+def test_pitched_workload_128(T):
+    """The 128^3 workload (50 steps) in the FFT layout, pitch 130."""
+    w = synth.WORKLOADS["c2"]
+    b = synth.make_b(w, 0)
+    pitch = T.fft_pitch(w.nx)
+    shape = (3, w.nz, w.ny, w.nx)
+    bp = pad(b, pitch, 11)
+    pp = pad(np.zeros(shape, np.float32), pitch, 12)
+    rp = pad(np.zeros(shape, np.float32), pitch, 13)
+    p, r = dev(pp), dev(rp)
+    with T.Tvfgp(w.nx, w.ny, w.nz, "auto", True, pitch=pitch) as h:
+        h.run(dev(bp), p, r, w.lam, w.steps, w.t0)
+        assert h.check() == 0
+    po = np.zeros(shape, np.float32)
+    ro = np.zeros_like(po)
+    oracle.fgp_run(b, po, ro, w.lam, w.steps, w.t0)
+    check(p, po, pp, w.nx, "p")
+    check(r, ro, rp, w.nx, "r")
+
+
+@pytest.mark.slow
+def test_pitched_512_cubed(T):
+    """512^3 with rows of 514 floats (the bench's --pitch fft configuration),
+    the first 2 of the workload's 20 outers, against the dense oracle."""
+    w = synth.WORKLOADS["c4"]
+    base = synth.phantom(w)
+    pitch = T.fft_pitch(w.nx)
+    shape = (3, w.nz, w.ny, w.nx)
+    po = np.zeros(shape, np.float32)
+    ro = np.zeros_like(po)
+    import torch
+    p = torch.zeros((3, w.nz, w.ny, pitch), device="cuda")
+    r = torch.zeros_like(p)
+    with T.Tvfgp(w.nx, w.ny, w.nz, "auto", True, pitch=pitch) as h:
+        for k in range(2):
+            b = synth.make_b(w, k, base)
+            h.run(dev(pad(b, pitch, 20 + k)), p, r, w.lam, w.steps, w.t0)
+            oracle.fgp_run(b, po, ro, w.lam, w.steps, w.t0)
+        assert h.check() == 0
+    assert np.array_equal(p.cpu().numpy()[..., :w.nx], po)
+    assert np.array_equal(r.cpu().numpy()[..., :w.nx], ro)
+    assert not p[..., w.nx:].any() and not r[..., w.nx:].any()
+
+
+def test_pitch_argument_errors(T):
+    import ctypes
+    h = ctypes.c_void_p()
+    assert T.raw_call("tvfgp_create_pitched", 8, 4, 4, 7, ctypes.byref(h)) == T.TVFGP_ERR_ARG
+    assert T.raw_call("tvfgp_create_pitched", 8, 4, 4, 65536, ctypes.byref(h)) == T.TVFGP_ERR_ARG
+    assert T.raw_call("tvfgp_create_pitched", 8, 4, 4, 10, None) == T.TVFGP_ERR_ARG
