@@ -332,6 +332,8 @@ def gpu_arm(args, world, rank, local_rank, dist):
              T.TVFGP_VARIANT_CUBE_TMA: "fgp_step_cube_tma"}.get(variant_used, "?")
     if f16:
         kname += "<__half>"
+    if pitch != w.nx and variant_used == T.TVFGP_VARIANT_FUSED:
+        kname = "fgp_step_fused4 (quads as two float2)" if w.nx % 4 == 0 else "fgp_step_fused2"
     traffic = ncu_traffic(kname, N)             # DRAM bytes per launch (ncu), or None
 
     # end to end: every step's b copied in from pinned host memory and its z

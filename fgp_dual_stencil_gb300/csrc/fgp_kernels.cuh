@@ -270,6 +270,39 @@ __device__ __forceinline__ float4 f4zero()
 {
     return make_float4(0.f, 0.f, 0.f, 0.f);
 }
+__device__ __forceinline__ float2 ld_ro2(const float *p) { return __ldg(reinterpret_cast<const float2 *>(p)); }
+__device__ __forceinline__ float2 ld_once2(const float *p) { return __ldcs(reinterpret_cast<const float2 *>(p)); }
+__device__ __forceinline__ void st2(float *p, float2 v) { *reinterpret_cast<float2 *>(p) = v; }
+__device__ __forceinline__ float2 f2zero() { return make_float2(0.f, 0.f); }
+
+// A quad of four x values moved as one 16-byte access (VW = 4) or as two
+// 8-byte halves (VW = 2: rows padded to a pitch that is even but not a
+// multiple of four, where a quad is only 8-byte aligned).
+template <int VW>
+__device__ __forceinline__ float4 ldq_ro(const float *p)
+{
+    if (VW == 4) return ld_ro4(p);
+    const float2 a = ld_ro2(p), b = ld_ro2(p + 2);
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+template <int VW>
+__device__ __forceinline__ float4 ldq_once(const float *p)
+{
+    if (VW == 4) return ld_once4(p);
+    const float2 a = ld_once2(p), b = ld_once2(p + 2);
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+template <int VW>
+__device__ __forceinline__ void stq(float *p, float4 v)
+{
+    if (VW == 4) {
+        st4(p, v);
+    } else {
+        st2(p, make_float2(v.x, v.y));
+        st2(p + 2, make_float2(v.z, v.w));
+    }
+}
+
 
 // Four consecutive values of a dual component, widened to float4, and back.
 __device__ __forceinline__ float4 ldv_ro(const float *p) { return ld_ro4(p); }
@@ -298,6 +331,27 @@ __device__ __forceinline__ void stv(__half *p, float4 v)
 __device__ __forceinline__ float ld1_ro(const __half *p) { return __half2float(__ldg(p)); }
 __device__ __forceinline__ float ld1_once(const __half *p) { return __half2float(__ldcs(p)); }
 __device__ __forceinline__ void st1(__half *p, float v) { *p = __float2half_rn(v); }
+
+// Dual quads by storage type: binary16 quads are 8 bytes and keep VW = 4.
+template <int VW> __device__ __forceinline__ float4 ldvq_ro(const float *p) { return ldq_ro<VW>(p); }
+template <int VW> __device__ __forceinline__ float4 ldvq_once(const float *p) { return ldq_once<VW>(p); }
+template <int VW> __device__ __forceinline__ void stvq(float *p, float4 v) { stq<VW>(p, v); }
+template <int VW> __device__ __forceinline__ float4 ldvq_ro(const __half *p)
+{
+    static_assert(VW == 4, "binary16 quads are moved whole");
+    return ldv_ro(p);
+}
+template <int VW> __device__ __forceinline__ float4 ldvq_once(const __half *p)
+{
+    static_assert(VW == 4, "binary16 quads are moved whole");
+    return ldv_once(p);
+}
+template <int VW> __device__ __forceinline__ void stvq(__half *p, float4 v)
+{
+    static_assert(VW == 4, "binary16 quads are moved whole");
+    stv(p, v);
+}
+
 
 // z at four consecutive x voxels from their b and r, the r0 of the voxel left
 // of the first one, and r1, r2 of the lower neighbours in y and z.
@@ -332,19 +386,20 @@ __device__ __forceinline__ float4 zquad(float4 B, float4 R0, float4 R1, float4 R
 #ifndef TVFGP_FUSED_MINB
 #define TVFGP_FUSED_MINB 6
 #endif
-template <int BY, int ZC, typename TS = float>
+template <int BY, int ZC, typename TS = float, int VW = 4>
 __global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(const StepArgsT<TS> a)
 {
     const int lane = threadIdx.x;
     const int x0 = (blockIdx.x * 32 + lane) * 4;
     const int y = blockIdx.y * BY + threadIdx.y;
     const int nx = a.nx, ny = a.ny, nz = a.nz;
+    const int px = a.px > 0 ? a.px : nx;         // row pitch
     if (y >= ny) return;                         // whole warp: y is warp-uniform
     const int zb = blockIdx.z * ZC;
     const int ze = min(zb + ZC, nz);
     const bool xin = x0 < nx;
     const bool hasY = (y + 1 < ny);              // warp-uniform
-    const int sz = nx * ny;
+    const int sz = px * ny;
     const float lam = a.lam, s = a.s, m = a.m;
 
     const float *__restrict__ b = a.b;
@@ -359,19 +414,19 @@ __global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(con
     TS *__restrict__ o2 = a.rd + 2 * a.N;
 
     int z = zb;
-    int i = x0 + nx * (y + ny * z);
+    int i = x0 + px * (y + ny * z);
 
     // prologue: own r at plane zb and z(i) there
     float4 R0c = f4zero(), R1c = f4zero(), R2c = f4zero(), Zc;
     {
         float4 Bc = f4zero(), R1lo = f4zero(), R2lo = f4zero();
         if (xin) {
-            Bc = ld_ro4(b + i);
-            R0c = ldv_ro(r0 + i);
-            R1c = ldv_ro(r1 + i);
-            R2c = ldv_ro(r2 + i);
-            if (y > 0) R1lo = ldv_ro(r1 + i - nx);
-            if (z > 0) R2lo = ldv_ro(r2 + i - sz);
+            Bc = ldq_ro<VW>(b + i);
+            R0c = ldvq_ro<VW>(r0 + i);
+            R1c = ldvq_ro<VW>(r1 + i);
+            R2c = ldvq_ro<VW>(r2 + i);
+            if (y > 0) R1lo = ldvq_ro<VW>(r1 + i - px);
+            if (z > 0) R2lo = ldvq_ro<VW>(r2 + i - sz);
         }
         float left = __shfl_up_sync(kFull, R0c.w, 1);
         if (lane == 0) left = (x0 > 0) ? ld1_ro(r0 + i - 1) : 0.0f;
@@ -379,7 +434,7 @@ __global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(con
     }
     // r2 of row y+1 one plane below (the z-lower neighbour of z(i+ey))
     float4 R2yp = f4zero();
-    if (xin && hasY && z > 0) R2yp = ldv_ro(r2 + i + nx - sz);
+    if (xin && hasY && z > 0) R2yp = ldvq_ro<VW>(r2 + i + px - sz);
 
     for (; z < ze; ++z, i += sz) {
         const bool hasZ = (z + 1 < nz);          // block-uniform
@@ -387,33 +442,33 @@ __global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(con
         // (1) the voxel's own p, first
         float4 P0 = f4zero(), P1 = f4zero(), P2 = f4zero();
         if (xin) {
-            P0 = ldv_once(p0 + i);
-            P1 = ldv_once(p1 + i);
-            P2 = ldv_once(p2 + i);
+            P0 = ldvq_once<VW>(p0 + i);
+            P1 = ldvq_once<VW>(p1 + i);
+            P2 = ldvq_once<VW>(p2 + i);
         }
         // (2) the next plane's own b, r (and r1 of its y-lower row)
         float4 Bn = f4zero(), R0n = f4zero(), R1n = f4zero(), R2n = f4zero(), R1lon = f4zero();
         if (xin && hasZ) {
-            Bn = ld_ro4(b + i + sz);
-            R0n = ldv_ro(r0 + i + sz);
-            R1n = ldv_ro(r1 + i + sz);
-            R2n = ldv_ro(r2 + i + sz);
-            if (y > 0) R1lon = ldv_ro(r1 + i + sz - nx);
+            Bn = ldq_ro<VW>(b + i + sz);
+            R0n = ldvq_ro<VW>(r0 + i + sz);
+            R1n = ldvq_ro<VW>(r1 + i + sz);
+            R2n = ldvq_ro<VW>(r2 + i + sz);
+            if (y > 0) R1lon = ldvq_ro<VW>(r1 + i + sz - px);
         }
         // (3) row y+1 of this plane
         float4 By = f4zero(), R0y = f4zero(), R1y = f4zero(), R2y = f4zero();
         if (xin && hasY) {
-            By = ld_ro4(b + i + nx);
-            R0y = ldv_ro(r0 + i + nx);
-            R1y = ldv_ro(r1 + i + nx);
-            R2y = ldv_ro(r2 + i + nx);
+            By = ldq_ro<VW>(b + i + px);
+            R0y = ldvq_ro<VW>(r0 + i + px);
+            R1y = ldvq_ro<VW>(r1 + i + px);
+            R2y = ldvq_ro<VW>(r2 + i + px);
         }
 
         // z(i+ey)
         float4 ZY = f4zero();
         if (hasY) {
             float left = __shfl_up_sync(kFull, R0y.w, 1);
-            if (lane == 0) left = (x0 > 0) ? ld1_ro(r0 + i + nx - 1) : 0.0f;
+            if (lane == 0) left = (x0 > 0) ? ld1_ro(r0 + i + px - 1) : 0.0f;
             ZY = zquad(By, R0y, R1y, R2y, left, R1c, R2yp, lam);
         }
         // z(i+ez)
@@ -428,7 +483,7 @@ __global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(con
         if (lane == 31 && x0 + 4 < nx) {
             const int j = i + 4;
             const float d0 = __fsub_rn(ld1_ro(r0 + j), R0c.w);
-            const float d1 = __fsub_rn(ld1_ro(r1 + j), y > 0 ? ld1_ro(r1 + j - nx) : 0.0f);
+            const float d1 = __fsub_rn(ld1_ro(r1 + j), y > 0 ? ld1_ro(r1 + j - px) : 0.0f);
             const float d2 = __fsub_rn(ld1_ro(r2 + j), z > 0 ? ld1_ro(r2 + j - sz) : 0.0f);
             zx = zval(__ldg(b + j), lam, d0, d1, d2);
         }
@@ -449,12 +504,12 @@ __global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(con
             dual_update(N0.y, N1.y, N2.y, __fsub_rn(Zc.y, Zc.z), G1.y, G2.y, P0.y, P1.y, P2.y, s, m);
             dual_update(N0.z, N1.z, N2.z, __fsub_rn(Zc.z, Zc.w), G1.z, G2.z, P0.z, P1.z, P2.z, s, m);
             dual_update(N0.w, N1.w, N2.w, gx3, G1.w, G2.w, P0.w, P1.w, P2.w, s, m);
-            stv(p0 + i, P0);
-            stv(p1 + i, P1);
-            stv(p2 + i, P2);
-            stv(o0 + i, N0);
-            stv(o1 + i, N1);
-            stv(o2 + i, N2);
+            stvq<VW>(p0 + i, P0);
+            stvq<VW>(p1 + i, P1);
+            stvq<VW>(p2 + i, P2);
+            stvq<VW>(o0 + i, N0);
+            stvq<VW>(o1 + i, N1);
+            stvq<VW>(o2 + i, N2);
         }
 
         R0c = R0n;
@@ -462,6 +517,167 @@ __global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(con
         R2c = R2n;
         Zc = ZZ;
         R2yp = R2y;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// FUSED2: the fused kernel's plan on pairs of x voxels (float2), for volumes
+// whose rows are padded to an even pitch that is not a multiple of four
+// floats (the in-place real-to-complex FFT layout: rows of nx+2 floats)
+// ---------------------------------------------------------------------------
+//
+// A warp is 32 consecutive x-pairs (64 voxels) of one row; z(i+ex) of the
+// pair's second voxel is the next lane's first z (lane 31 computes it);
+// z(i+ey) and z(i+ez) are recomputed from row y+1 and from the next plane,
+// whose own data is the prefetch of the next iteration.  Requirements: nx
+// and the pitch even, every pointer 8-byte aligned.
+
+// z of a pair of x voxels, in the canonical order
+__device__ __forceinline__ float2 zpair(float2 B, float2 R0, float2 R1, float2 R2, float r0left, float2 R1lo,
+                                        float2 R2lo, float lam)
+{
+    float2 z;
+    z.x = zval(B.x, lam, __fsub_rn(R0.x, r0left), __fsub_rn(R1.x, R1lo.x), __fsub_rn(R2.x, R2lo.x));
+    z.y = zval(B.y, lam, __fsub_rn(R0.y, R0.x), __fsub_rn(R1.y, R1lo.y), __fsub_rn(R2.y, R2lo.y));
+    return z;
+}
+
+template <int BY, int ZC>
+__global__ void __launch_bounds__(32 * BY) fgp_step_fused2(const StepArgs a)
+{
+    const int lane = threadIdx.x;
+    const int x0 = (blockIdx.x * 32 + lane) * 2;
+    const int y = blockIdx.y * BY + threadIdx.y;
+    const int nx = a.nx, ny = a.ny, nz = a.nz;
+    const int px = a.px > 0 ? a.px : nx;         // row pitch
+    if (y >= ny) return;                         // whole warp: y is warp-uniform
+    const int zb = blockIdx.z * ZC;
+    const int ze = min(zb + ZC, nz);
+    const bool xin = x0 < nx;
+    const bool hasY = (y + 1 < ny);
+    const long long sz = (long long)px * ny;
+    const float lam = a.lam, s = a.s, m = a.m;
+
+    const float *__restrict__ b = a.b;
+    const float *__restrict__ r0 = a.rs;
+    const float *__restrict__ r1 = a.rs + a.N;
+    const float *__restrict__ r2 = a.rs + 2 * a.N;
+    float *__restrict__ p0 = a.p;
+    float *__restrict__ p1 = a.p + a.N;
+    float *__restrict__ p2 = a.p + 2 * a.N;
+    float *__restrict__ o0 = a.rd;
+    float *__restrict__ o1 = a.rd + a.N;
+    float *__restrict__ o2 = a.rd + 2 * a.N;
+
+    int z = zb;
+    long long i = x0 + (long long)px * y + sz * z;
+
+    // prologue: own r at plane zb and z(i) there
+    float2 R0c = f2zero(), R1c = f2zero(), R2c = f2zero(), Zc;
+    {
+        float2 Bc = f2zero(), R1lo = f2zero(), R2lo = f2zero();
+        if (xin) {
+            Bc = ld_ro2(b + i);
+            R0c = ld_ro2(r0 + i);
+            R1c = ld_ro2(r1 + i);
+            R2c = ld_ro2(r2 + i);
+            if (y > 0) R1lo = ld_ro2(r1 + i - px);
+            if (z > 0) R2lo = ld_ro2(r2 + i - sz);
+        }
+        float left = __shfl_up_sync(kFull, R0c.y, 1);
+        if (lane == 0) left = (x0 > 0) ? __ldg(r0 + i - 1) : 0.0f;
+        Zc = zpair(Bc, R0c, R1c, R2c, left, R1lo, R2lo, lam);
+    }
+    float2 R2yp = f2zero();                      // r2 of row y+1 one plane below
+    if (xin && hasY && z > 0) R2yp = ld_ro2(r2 + i + px - sz);
+
+    for (; z < ze; ++z, i += sz) {
+        const bool hasZ = (z + 1 < nz);
+        // the voxel's own p, first
+        float2 P0 = f2zero(), P1 = f2zero(), P2 = f2zero();
+        if (xin) {
+            P0 = ld_once2(p0 + i);
+            P1 = ld_once2(p1 + i);
+            P2 = ld_once2(p2 + i);
+        }
+        // the next plane's own b, r (and r1 of its y-lower row)
+        float2 Bn = f2zero(), R0n = f2zero(), R1n = f2zero(), R2n = f2zero(), R1lon = f2zero();
+        if (xin && hasZ) {
+            Bn = ld_ro2(b + i + sz);
+            R0n = ld_ro2(r0 + i + sz);
+            R1n = ld_ro2(r1 + i + sz);
+            R2n = ld_ro2(r2 + i + sz);
+            if (y > 0) R1lon = ld_ro2(r1 + i + sz - px);
+        }
+        // row y+1 of this plane
+        float2 By = f2zero(), R0y = f2zero(), R1y = f2zero(), R2y = f2zero();
+        if (xin && hasY) {
+            By = ld_ro2(b + i + px);
+            R0y = ld_ro2(r0 + i + px);
+            R1y = ld_ro2(r1 + i + px);
+            R2y = ld_ro2(r2 + i + px);
+        }
+        float2 ZY = f2zero();
+        if (hasY) {
+            float left = __shfl_up_sync(kFull, R0y.y, 1);
+            if (lane == 0) left = (x0 > 0) ? __ldg(r0 + i + px - 1) : 0.0f;
+            ZY = zpair(By, R0y, R1y, R2y, left, R1c, R2yp, lam);
+        }
+        float2 ZZ = f2zero();
+        if (hasZ) {
+            float left = __shfl_up_sync(kFull, R0n.y, 1);
+            if (lane == 0) left = (x0 > 0) ? __ldg(r0 + i + sz - 1) : 0.0f;
+            ZZ = zpair(Bn, R0n, R1n, R2n, left, R1lon, R2c, lam);
+        }
+        // z(i+ex) of the second voxel: the next lane's first z
+        float zx = __shfl_down_sync(kFull, Zc.x, 1);
+        if (lane == 31 && x0 + 2 < nx) {
+            const long long j = i + 2;
+            const float d0 = __fsub_rn(__ldg(r0 + j), R0c.y);
+            const float d1 = __fsub_rn(__ldg(r1 + j), y > 0 ? __ldg(r1 + j - px) : 0.0f);
+            const float d2 = __fsub_rn(__ldg(r2 + j), z > 0 ? __ldg(r2 + j - sz) : 0.0f);
+            zx = zval(__ldg(b + j), lam, d0, d1, d2);
+        }
+        if (xin) {
+            const float gx1 = (x0 + 1 < nx - 1) ? __fsub_rn(Zc.y, zx) : 0.0f;
+            const float g1x = hasY ? __fsub_rn(Zc.x, ZY.x) : 0.0f, g1y = hasY ? __fsub_rn(Zc.y, ZY.y) : 0.0f;
+            const float g2x = hasZ ? __fsub_rn(Zc.x, ZZ.x) : 0.0f, g2y = hasZ ? __fsub_rn(Zc.y, ZZ.y) : 0.0f;
+            float2 N0 = R0c, N1 = R1c, N2 = R2c;
+            dual_update(N0.x, N1.x, N2.x, __fsub_rn(Zc.x, Zc.y), g1x, g2x, P0.x, P1.x, P2.x, s, m);
+            dual_update(N0.y, N1.y, N2.y, gx1, g1y, g2y, P0.y, P1.y, P2.y, s, m);
+            st2(p0 + i, P0);
+            st2(p1 + i, P1);
+            st2(p2 + i, P2);
+            st2(o0 + i, N0);
+            st2(o1 + i, N1);
+            st2(o2 + i, N2);
+        }
+        R0c = R0n;
+        R1c = R1n;
+        R2c = R2n;
+        Zc = ZZ;
+        R2yp = R2y;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// rows between a padded and a dense layout
+// ---------------------------------------------------------------------------
+//
+// One block per row: copies the row's nx floats (nx % 4 == 0) from src, row
+// pitch spitch, to dst, row pitch dpitch, as 8-byte halves of quads (both
+// pitches even, both buffers 8-byte aligned); x >= nx is never touched.
+__global__ void __launch_bounds__(128) repack_rows(float *__restrict__ dst, int dpitch,
+                                                   const float *__restrict__ src, int spitch, int nx)
+{
+    const long long row = blockIdx.x;
+    const float *s = src + row * spitch;
+    float *d = dst + row * dpitch;
+    for (int x = 4 * threadIdx.x; x < nx; x += 4 * blockDim.x) {
+        const float2 lo = __ldcs(reinterpret_cast<const float2 *>(s + x));
+        const float2 hi = __ldcs(reinterpret_cast<const float2 *>(s + x + 2));
+        st2(d + x, lo);
+        st2(d + x + 2, hi);
     }
 }
 

@@ -112,6 +112,10 @@ struct tvfgp_handle {
     Zmarch2Plan z2plan;
     GraphEntry graphs[kGraphSlots];
     unsigned long long graph_clock;
+    // runs on padded rows: a dense handle of the same volume and its
+    // staging buffers (b, p, r: 7*nx*ny*nz floats), made on first use
+    tvfgp_handle *shadow;
+    float *pk;
 };
 
 namespace {
@@ -132,9 +136,13 @@ int check_ptr(const void *p)
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned8(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
 
 // Rows stored without padding: the vector and TMA kernels need it.
 bool dense(const tvfgp_handle *h) { return h->px == h->nx; }
+
+// Padded rows the float2 kernel can take: nx and the pitch even.
+bool pair_rows(const tvfgp_handle *h) { return !dense(h) && h->nx % 2 == 0 && h->px % 2 == 0; }
 
 // The copy of a whole dual field (3 components) with elements of es bytes:
 // contiguous, or only the x < nx part of every padded row.
@@ -169,9 +177,43 @@ int check_lambda(float lam)
 // s = 1/(12 lambda), evaluated in double and rounded once to float.
 float step_of(float lam) { return static_cast<float>(1.0 / (12.0 * static_cast<double>(lam))); }
 
-int resolve_variant(const tvfgp_handle *h, int requested, bool vec_ok)
+// Kernels that are halves of a step of the two-kernel variant.
+constexpr int kKernPrimalZVec = 100;     // z = primal of r_src into the handle's z buffer
+constexpr int kKernPrimalZScalar = 101;
+constexpr int kKernDualZVec = 102;       // the rest of the step, reading that z
+constexpr int kKernDualZScalar = 103;
+// One-step kernels on a dual stored as binary16.
+constexpr int kKernFusedH = 120;
+constexpr int kKernScalarH = 121;
+constexpr int kKernZmarchH = 122;
+// The fused kernel on padded rows (even pitch): on quads moved as two 8-byte
+// halves when nx % 4 == 0, on pairs of voxels otherwise.
+constexpr int kKernFused2 = 130;
+constexpr int kKernFusedP = 131;
+constexpr int kFused2BY = 4, kFused2ZC = 8;
+
+// The public variant a kernel belongs to (what tvfgp_last_variant reports).
+int public_variant(int kernel)
+{
+    if (kernel == kKernFused2 || kernel == kKernFusedP || kernel == kKernFusedH) return TVFGP_VARIANT_FUSED;
+    if (kernel == kKernScalarH) return TVFGP_VARIANT_SCALAR;
+    if (kernel == kKernZmarchH) return TVFGP_VARIANT_ZMARCH_TMA;
+    if (kernel >= kKernPrimalZVec && kernel <= kKernDualZScalar) return TVFGP_VARIANT_SEPARATE;
+    return kernel;
+}
+
+// vec_ok: dense rows, nx % 4 == 0 and 16-byte aligned pointers (the float4
+// and TMA kernels).  On padded rows every vector variant becomes the float2
+// fused kernel when pair_ok (nx and the pitch even, 8-byte aligned pointers),
+// else the scalar one; SCALAR and SEPARATE stay.
+int resolve_variant(const tvfgp_handle *h, int requested, bool vec_ok, bool pair_ok = false)
 {
     int v = requested == TVFGP_VARIANT_AUTO ? kAutoVariant : requested;
+    if (!dense(h)) {
+        if (v == TVFGP_VARIANT_SCALAR || v == TVFGP_VARIANT_SEPARATE) return v;
+        if (!pair_ok) return TVFGP_VARIANT_SCALAR;
+        return h->nx % 4 == 0 ? kKernFusedP : kKernFused2;
+    }
     if (v == TVFGP_VARIANT_FUSED || v == TVFGP_VARIANT_ZMARCH_TMA || v == TVFGP_VARIANT_ZMARCH2_TMA ||
         v == TVFGP_VARIANT_CUBE_TMA) {
         if (!vec_ok) return TVFGP_VARIANT_SCALAR;
@@ -225,15 +267,6 @@ LaunchCfg step_cfg(const tvfgp_handle *h, int variant)
     return c;
 }
 
-// Kernels that are halves of a step of the two-kernel variant.
-constexpr int kKernPrimalZVec = 100;     // z = primal of r_src into the handle's z buffer
-constexpr int kKernPrimalZScalar = 101;
-constexpr int kKernDualZVec = 102;       // the rest of the step, reading that z
-constexpr int kKernDualZScalar = 103;
-// One-step kernels on a dual stored as binary16.
-constexpr int kKernFusedH = 120;
-constexpr int kKernScalarH = 121;
-constexpr int kKernZmarchH = 122;
 
 // One kernel launch of a run: a single step (p updated in place, r_src ->
 // r_dst), a two-step launch (p_src -> p_dst and r_src -> r_dst), or a half
@@ -270,6 +303,20 @@ LaunchCfg item_cfg(const tvfgp_handle *h, int kernel)
     if (kernel == kKernScalarH) {
         LaunchCfg c = step_cfg(h, TVFGP_VARIANT_SCALAR);
         c.func = reinterpret_cast<const void *>(&fgp_step_scalar<__half>);
+        return c;
+    }
+    if (kernel == kKernFusedP) {
+        LaunchCfg c = step_cfg(h, TVFGP_VARIANT_FUSED);
+        c.func = reinterpret_cast<const void *>(&fgp_step_fused4<kFusedBY, kFusedZC, float, 2>);
+        return c;
+    }
+    if (kernel == kKernFused2) {
+        LaunchCfg c;
+        c.smem = 0;
+        c.func = reinterpret_cast<const void *>(&fgp_step_fused2<kFused2BY, kFused2ZC>);
+        c.block = dim3(32, kFused2BY, 1);
+        c.grid = dim3((h->nx / 2 + 31) / 32, (h->ny + kFused2BY - 1) / kFused2BY,
+                      (h->nz + kFused2ZC - 1) / kFused2ZC);
         return c;
     }
     if (kernel == kKernZmarchH) {
@@ -440,7 +487,7 @@ int launch_item(tvfgp_handle *h, const Item &it, const float *b, float lam, cuda
         return from_cuda(e);
     }
     h->launches += 1;
-    h->last_variant = it.kernel;
+    h->last_variant = public_variant(it.kernel);
     return TVFGP_OK;
 }
 
@@ -576,7 +623,7 @@ int run_graph(tvfgp_handle *h, int variant, const float *b, float *p, float *r, 
         return from_cuda(e);
     }
     h->launches += static_cast<long long>(items.size());
-    h->last_variant = items.empty() ? variant : items.front().kernel;
+    h->last_variant = public_variant(items.empty() ? variant : items.front().kernel);
     return TVFGP_OK;
 }
 
@@ -605,6 +652,47 @@ int ensure_pair_scratch(tvfgp_handle *h)
         return from_cuda(e);
     }
     return TVFGP_OK;
+}
+
+// Runs on padded rows with at least this many steps are packed into dense
+// buffers, run by the dense kernels and unpacked (see tvfgp_run).
+constexpr int kPackMinSteps = 4;
+
+int ensure_shadow(tvfgp_handle *h)
+{
+    if (h->shadow) return TVFGP_OK;
+    const size_t n = static_cast<size_t>(h->nx) * h->ny * h->nz;
+    cudaError_t e = cudaMalloc(&h->pk, sizeof(float) * 7 * n);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        h->pk = nullptr;
+        return from_cuda(e);
+    }
+    tvfgp_t s = nullptr;
+    const int rc = tvfgp_create_ex(h->nx, h->ny, h->nz, TVFGP_VARIANT_AUTO, 0u, &s);
+    if (rc != TVFGP_OK) {
+        cudaFree(h->pk);
+        h->pk = nullptr;
+        return rc;
+    }
+    h->shadow = s;
+    return TVFGP_OK;
+}
+
+// `rows` rows of nx floats between a padded buffer (pitch px) and a dense
+// one: a kernel when nx % 4 == 0 and the pitch is even (8-byte halves of
+// quads), else a 2D copy.
+cudaError_t repack(tvfgp_handle *h, float *dst, const float *src, size_t rows, bool to_dense, cudaStream_t st)
+{
+    const int dp = to_dense ? h->nx : h->px, sp = to_dense ? h->px : h->nx;
+    if (h->nx % 4 == 0 && h->px % 2 == 0 && aligned8(dst) && aligned8(src) && rows <= 0x7fffffffULL) {
+        repack_rows<<<static_cast<unsigned>(rows), 128, 0, st>>>(dst, dp, src, sp, h->nx);
+        h->launches += 1;
+        return cudaGetLastError();
+    }
+    const size_t w = sizeof(float) * static_cast<size_t>(h->nx);
+    return cudaMemcpy2DAsync(dst, sizeof(float) * dp, src, sizeof(float) * sp, w, rows, cudaMemcpyDeviceToDevice,
+                             st);
 }
 
 }  // namespace
@@ -670,6 +758,8 @@ static int create_impl(int nx, int ny, int nz, int px, int variant, unsigned fla
     h->pair_scratch = nullptr;
     h->zscratch = nullptr;
     h->d_err = nullptr;
+    h->shadow = nullptr;
+    h->pk = nullptr;
     cudaError_t e = cudaMalloc(&h->scratch, sizeof(float) * 3 * static_cast<size_t>(h->N));
     if (e == cudaSuccess) e = cudaMalloc(&h->d_err, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(int));
@@ -723,6 +813,8 @@ int tvfgp_destroy(tvfgp_t h)
     cudaFree(h->pair_scratch);
     cudaFree(h->zscratch);
     cudaFree(h->d_err);
+    cudaFree(h->pk);
+    if (h->shadow) tvfgp_destroy(h->shadow);
     h->magic = 0;
     delete h;
     return TVFGP_OK;
@@ -777,7 +869,8 @@ int tvfgp_step(tvfgp_t h, const float *b, float *p, const float *r_src, float *r
         return TVFGP_ERR_ARG;
     const bool vec_ok = dense(h) && (h->nx % 4 == 0) && aligned16(b) && aligned16(p) && aligned16(r_src) &&
                         aligned16(r_dst);
-    int variant = resolve_variant(h, h->variant, vec_ok);
+    const bool pair_ok = pair_rows(h) && aligned8(b) && aligned8(p) && aligned8(r_src) && aligned8(r_dst);
+    int variant = resolve_variant(h, h->variant, vec_ok, pair_ok);
     if (variant == TVFGP_VARIANT_ZMARCH2_TMA) variant = TVFGP_VARIANT_ZMARCH_TMA;   // one step only
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (variant == TVFGP_VARIANT_SEPARATE) {
@@ -815,12 +908,46 @@ int tvfgp_run(tvfgp_t h, const float *b, float *p, float *r, float lambda, int n
         if (t_final) *t_final = tf;
         return TVFGP_OK;
     }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // Padded rows defeat the 16-byte accesses of the fastest kernels; a run
+    // long enough is cheaper as pack -> dense run -> unpack (26 volume moves
+    // against 13 per step saved at the dense kernels' speed).  The padding
+    // is never written.
+    const bool packed_variant = h->variant == TVFGP_VARIANT_AUTO || h->variant == TVFGP_VARIANT_ZMARCH_TMA ||
+                                h->variant == TVFGP_VARIANT_ZMARCH2_TMA || h->variant == TVFGP_VARIANT_CUBE_TMA;
+    if (!dense(h) && h->nx % 4 == 0 && nsteps >= kPackMinSteps && packed_variant &&
+        ensure_shadow(h) == TVFGP_OK) {
+        tvfgp_handle *sh = h->shadow;
+        if ((rc = tvfgp_set_variant(sh, h->variant)) || (rc = tvfgp_set_graph(sh, h->graph_on))) return rc;
+        const size_t n = static_cast<size_t>(h->nx) * h->ny * h->nz;
+        const size_t rows = static_cast<size_t>(h->ny) * h->nz;
+        float *db = h->pk, *dp = h->pk + n, *dr = h->pk + 4 * n;
+        cudaError_t e = repack(h, db, b, rows, true, st);
+        if (e == cudaSuccess) e = repack(h, dp, p, 3 * rows, true, st);
+        if (e == cudaSuccess) e = repack(h, dr, r, 3 * rows, true, st);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return from_cuda(e);
+        }
+        const long long before = sh->launches;
+        rc = tvfgp_run(sh, db, dp, dr, lambda, nsteps, t0, stream, t_final);
+        if (rc != TVFGP_OK) return rc;
+        h->launches += sh->launches - before;
+        e = repack(h, p, dp, 3 * rows, false, st);
+        if (e == cudaSuccess) e = repack(h, r, dr, 3 * rows, false, st);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return from_cuda(e);
+        }
+        h->last_variant = sh->last_variant;
+        return TVFGP_OK;
+    }
     const bool vec_ok = dense(h) && (h->nx % 4 == 0) && aligned16(b) && aligned16(p) && aligned16(r);
-    const int variant = resolve_variant(h, h->variant, vec_ok);
+    const bool pair_ok = pair_rows(h) && aligned8(b) && aligned8(p) && aligned8(r);
+    const int variant = resolve_variant(h, h->variant, vec_ok, pair_ok);
     std::vector<Item> items;
     bool copy_back = false;
     plan_run(h, variant, vec_ok, p, r, m, items, &copy_back);
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (h->graph_on) {
         rc = run_graph(h, variant, b, p, r, lambda, nsteps, t0, items, copy_back, dual_copy(h, 4), st);
     } else {
@@ -835,8 +962,7 @@ int tvfgp_run(tvfgp_t h, const float *b, float *p, float *r, float lambda, int n
         }
     }
     if (rc == TVFGP_OK) {
-        h->last_variant = items.front().kernel >= kKernPrimalZVec ? TVFGP_VARIANT_SEPARATE
-                                                                : items.front().kernel;
+        h->last_variant = public_variant(items.front().kernel);
         if (t_final) *t_final = tf;
     }
     return rc;
@@ -995,6 +1121,10 @@ int tvfgp_check(tvfgp_t h, tvfgp_stream_t stream)
     if (e != cudaSuccess) {
         cudaGetLastError();
         return from_cuda(e);
+    }
+    if (h->shadow) {                          // kernels of a packed run report there
+        const int rc = tvfgp_check(h->shadow, stream);
+        if (rc != TVFGP_OK) return rc;
     }
     return flag != 0 ? TVFGP_ERR_TIMEOUT : TVFGP_OK;
 }

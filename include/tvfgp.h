@@ -110,10 +110,20 @@ int tvfgp_create(int nx, int ny, int nz, tvfgp_t *out);
  * real-to-complex FFT, the padded volumes of the page's solver ("Profiler
  * counters": a 256³ volume takes 64.5 MiB).  The calls read and write only
  * x < nx; the padding is never touched.  nx <= pitch <= 65535, else
- * TVFGP_ERR_ARG.  Padded rows are in general not 16-byte aligned, so every
- * call on such a handle runs the scalar kernels (last_variant reports
- * SCALAR), whatever variant is set.  The scratch dual is 3*pitch*ny*nz
- * floats.  tvfgp_run_noalloc has no pitched form. */
+ * TVFGP_ERR_ARG.  Padded rows are in general not 16-byte aligned, so the
+ * float4 and TMA kernels cannot read them in place.  A tvfgp_run of 4 or more
+ * steps on a handle set to AUTO, ZMARCH_TMA, ZMARCH2_TMA or CUBE_TMA with
+ * nx % 4 == 0 therefore packs b, p and r into dense buffers, runs the dense
+ * kernels of that variant on them and unpacks p and r (last_variant reports
+ * the dense variant); the handle then owns a dense handle and 7*nx*ny*nz
+ * more floats, allocated on that first run (if that allocation fails the
+ * run proceeds in place).  Other runs and tvfgp_step work in place: the
+ * fused kernel on 8-byte halves of quads (or on pairs when nx % 4 == 2)
+ * when nx and the pitch are even and b, p and r are 8-byte aligned
+ * (last_variant reports FUSED), else the scalar kernel; SCALAR and SEPARATE
+ * handles keep their scalar kernels.  The primal and the binary16 calls run
+ * their scalar kernels.  The scratch dual is 3*pitch*ny*nz floats.
+ * tvfgp_run_noalloc has no pitched form. */
 int tvfgp_create_pitched(int nx, int ny, int nz, int pitch, tvfgp_t *out);
 
 /* As tvfgp_create, choosing the kernel variant (enum tvfgp_variant).  flags

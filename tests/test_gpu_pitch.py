@@ -31,6 +31,22 @@ def dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
+def pitched_variant(T, nx, pitch, variant="auto", nsteps=1):
+    """What a pitched handle runs.  Runs of 4 or more steps with nx % 4 == 0
+    on AUTO and the TMA variants are packed into dense buffers and run by the
+    dense kernels; otherwise the fused kernel on 8-byte halves or pairs
+    (reported as FUSED) when nx and the pitch are even, else the scalar
+    kernel; SCALAR and SEPARATE handles keep theirs."""
+    if nsteps >= 4 and nx % 4 == 0 and variant in ("auto", "zmarch", "zmarch2", "cube"):
+        return {"auto": T.TVFGP_VARIANT_ZMARCH2_TMA, "zmarch": T.TVFGP_VARIANT_ZMARCH_TMA,
+                "zmarch2": T.TVFGP_VARIANT_ZMARCH2_TMA, "cube": T.TVFGP_VARIANT_CUBE_TMA}[variant]
+    if variant == "separate":
+        return T.TVFGP_VARIANT_SEPARATE
+    if variant == "scalar" or nx % 2 or pitch % 2:
+        return T.TVFGP_VARIANT_SCALAR
+    return T.TVFGP_VARIANT_FUSED
+
+
 def check(got, want, padded_before, nx, what):
     g = got.detach().cpu().numpy()
     assert np.array_equal(g[..., :nx], want), "%s differs from the oracle" % what
@@ -51,12 +67,12 @@ def test_pitched_equals_dense_oracle(T, shape, pitch, graph):
     r0 = synth.random_dual(shape, 63, scale=0.6)
     bp, pp, rp = pad(b, pitch, 1), pad(p0, pitch, 2), pad(r0, pitch, 3)
     zp = pad(np.zeros_like(b), pitch, 4)
-    for nsteps in (0, 1, 2, 5):
+    for nsteps in (0, 1, 2, 5, 6):
         p, r, z = dev(pp), dev(rp), dev(zp)
         with T.Tvfgp(nx, ny, nz, "auto", graph, pitch=pitch) as h:
             h.run(dev(bp), p, r, 0.07, nsteps, 1.0)
             h.primal(dev(bp), p, 0.07, z=z)
-            assert h.last_variant == T.TVFGP_VARIANT_SCALAR or nsteps == 0
+            assert h.last_variant == pitched_variant(T, nx, pitch, "auto", nsteps) or nsteps == 0
             assert h.check() == 0
         po, ro = p0.copy(), r0.copy()
         oracle.fgp_run(b, po, ro, 0.07, nsteps, 1.0)
@@ -65,10 +81,11 @@ def test_pitched_equals_dense_oracle(T, shape, pitch, graph):
         check(z, oracle.primal(b, po, 0.07), zp, nx, "z")
 
 
-@pytest.mark.parametrize("variant", ["separate", "zmarch2", "fused"])
-def test_pitched_any_variant_runs_scalar(T, variant):
-    """Every variant set on a pitched handle runs the scalar kernels (the two-
-    kernel variant its scalar pair), with the same bits."""
+@pytest.mark.parametrize("variant", ["separate", "zmarch2", "zmarch", "fused", "scalar", "cube"])
+def test_pitched_any_variant(T, variant):
+    """Every variant set on a pitched handle runs the float2 fused kernel or a
+    scalar kernel (the two-kernel variant its scalar pair), with the same
+    bits."""
     shape = (48, 11, 9)
     nx, ny, nz = shape
     pitch = T.fft_pitch(nx)
@@ -79,8 +96,7 @@ def test_pitched_any_variant_runs_scalar(T, variant):
     p, r = dev(pp), dev(rp)
     with T.Tvfgp(nx, ny, nz, variant, False, pitch=pitch) as h:
         h.run(dev(bp), p, r, 0.05, 6, 1.0)
-        want = T.TVFGP_VARIANT_SEPARATE if variant == "separate" else T.TVFGP_VARIANT_SCALAR
-        assert h.last_variant == want
+        assert h.last_variant == pitched_variant(T, nx, pitch, variant, 6)
         assert h.check() == 0
     oracle.fgp_run(b, p0, r0, 0.05, 6, 1.0)
     check(p, p0, pp, nx, "p")
