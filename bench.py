@@ -58,6 +58,8 @@ def parse_args():
     ap.add_argument("--pitch", default="dense", choices=["dense", "fft"],
                     help="row layout of every volume: dense, or padded to 2*(nx/2+1) floats "
                          "(in-place real-to-complex FFT layout; runs the scalar kernels)")
+    ap.add_argument("--b-host", default="wc", choices=["wc", "pinned"],
+                    help="page-locked host staging of b for the end-to-end run: write-combined or cached")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -248,7 +250,7 @@ def gpu_arm(args, world, rank, local_rank, dist):
     # host showed copy times varying several-fold from copy to copy)
     b_host = []
     for k in range(n_b):
-        t = T.host_tensor((w.nz, w.ny, pitch), write_combined=True)
+        t = T.host_tensor((w.nz, w.ny, pitch), write_combined=args.b_host == "wc")
         bk = synth.make_b(w, k, base)
         if pitch == w.nx:
             t.numpy()[...] = bk
@@ -346,8 +348,8 @@ def gpu_arm(args, world, rank, local_rank, dist):
                "h2d_bytes_per_step": 4 * w.ny * w.nz * pitch, "d2h_bytes_per_step": 4 * w.ny * w.nz * pitch,
                "ms_per_step": round(e2e_s * 1e3 / K, 4),
                "overlap": "H2D of step j+1 and D2H of step j on two copy streams, double-buffered",
-               "host_memory": "b from write-combined page-locked memory, z to page-locked memory "
-                              "(tvfgp_host_alloc)"}
+               "host_memory": "b from %s page-locked memory, z to page-locked memory (tvfgp_host_alloc)"
+                              % ("write-combined" if args.b_host == "wc" else "cached")}
         if h.check(stream) != T.TVFGP_OK:
             raise RuntimeError("device error word set during the end-to-end run")
 
