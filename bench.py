@@ -60,6 +60,8 @@ def parse_args():
                          "(in-place real-to-complex FFT layout; runs the scalar kernels)")
     ap.add_argument("--b-host", default="wc", choices=["wc", "pinned"],
                     help="page-locked host staging of b for the end-to-end run: write-combined or cached")
+    ap.add_argument("--z-host", default="pinned", choices=["wc", "pinned"],
+                    help="page-locked host memory receiving z in the end-to-end run: write-combined or cached")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -343,13 +345,15 @@ def gpu_arm(args, world, rank, local_rank, dist):
     # streams (double-buffered) and overlap the previous / next step's compute
     e2e = None
     if not args.no_e2e:
-        e2e_s = end_to_end(torch, h, w, b_host, p, r, stream, dev, K, dist, run, primal)
+        e2e_s = end_to_end(torch, h, w, b_host, p, r, stream, dev, K, dist, run, primal,
+                           z_wc=args.z_host == "wc")
         e2e = {"value": round(world * N * w.steps * K / e2e_s / 1e9, 3), "unit": UNIT,
                "h2d_bytes_per_step": 4 * w.ny * w.nz * pitch, "d2h_bytes_per_step": 4 * w.ny * w.nz * pitch,
                "ms_per_step": round(e2e_s * 1e3 / K, 4),
                "overlap": "H2D of step j+1 and D2H of step j on two copy streams, double-buffered",
-               "host_memory": "b from %s page-locked memory, z to page-locked memory (tvfgp_host_alloc)"
-                              % ("write-combined" if args.b_host == "wc" else "cached")}
+               "host_memory": "b from %s, z to %s page-locked memory (tvfgp_host_alloc)"
+                              % ("write-combined" if args.b_host == "wc" else "cached",
+                                 "write-combined" if args.z_host == "wc" else "cached")}
         if h.check(stream) != T.TVFGP_OK:
             raise RuntimeError("device error word set during the end-to-end run")
 
@@ -416,7 +420,7 @@ def gpu_arm(args, world, rank, local_rank, dist):
     return out
 
 
-def end_to_end(torch, h, w, b_host, p, r, stream, dev, K, dist, run, primal):
+def end_to_end(torch, h, w, b_host, p, r, stream, dev, K, dist, run, primal, z_wc=False):
     """Wall time of K outer iterations where each step's b comes from pinned
     host memory and its z goes back to pinned host memory."""
     n_b = len(b_host)
@@ -424,7 +428,7 @@ def end_to_end(torch, h, w, b_host, p, r, stream, dev, K, dist, run, primal):
     b_in = [torch.empty(shape, device=dev) for _ in range(2)]
     z_out = [torch.empty(shape, device=dev) for _ in range(2)]
     from fgp_dual_stencil_gb300 import tvfgp as T
-    z_host = [T.host_tensor(shape) for _ in range(2)]
+    z_host = [T.host_tensor(shape, write_combined=z_wc) for _ in range(2)]
     s_in = torch.cuda.Stream(dev)
     s_out = torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]       # b_in[s] filled
