@@ -296,9 +296,13 @@ __global__ void __launch_bounds__(ZmLayout<TS>::THREADS, ZmLayout<TS>::MINB)
     auto parity_of = [&](int q) { return static_cast<uint32_t>(((q - z0) / L::STAGES) & 1); };
     auto zrow = [&](int q, int rr) { return zpl + ((q % 3) * L::ROWS + rr) * L::ZP; };
 
-    // prologue: z of plane z0, own r at z0
+    // prologue: z of plane z0, own r at z0.  The z at column x0+TX of every
+    // row (the x+1 neighbour of the row's last quad) is computed by thread
+    // hrow = tid for rows tid < ROWS: one warp does all rows at once.
     float4 Rc0, Rc1, Rc2, Zc;
-    float r2halo = 0.0f;                            // r2 at column x0+TX of the current plane
+    const bool do_halo = tid < L::ROWS;
+    const int hrow = tid;
+    float r2halo = 0.0f;                            // r2 at column x0+TX of row hrow, current plane
     bool ok = true;
     {
         float4 r2lo = f4zero();
@@ -307,7 +311,7 @@ __global__ void __launch_bounds__(ZmLayout<TS>::THREADS, ZmLayout<TS>::MINB)
             ok = mbar_wait_tma(&bars[L::STAGES], 0);
             const TS *P2 = reinterpret_cast<const TS *>(smem + L::OFF_PREV);
             r2lo = lds4(P2 + row * L::RW + 4 * qx);
-            r2lo_h = lds1(P2 + row * L::RW + L::TX);
+            if (do_halo) r2lo_h = lds1(P2 + hrow * L::RW + L::TX);
         }
         ok = ok && mbar_wait_tma(&bars[0], 0);
         if (ok) {
@@ -315,7 +319,7 @@ __global__ void __launch_bounds__(ZmLayout<TS>::THREADS, ZmLayout<TS>::MINB)
             zm_quad<TS>(st, row, qx, r2lo, lam, Rc0, Rc1, Rc2, Zc);
             float *zr = zrow(z0, row);
             *reinterpret_cast<float4 *>(zr + 4 * qx) = Zc;
-            if (qx == L::QX - 1) zr[L::TX] = zm_halo<TS>(st, row, r2lo_h, lam, r2halo);
+            if (do_halo) zrow(z0, hrow)[L::TX] = zm_halo<TS>(st, hrow, r2lo_h, lam, r2halo);
         } else {
             *abort_flag = 1;
         }
@@ -340,7 +344,7 @@ __global__ void __launch_bounds__(ZmLayout<TS>::THREADS, ZmLayout<TS>::MINB)
                 zm_quad<TS>(st, row, qx, Rc2, lam, Rn0, Rn1, Rn2, Zn);
                 float *zr = zrow(z + 1, row);
                 *reinterpret_cast<float4 *>(zr + 4 * qx) = Zn;
-                if (qx == L::QX - 1) zr[L::TX] = zm_halo<TS>(st, row, r2halo, lam, r2halo_n);
+                if (do_halo) zrow(z + 1, hrow)[L::TX] = zm_halo<TS>(st, hrow, r2halo, lam, r2halo_n);
             } else {
                 *abort_flag = 1;
             }
