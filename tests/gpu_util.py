@@ -42,7 +42,21 @@ def run_workload_gpu(w, variant="auto", graph=False, p0=None, r0=None):
     return b_np, host(p), host(r), host(zp), host(zr), launched
 
 
+_ORACLE_RUNS = {}
+
+
 def run_workload_oracle(w, p0=None, r0=None):
+    """The workload on the oracle: (b_last, p, r, z_of_p, z_of_r).  Runs from
+    p = r = 0 are computed once per test session and shared (the arrays are
+    only read by the callers)."""
+    if p0 is None and r0 is None:
+        if w.key not in _ORACLE_RUNS:
+            _ORACLE_RUNS[w.key] = _run_workload_oracle(w)
+        return _ORACLE_RUNS[w.key]
+    return _run_workload_oracle(w, p0, r0)
+
+
+def _run_workload_oracle(w, p0=None, r0=None):
     base = synth.phantom(w)
     shape = (3, w.nz, w.ny, w.nx)
     p = np.zeros(shape, np.float32) if p0 is None else p0.copy()

@@ -190,3 +190,21 @@ def test_f16_argument_errors(T):
         assert T.tvfgp_launch_count(h) == 0
     finally:
         T.tvfgp_destroy(h)
+
+
+@pytest.mark.slow
+def test_f16_1000x600x300_exact(T):
+    """The 1000x600x300 blob volume with a binary16 dual (nx % 8 == 0: the
+    z-march), its first 30 steps, against the binary16 oracle."""
+    w = synth.WORKLOADS["c5"]
+    b = synth.make_b(w, 0, synth.phantom(w))
+    shape = (3, w.nz, w.ny, w.nx)
+    ph = np.zeros(shape, np.uint16)
+    rh = np.zeros(shape, np.uint16)
+    p, r = dev16(ph), dev16(rh)
+    with T.Tvfgp(w.nx, w.ny, w.nz, "auto", True) as h:
+        h.run_f16(dev(b), p, r, w.lam, 30, w.t0)
+        assert h.last_variant == T.TVFGP_VARIANT_ZMARCH_TMA
+        assert h.check() == 0
+    oracle.fgp_run_h16(b, ph, rh, w.lam, 30, w.t0)
+    assert np.array_equal(bits(p), ph) and np.array_equal(bits(r), rh)

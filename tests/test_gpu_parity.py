@@ -41,7 +41,7 @@ def test_small_workloads_exact(T, key, variant):
     assert launched == w.outers * per_outer + 2
 
 
-@pytest.mark.parametrize("variant", ["auto", "cube"])
+@pytest.mark.parametrize("variant", ["auto", "cube", "zmarch", "fused", "separate", "scalar"])
 def test_256_warm_started_outers_graph(T, variant):
     """20 outers x 10 steps, fresh noise per outer, t0 reset, graph replay
     re-parameterised with every new b."""
@@ -52,11 +52,12 @@ def test_256_warm_started_outers_graph(T, variant):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("key,variant", [("c4", "auto"), ("c5", "auto"), ("c4", "zmarch2")])
+@pytest.mark.parametrize("key,variant", [("c4", "auto"), ("c5", "auto"), ("c4", "zmarch2"), ("c4", "cube"),
+                                         ("c5", "zmarch")])
 def test_large_workloads(T, key, variant):
     """The 512^3 workload in the configuration the bench times (AUTO variant,
-    graph replay), the 1000x600x300 blob volume, and 512^3 with two steps per
-    launch."""
+    graph replay), the 1000x600x300 blob volume, and both again with other
+    kernels (two steps per launch, cube tiles, one step per launch)."""
     w = synth.WORKLOADS[key]
     b, *gpu, _ = run_workload_gpu(w, variant, graph=(key == "c4"))
     ref = run_workload_oracle(w)

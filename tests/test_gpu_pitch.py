@@ -178,3 +178,24 @@ def test_pitch_argument_errors(T):
     assert T.raw_call("tvfgp_create_pitched", 8, 4, 4, 7, ctypes.byref(h)) == T.TVFGP_ERR_ARG
     assert T.raw_call("tvfgp_create_pitched", 8, 4, 4, 65536, ctypes.byref(h)) == T.TVFGP_ERR_ARG
     assert T.raw_call("tvfgp_create_pitched", 8, 4, 4, 10, None) == T.TVFGP_ERR_ARG
+
+
+@pytest.mark.slow
+def test_pitched_1000x600x300(T):
+    """The 1000x600x300 workload (100 steps) with rows of 1002 floats, which
+    bench --pitch fft times on the packed path, against the dense oracle."""
+    import torch
+    from gpu_util import run_workload_oracle
+    w = synth.WORKLOADS["c5"]
+    b = synth.make_b(w, 0, synth.phantom(w))
+    pitch = T.fft_pitch(w.nx)
+    p = torch.zeros((3, w.nz, w.ny, pitch), device="cuda")
+    r = torch.zeros_like(p)
+    with T.Tvfgp(w.nx, w.ny, w.nz, "auto", True, pitch=pitch) as h:
+        h.run(dev(pad(b, pitch, 30)), p, r, w.lam, w.steps, w.t0)
+        assert h.last_variant == T.TVFGP_VARIANT_ZMARCH2_TMA
+        assert h.check() == 0
+    _, po, ro, _, _ = run_workload_oracle(w)
+    assert np.array_equal(p.cpu().numpy()[..., :w.nx], po)
+    assert np.array_equal(r.cpu().numpy()[..., :w.nx], ro)
+    assert not p[..., w.nx:].any() and not r[..., w.nx:].any()
