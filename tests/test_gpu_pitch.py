@@ -199,3 +199,26 @@ def test_pitched_1000x600x300(T):
     assert np.array_equal(p.cpu().numpy()[..., :w.nx], po)
     assert np.array_equal(r.cpu().numpy()[..., :w.nx], ro)
     assert not p[..., w.nx:].any() and not r[..., w.nx:].any()
+
+
+@pytest.mark.parametrize("shape,pitch", [((32, 9, 7), None), ((34, 9, 7), None), ((33, 5, 4), None),
+                                         ((40, 6, 5), 45)])
+def test_pitched_single_step(T, shape, pitch):
+    """tvfgp_step on padded rows (the in-place kernels: quads as two halves,
+    pairs, or scalar) against one oracle step; r_dst's padding untouched."""
+    nx, ny, nz = shape
+    pitch = pitch or T.fft_pitch(nx)
+    b = synth.random_case(shape, 91)
+    p0 = synth.random_dual(shape, 92, scale=0.4)
+    r0 = synth.random_dual(shape, 93, scale=0.6)
+    bp, pp, rp, rdp = pad(b, pitch, 14), pad(p0, pitch, 15), pad(r0, pitch, 16), pad(np.zeros_like(r0), pitch, 17)
+    p, rs, rd = dev(pp), dev(rp), dev(rdp)
+    with T.Tvfgp(nx, ny, nz, pitch=pitch) as h:
+        h.step(dev(bp), p, rs, rd, 0.06, 0.3)
+        assert h.last_variant == pitched_variant(T, nx, pitch)
+        assert h.check() == 0
+    po = p0.copy()
+    ro, _ = oracle.fgp_step(b, po, r0, 0.06, 0.3)
+    check(p, po, pp, nx, "p")
+    check(rd, ro, rdp, nx, "r_dst")
+    check(rs, r0, rp, nx, "r_src")
