@@ -384,7 +384,7 @@ __device__ __forceinline__ float4 zquad(float4 B, float4 R0, float4 R1, float4 R
 // next plane's own b and r, then row y+1: no barrier exists in this kernel.
 // Requirements: nx % 4 == 0 and 16-byte aligned b, p, rs, rd.
 #ifndef TVFGP_FUSED_MINB
-#define TVFGP_FUSED_MINB 6
+#define TVFGP_FUSED_MINB 5
 #endif
 template <int BY, int ZC, typename TS = float, int VW = 4>
 __global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(const StepArgsT<TS> a)
