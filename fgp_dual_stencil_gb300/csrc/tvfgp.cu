@@ -1,11 +1,14 @@
 // C-ABI of the FGP step library (declarations and contract: include/tvfgp.h).
 //
 // Host side: argument checks, the FISTA momentum schedule in double, the
-// ping-pong of r between the caller's buffer and the handle's scratch
-// buffer, eager launches back to back with no host synchronisation, and a
-// CUDA graph of the whole nsteps loop that is re-parameterised in place when
-// the buffers, lambda or t0 change (page "TV solver: the FGP step on the
-// GPU", sections "Variants" and "What made the difference").
+// plan of a run (two-step launches that route p and r through the handle's
+// two extra dual sets, or one-step launches that ping-pong r with the
+// scratch dual), eager launches back to back with no host synchronisation,
+// and a CUDA graph of the whole nsteps loop that is re-parameterised in place
+// when the buffers, lambda or t0 change (page "TV solver: the FGP step on the
+// GPU", sections "Variants" and "What made the difference").  Volumes with
+// padded rows run in place on the scalar / 8-byte kernels, or are packed
+// into dense buffers for long runs (tvfgp_create_pitched).
 #include "tvfgp.h"
 #include "fgp_kernels.cuh"
 #include "zmarch_tma.cuh"
