@@ -44,6 +44,32 @@ constexpr int kFusedBY = TVFGP_FUSED_BY;
 constexpr int kFusedZC = TVFGP_FUSED_ZC;
 constexpr int kPrimalBY = 8;
 
+// Test hook (tvfgp_debug_fail_allocs): the library's next g_alloc_skip
+// device allocations succeed, the g_alloc_fail after them fail.
+std::mutex g_alloc_mutex;
+int g_alloc_skip = 0, g_alloc_fail = 0;
+
+// Every device allocation of the library goes through here.
+template <typename T>
+cudaError_t dev_alloc(T **ptr, size_t bytes)
+{
+    bool fail = false;
+    {
+        std::lock_guard<std::mutex> lock(g_alloc_mutex);
+        if (g_alloc_skip > 0) {
+            --g_alloc_skip;
+        } else if (g_alloc_fail > 0) {
+            --g_alloc_fail;
+            fail = true;
+        }
+    }
+    if (fail) {
+        *ptr = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    return cudaMalloc(reinterpret_cast<void **>(ptr), bytes);
+}
+
 // The default vector variant chosen by AUTO.
 constexpr int kAutoVariant = TVFGP_VARIANT_ZMARCH2_TMA;
 
@@ -636,7 +662,7 @@ int run_graph(tvfgp_handle *h, int variant, const float *b, float *p, float *r, 
 int ensure_z_scratch(tvfgp_handle *h)
 {
     if (h->zscratch) return TVFGP_OK;
-    cudaError_t e = cudaMalloc(&h->zscratch, sizeof(float) * static_cast<size_t>(h->N));
+    cudaError_t e = dev_alloc(&h->zscratch, sizeof(float) * static_cast<size_t>(h->N));
     if (e != cudaSuccess) {
         cudaGetLastError();
         h->zscratch = nullptr;
@@ -648,7 +674,7 @@ int ensure_z_scratch(tvfgp_handle *h)
 int ensure_pair_scratch(tvfgp_handle *h)
 {
     if (h->pair_scratch) return TVFGP_OK;
-    cudaError_t e = cudaMalloc(&h->pair_scratch, sizeof(float) * 9 * static_cast<size_t>(h->N));
+    cudaError_t e = dev_alloc(&h->pair_scratch, sizeof(float) * 9 * static_cast<size_t>(h->N));
     if (e != cudaSuccess) {
         cudaGetLastError();
         h->pair_scratch = nullptr;
@@ -665,7 +691,7 @@ int ensure_shadow(tvfgp_handle *h)
 {
     if (h->shadow) return TVFGP_OK;
     const size_t n = static_cast<size_t>(h->nx) * h->ny * h->nz;
-    cudaError_t e = cudaMalloc(&h->pk, sizeof(float) * 7 * n);
+    cudaError_t e = dev_alloc(&h->pk, sizeof(float) * 7 * n);
     if (e != cudaSuccess) {
         cudaGetLastError();
         h->pk = nullptr;
@@ -763,8 +789,8 @@ static int create_impl(int nx, int ny, int nz, int px, int variant, unsigned fla
     h->d_err = nullptr;
     h->shadow = nullptr;
     h->pk = nullptr;
-    cudaError_t e = cudaMalloc(&h->scratch, sizeof(float) * 3 * static_cast<size_t>(h->N));
-    if (e == cudaSuccess) e = cudaMalloc(&h->d_err, sizeof(int));
+    cudaError_t e = dev_alloc(&h->scratch, sizeof(float) * 3 * static_cast<size_t>(h->N));
+    if (e == cudaSuccess) e = dev_alloc(&h->d_err, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(int));
     if (e == cudaSuccess) {
         if (zmarch_plan(nx, ny, nz, &h->zplan) != TVFGP_OK ||
@@ -1172,6 +1198,15 @@ int tvfgp_debug_projection_check(int mode, unsigned long long count, unsigned lo
     projection_check<<<sms * 8, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(mode, count, seed, out);
     e = cudaGetLastError();
     return e == cudaSuccess ? TVFGP_OK : from_cuda(e);
+}
+
+int tvfgp_debug_fail_allocs(int skip, int count)
+{
+    if (skip < 0 || count < 0) return TVFGP_ERR_ARG;
+    std::lock_guard<std::mutex> lock(g_alloc_mutex);
+    g_alloc_skip = count > 0 ? skip : 0;
+    g_alloc_fail = count;
+    return TVFGP_OK;
 }
 
 int tvfgp_debug_timeout_probe(tvfgp_t h, int spins, tvfgp_stream_t stream)

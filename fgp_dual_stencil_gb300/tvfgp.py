@@ -68,6 +68,7 @@ def _load():
         "tvfgp_last_variant": ([vp], i),
         "tvfgp_launch_count": ([vp], ll),
         "tvfgp_debug_timeout_probe": ([vp, i, vp], i),
+        "tvfgp_debug_fail_allocs": ([i, i], i),
         "tvfgp_debug_projection_check": ([i, ctypes.c_ulonglong, ctypes.c_ulonglong, vp, vp], i),
         "tvfgp_run_noalloc": ([i, i, i, vp, vp, vp, f, i, d, vp, ctypes.POINTER(d)], i),
         "tvfgp_host_alloc": ([ctypes.c_size_t, i, ctypes.POINTER(vp)], i),
@@ -253,6 +254,12 @@ def tvfgp_debug_projection_check(mode: int, count: int, seed: int, out, stream=N
         raise ValueError("out must be a CUDA int64 tensor of 2 elements")
     _ok(_lib.tvfgp_debug_projection_check(int(mode), int(count), int(seed) & (2**64 - 1), out.data_ptr(),
                                           _stream(stream)), "tvfgp_debug_projection_check")
+
+
+def tvfgp_debug_fail_allocs(skip: int, count: int) -> None:
+    """Let the library's next `skip` device allocations succeed and fail the
+    `count` after them (test hook; count = 0 clears it)."""
+    _ok(_lib.tvfgp_debug_fail_allocs(int(skip), int(count)), "tvfgp_debug_fail_allocs")
 
 
 def tvfgp_debug_timeout_probe(h: int, spins: int, stream=None) -> None:

@@ -232,6 +232,13 @@ int tvfgp_host_free(void *p);
  * reports TVFGP_ERR_TIMEOUT.  1 <= spins <= 2^24. */
 int tvfgp_debug_timeout_probe(tvfgp_t h, int spins, tvfgp_stream_t stream);
 
+/* Test hook for allocation failures: of the library's next device
+ * allocations (handle scratch, error word, extra dual sets, z volume,
+ * packed staging), the first `skip` succeed and the `count` after them fail
+ * with TVFGP_ERR_OOM without reaching the CUDA allocator; count = 0 clears
+ * the hook.  Process-wide.  skip or count < 0: TVFGP_ERR_ARG. */
+int tvfgp_debug_fail_allocs(int skip, int count);
+
 /* Self-check of the step kernels' projection onto the unit ball, which
  * evaluates q / max(1, |q|) with a hardware square-root estimate and fused
  * multiply-add corrections instead of IEEE square root and division, and

@@ -102,3 +102,17 @@ def test_host_alloc_argument_checks(T):
     assert p.value is None
     assert T.raw_call("tvfgp_host_alloc", 16, 0, None) == T.TVFGP_ERR_ARG
     assert T.raw_call("tvfgp_host_free", None) == T.TVFGP_OK
+
+
+def test_allocation_failure_hook_without_gpu(T):
+    """The allocation-failure hook fails a create cleanly before any device
+    allocation is attempted; its arguments are checked."""
+    assert T.raw_call("tvfgp_debug_fail_allocs", -1, 1) == T.TVFGP_ERR_ARG
+    assert T.raw_call("tvfgp_debug_fail_allocs", 0, -1) == T.TVFGP_ERR_ARG
+    assert T.raw_call("tvfgp_debug_fail_allocs", 0, 1) == T.TVFGP_OK
+    h = ctypes.c_void_p(5)
+    try:
+        assert T.raw_call("tvfgp_create", 8, 8, 8, ctypes.byref(h)) == T.TVFGP_ERR_OOM
+        assert h.value is None
+    finally:
+        assert T.raw_call("tvfgp_debug_fail_allocs", 0, 0) == T.TVFGP_OK
