@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 import subprocess
+import sys
 
 import numpy as np
 import pytest
@@ -116,3 +117,22 @@ def test_allocation_failure_hook_without_gpu(T):
         assert h.value is None
     finally:
         assert T.raw_call("tvfgp_debug_fail_allocs", 0, 0) == T.TVFGP_OK
+
+
+def test_binding_fails_loudly_without_the_library():
+    """With libtvfgp.so absent the binding raises ImportError at import; there
+    is no fallback path."""
+    code = (
+        "import os, sys\n"
+        "sys.path.insert(0, %r)\n"
+        "real = os.path.exists\n"
+        "os.path.exists = lambda p: False if str(p).endswith('libtvfgp.so') else real(p)\n"
+        "try:\n"
+        "    import fgp_dual_stencil_gb300.tvfgp\n"
+        "except ImportError as e:\n"
+        "    print('ImportError:', e)\n"
+        "    sys.exit(0)\n"
+        "sys.exit(3)\n" % ROOT)
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert "libtvfgp.so is not built" in out.stdout
