@@ -57,7 +57,8 @@ def parse_args():
                     help="storage of p and r (f16: binary16, fp32 arithmetic; changes the result)")
     ap.add_argument("--pitch", default="dense", choices=["dense", "fft"],
                     help="row layout of every volume: dense, or padded to 2*(nx/2+1) floats "
-                         "(in-place real-to-complex FFT layout; runs the scalar kernels)")
+                         "(in-place real-to-complex FFT layout: runs of >= 4 steps are packed into "
+                         "dense buffers, shorter ones run in place)")
     ap.add_argument("--b-host", default="wc", choices=["wc", "pinned"],
                     help="page-locked host staging of b for the end-to-end run: write-combined or cached")
     ap.add_argument("--z-host", default="pinned", choices=["wc", "pinned"],
