@@ -339,8 +339,8 @@ def test_half_conversions_match_ieee_binary16():
     rng = np.random.default_rng(0)
     x = (rng.standard_normal(400_000) * np.exp(rng.uniform(-20, 12, 400_000))).astype(np.float32)
     # exact halfway cases between neighbouring binary16 values: ties to even
-    mids = ((ref[:-1].astype(np.float64) + ref[1:].astype(np.float64)) / 2)[np.isfinite(ref[:-1]) &
-                                                                              np.isfinite(ref[1:])]
+    finite = np.isfinite(ref[:-1]) & np.isfinite(ref[1:])
+    mids = (ref[:-1][finite].astype(np.float64) + ref[1:][finite].astype(np.float64)) / 2
     mids = mids[np.abs(mids) < 65504].astype(np.float32)
     x = np.concatenate([x, mids, np.array([0.0, -0.0, 65504, 65519.9, 65520, 1e-8, -6e-8], np.float32)])
     with np.errstate(over="ignore"):
