@@ -63,6 +63,9 @@ namespace tvfgp {
 #ifndef TVFGP_Z2_WAVES
 #define TVFGP_Z2_WAVES 2          // fewest waves of CTAs over the resident slots
 #endif
+#ifndef TVFGP_Z2_EDGE_SPLIT
+#define TVFGP_Z2_EDGE_SPLIT 1     // boundary tests in step k only in CTAs that touch a face
+#endif
 
 constexpr int Z2_TX = TVFGP_Z2_TX;          // output tile width
 constexpr int Z2_TY = TVFGP_Z2_TY;          // output tile height
@@ -110,6 +113,12 @@ constexpr int Z2_TASKS_D = Z2_QD * Z2_TY;
 // of z^{k+1}'s x+1 column and y+1 row go to the threads from TASKS_D on, which
 // are free after the barrier.
 constexpr int Z2_THREADS = (Z2_TASKS_A + 31) / 32 * 32;
+// The thread that issues the copies of the next planes: the last one, in the
+// warp with the least work (none of the tile's four phases).
+#ifndef TVFGP_Z2_PRODUCER
+#define TVFGP_Z2_PRODUCER (Z2_THREADS - 1)
+#endif
+constexpr int Z2_PRODUCER = TVFGP_Z2_PRODUCER;
 constexpr int Z2_RING_B = Z2_TASKS_B - Z2_TASKS_D;        // 2 QA + 2 TY
 constexpr int Z2_HALO_C = (Z2_TY + 1) + Z2_QD;            // z^{k+1} quads outside the tile
 constexpr int Z2_HALO_T = Z2_THREADS - Z2_TASKS_D;        // threads that take them
@@ -178,7 +187,7 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     auto slot = [&](int q) { return (q - f) % Z2_STAGES; };
     auto stage = [&](int q) { return smem + slot(q) * Z2_STAGE_STRIDE; };
     auto parity = [&](int q) { return static_cast<uint32_t>(((q - f) / Z2_STAGES) & 1); };
-    auto issue = [&](int q) {                   // thread 0 only
+    auto issue = [&](int q) {                   // the producer thread only
         unsigned char *st = stage(q);
         uint64_t *bar = &bars[slot(q)];
         const bool with_p = q <= uk_last;       // the plane past the last step-k plane feeds z^k only
@@ -219,6 +228,14 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     const bool doA = tid < Z2_TASKS_A;
     const bool doB = tid < Z2_TASKS_B;
     const bool my_tile = tid < Z2_TASKS_D;
+    // Step k's quads cover lx -4..TX+3, ly -1..TY.  When all of them lie
+    // inside the volume and none touches the upper x face, step k needs no
+    // per-voxel boundary test (most CTAs of a large volume).
+#if TVFGP_Z2_EDGE_SPLIT
+    const bool edge = !(x0 >= 4 && x0 + Z2_TX + 5 <= nx && y0 >= 1 && y0 + Z2_TY + 2 <= ny);
+#else
+    const bool edge = true;
+#endif
 
     // z^k of plane q for this thread's quad, from the staged plane st and the
     // r2 of the plane below (lo: a staged r2 box, or nullptr at plane 0);
@@ -244,7 +261,7 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
         return Z;
     };
 
-    if (tid == 0) {
+    if (tid == Z2_PRODUCER) {
         if (f > 0) {
             mbar_expect_tx(&bars[Z2_STAGES], Z2_BYTES_R);
             tma_load_3d(smem + Z2_OFF_PREV, &za.tr2, x0 - 4, y0 - 2, f - 1, &bars[Z2_STAGES]);
@@ -304,7 +321,6 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
                    R2 = lds4(F(st, Z2_OFF_R2) + ro);
             float4 P0 = lds4(F(st, Z2_OFF_P0) + po), P1 = lds4(F(st, Z2_OFF_P1) + po),
                    P2 = lds4(F(st, Z2_OFF_P2) + po);
-            const bool yin = y >= 0 && y < ny;
             const bool gy = y < ny - 1;
             const float zcv[5] = {zc.x, zc.y, zc.z, zc.w, zx};
             const float zyv[4] = {zy.x, zy.y, zy.z, zy.w};
@@ -313,19 +329,26 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
             float *g0 = &G0.x, *g1 = &G1.x, *g2 = &G2.x;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int xe = x + e;
-                g0[e] = (xe < nx - 1) ? __fsub_rn(zcv[e], zcv[e + 1]) : 0.0f;
+                g0[e] = __fsub_rn(zcv[e], zcv[e + 1]);
                 g1[e] = gy ? __fsub_rn(zcv[e], zyv[e]) : 0.0f;
                 g2[e] = hasZ ? __fsub_rn(zcv[e], zzv[e]) : 0.0f;
+            }
+            if (edge) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (!(x + e < nx - 1)) g0[e] = 0.0f;
             }
             dual_update4(R0, R1, R2, G0, G1, G2, P0, P1, P2, s, m0);
             // voxels of the ring outside the volume: r^{k+1} = 0, the r(-1) = 0
             // boundary of step k+1 (their p is never used)
-            float *r0 = &R0.x, *r1 = &R1.x, *r2 = &R2.x;
+            if (edge) {
+                const bool yin = y >= 0 && y < ny;
+                float *r0 = &R0.x, *r1 = &R1.x, *r2 = &R2.x;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int xe = x + e;
-                if (!(yin && xe >= 0 && xe < nx)) r0[e] = r1[e] = r2[e] = 0.0f;
+                for (int e = 0; e < 4; ++e) {
+                    const int xe = x + e;
+                    if (!(yin && xe >= 0 && xe < nx)) r0[e] = r1[e] = r2[e] = 0.0f;
+                }
             }
             const int mo = row * Z2_PK + c;
             *reinterpret_cast<float4 *>(mrp(q, 0) + mo) = R0;
@@ -394,7 +417,7 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
         cP2 = nP2;
         __syncthreads();
         // every read of plane q's stage is done: the slot takes the next plane
-        if (tid == 0 && next_issue <= last && q <= uk_last) {
+        if (tid == Z2_PRODUCER && next_issue <= last && q <= uk_last) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             issue(next_issue++);
         }
