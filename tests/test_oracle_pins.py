@@ -325,6 +325,72 @@ def test_fgp_converges_to_certified_tv_prox(shape, lam):
     assert np.abs(z32 - x_star).max() <= 1e-4
 
 
+def tv1d_brute_force(y, lam):
+    """Exact minimiser of 1/2 |x - y|^2 + lam * sum_i |x(i+1) - x(i)| for a
+    short signal, by enumeration.  With u the dual (x = y - D^T u, where
+    (D^T u)(i) = u(i-1) - u(i) and u(-1) = u(n-1) = 0), optimality makes x
+    constant on runs between jumps and u = lam * sign(jump) at each jump, so
+    summing x = y - D^T u over a run [a, e] gives its value
+    mean(y[a..e]) - (u(a-1) - u(e)) / (e - a + 1).  Every choice, per edge,
+    of "no jump", "up" or "down" yields such a candidate; the optimum is one
+    of them, and since each candidate is a feasible point, it is the one of
+    least objective."""
+    import itertools
+    n = len(y)
+    best, best_x = np.inf, None
+    for pattern in itertools.product((0, 1, -1), repeat=n - 1):
+        x = np.empty(n)
+        a = 0
+        for e in range(n):
+            if e == n - 1 or pattern[e] != 0:
+                u_left = lam * pattern[a - 1] if a > 0 else 0.0
+                u_right = lam * pattern[e] if e < n - 1 else 0.0
+                x[a:e + 1] = y[a:e + 1].mean() - (u_left - u_right) / (e - a + 1)
+                a = e + 1
+        obj = 0.5 * ((x - y) ** 2).sum() + lam * np.abs(np.diff(x)).sum()
+        if obj < best:
+            best, best_x = obj, x
+    return best_x
+
+
+def test_tv1d_brute_force_on_hand_cases():
+    # no jump can pay for itself when lam is large: the mean
+    y = np.array([0.1, 0.9, 0.3, 0.7])
+    assert np.allclose(tv1d_brute_force(y, 10.0), y.mean())
+    # a single step: each run moves towards the other by lam / (its length)
+    y = np.array([0.0, 0.0, 1.0, 1.0])
+    assert np.allclose(tv1d_brute_force(y, 0.1), [0.05, 0.05, 0.95, 0.95])
+    # lam -> 0 gives y back
+    y = np.array([0.3, 0.1, 0.4, 0.1, 0.5])
+    assert np.allclose(tv1d_brute_force(y, 1e-9), y, atol=1e-8)
+
+
+@pytest.mark.parametrize("axis", [0, 1, 2])
+@pytest.mark.parametrize("n,lam,seed", [(7, 0.05, 1), (8, 0.1, 2), (9, 0.02, 3)])
+def test_fgp_on_a_line_is_1d_tv_denoising(axis, n, lam, seed):
+    """On an n x 1 x 1 volume (or its y / z twins) with b >= 0 the prox is
+    plain 1D TV denoising (x >= 0 is inactive by the maximum principle), so a
+    long FGP run must reach the brute-force minimiser."""
+    rng = np.random.default_rng(seed)
+    y = np.clip(np.repeat(rng.uniform(0.0, 1.0, size=3), [2, n - 4, 2]) + rng.normal(0.0, 0.1, size=n), 0.0, None)
+    x_star = tv1d_brute_force(y, lam)
+    shape = [1, 1, 1]
+    shape[2 - axis] = n                        # arrays are (nz, ny, nx)
+    b = y.reshape(shape)
+    p, r = zeros_dual(b), zeros_dual(b)
+    oracle.fgp_run(b, p, r, lam, 20000, 1.0)
+    z = oracle.primal(b, p, lam).ravel()
+    assert np.abs(z - x_star).max() <= 1e-6
+    # the other components of the dual stay exactly 0
+    for a in range(3):
+        if a != axis:
+            assert np.all(p[a] == 0) and np.all(r[a] == 0)
+    b32 = b.astype(np.float32)
+    p32, r32 = zeros_dual(b32), zeros_dual(b32)
+    oracle.fgp_run(b32, p32, r32, lam, 5000, 1.0)
+    assert np.abs(oracle.primal(b32, p32, lam).ravel() - x_star).max() <= 1e-4
+
+
 # ---------------------------------------------------------------------------
 # binary16 storage of the dual
 # ---------------------------------------------------------------------------
