@@ -44,6 +44,11 @@ struct StepArgsT {
     int nx, ny, nz;
     long long N;       // elements per volume: px*ny*nz
     int px = 0;        // row pitch in elements (0: nx); only the scalar kernels take px != nx
+    // packing step (fused kernel only): p' goes to po and r to rd as dense
+    // volumes of No elements each, and b is copied to bo (dense)
+    TS *po = nullptr;
+    float *bo = nullptr;
+    long long No = 0;
 };
 using StepArgs = StepArgsT<float>;
 
@@ -383,12 +388,16 @@ __device__ __forceinline__ float4 zquad(float4 B, float4 R0, float4 R1, float4 R
 // The voxel's own p loads are issued first in every iteration, then the
 // next plane's own b and r, then row y+1: no barrier exists in this kernel.
 // Requirements: nx % 4 == 0 and 16-byte aligned b, p, rs, rd.
+// With PACK, the step reads padded rows (pitch px, 8-byte halves of quads)
+// and writes p', r and a copy of b as dense volumes (16-byte stores), so the
+// first step of a run on the real-to-complex FFT layout also packs it.
 #ifndef TVFGP_FUSED_MINB
 #define TVFGP_FUSED_MINB 5
 #endif
-template <int BY, int ZC, typename TS = float, int VW = 4>
+template <int BY, int ZC, typename TS = float, int VW = 4, bool PACK = false>
 __global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(const StepArgsT<TS> a)
 {
+    static_assert(!PACK || (VW == 2 && sizeof(TS) == 4), "packing reads padded fp32 rows");
     const int lane = threadIdx.x;
     const int x0 = (blockIdx.x * 32 + lane) * 4;
     const int y = blockIdx.y * BY + threadIdx.y;
@@ -409,12 +418,20 @@ __global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(con
     TS *__restrict__ p0 = a.p;
     TS *__restrict__ p1 = a.p + a.N;
     TS *__restrict__ p2 = a.p + 2 * a.N;
+    // outputs: in place (p) and at the input's layout (r), or dense when packing
+    const long long No = PACK ? a.No : a.N;
+    TS *__restrict__ q0 = PACK ? a.po : a.p;
+    TS *__restrict__ q1 = q0 + No;
+    TS *__restrict__ q2 = q0 + 2 * No;
     TS *__restrict__ o0 = a.rd;
-    TS *__restrict__ o1 = a.rd + a.N;
-    TS *__restrict__ o2 = a.rd + 2 * a.N;
+    TS *__restrict__ o1 = a.rd + No;
+    TS *__restrict__ o2 = a.rd + 2 * No;
+    constexpr int VO = PACK ? 4 : VW;            // store width
+    const int szo = PACK ? nx * ny : px * ny;
 
     int z = zb;
     int i = x0 + px * (y + ny * z);
+    int io = PACK ? x0 + nx * (y + ny * z) : i;
 
     // prologue: own r at plane zb and z(i) there
     float4 R0c = f4zero(), R1c = f4zero(), R2c = f4zero(), Zc;
@@ -431,12 +448,13 @@ __global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(con
         float left = __shfl_up_sync(kFull, R0c.w, 1);
         if (lane == 0) left = (x0 > 0) ? ld1_ro(r0 + i - 1) : 0.0f;
         Zc = zquad(Bc, R0c, R1c, R2c, left, R1lo, R2lo, lam);
+        if (PACK && xin) stq<4>(a.bo + io, Bc);
     }
     // r2 of row y+1 one plane below (the z-lower neighbour of z(i+ey))
     float4 R2yp = f4zero();
     if (xin && hasY && z > 0) R2yp = ldvq_ro<VW>(r2 + i + px - sz);
 
-    for (; z < ze; ++z, i += sz) {
+    for (; z < ze; ++z, i += sz, io += szo) {
         const bool hasZ = (z + 1 < nz);          // block-uniform
 
         // (1) the voxel's own p, first
@@ -504,12 +522,13 @@ __global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(con
             dual_update(N0.y, N1.y, N2.y, __fsub_rn(Zc.y, Zc.z), G1.y, G2.y, P0.y, P1.y, P2.y, s, m);
             dual_update(N0.z, N1.z, N2.z, __fsub_rn(Zc.z, Zc.w), G1.z, G2.z, P0.z, P1.z, P2.z, s, m);
             dual_update(N0.w, N1.w, N2.w, gx3, G1.w, G2.w, P0.w, P1.w, P2.w, s, m);
-            stvq<VW>(p0 + i, P0);
-            stvq<VW>(p1 + i, P1);
-            stvq<VW>(p2 + i, P2);
-            stvq<VW>(o0 + i, N0);
-            stvq<VW>(o1 + i, N1);
-            stvq<VW>(o2 + i, N2);
+            stvq<VO>(q0 + io, P0);
+            stvq<VO>(q1 + io, P1);
+            stvq<VO>(q2 + io, P2);
+            stvq<VO>(o0 + io, N0);
+            stvq<VO>(o1 + io, N1);
+            stvq<VO>(o2 + io, N2);
+            if (PACK && z + 1 < ze) stq<4>(a.bo + io + szo, Bn);
         }
 
         R0c = R0n;

@@ -73,11 +73,17 @@ cudaError_t dev_alloc(T **ptr, size_t bytes)
 // The default vector variant chosen by AUTO.
 constexpr int kAutoVariant = TVFGP_VARIANT_ZMARCH2_TMA;
 
+// The parameter struct a kernel takes (checked against the one filled in
+// before every launch, so that a kernel id mapped differently by item_cfg
+// and fill_item fails instead of launching on the wrong struct).
+enum ArgKind { kArgStep, kArgStepH, kArgZmarch, kArgZmarchH, kArgCube, kArgPair, kArgPrimal, kArgDual };
+
 struct LaunchCfg {
     const void *func;
     dim3 grid;
     dim3 block;
     size_t smem;
+    int args = kArgStep;
 };
 
 // The copy of the final r back from the scratch dual: one contiguous copy of
@@ -220,12 +226,20 @@ constexpr int kKernZmarchH = 122;
 constexpr int kKernFused2 = 130;
 constexpr int kKernFusedP = 131;
 constexpr int kFused2BY = 4, kFused2ZC = 8;
+// The fused kernel's packing step: padded rows in, dense volumes out (the
+// first step of a packed run).
+constexpr int kKernPackStep = 132;
+// The two-step kernel writing p and r onto padded rows (the last launch of
+// a packed run).
+constexpr int kKernPairPadded = 133;
 
 // The public variant a kernel belongs to (what tvfgp_last_variant reports).
 int public_variant(int kernel)
 {
-    if (kernel == kKernFused2 || kernel == kKernFusedP || kernel == kKernFusedH) return TVFGP_VARIANT_FUSED;
+    if (kernel == kKernFused2 || kernel == kKernFusedP || kernel == kKernFusedH || kernel == kKernPackStep)
+        return TVFGP_VARIANT_FUSED;
     if (kernel == kKernScalarH) return TVFGP_VARIANT_SCALAR;
+    if (kernel == kKernPairPadded) return TVFGP_VARIANT_ZMARCH2_TMA;
     if (kernel == kKernZmarchH) return TVFGP_VARIANT_ZMARCH_TMA;
     if (kernel >= kKernPrimalZVec && kernel <= kKernDualZScalar) return TVFGP_VARIANT_SEPARATE;
     return kernel;
@@ -283,11 +297,13 @@ LaunchCfg step_cfg(const tvfgp_handle *h, int variant)
         c.block = dim3(zmarch_threads(), 1, 1);
         c.grid = zmarch_grid(h->zplan);
         c.smem = zmarch_smem_bytes();
+        c.args = kArgZmarch;
     } else if (variant == TVFGP_VARIANT_CUBE_TMA) {
         c.func = cube_kernel();
         c.block = dim3(cube_threads(), 1, 1);
         c.grid = cube_grid(h->nx, h->ny, h->nz);
         c.smem = cube_smem_bytes();
+        c.args = kArgCube;
     } else {
         c.func = reinterpret_cast<const void *>(&fgp_step_scalar<float>);
         c.block = dim3(32, 8, 1);
@@ -307,6 +323,13 @@ struct Item {
     const float *r_src;
     float *r_dst;
     float m0, m1;           // momentum weights of its step(s)
+    // launches of a packed run on padded rows (else left at their defaults):
+    const float *b = nullptr;   // this launch's b (nullptr: the run's)
+    float *b_out = nullptr;     // packing step: the dense copy of b
+    int ipx = 0;                // packing step: the inputs' row pitch ...
+    long long in_n = 0;         // ... and elements per volume
+    int opx = 0;                // two-step launch: the outputs' row pitch (0: dense) ...
+    long long out_n = 0;        // ... and elements per volume
 };
 
 // Kernel-argument storage for one launch of any kernel family.
@@ -322,21 +345,44 @@ struct KArgs {
     void *ptrs[1];
 };
 
+// The member of k that a kernel of ArgKind `kind` takes.
+const void *arg_slot(const KArgs &k, int kind)
+{
+    switch (kind) {
+    case kArgStep: return &k.a;
+    case kArgStepH: return &k.ah;
+    case kArgZmarch: return &k.za;
+    case kArgZmarchH: return &k.zah;
+    case kArgCube: return &k.cb;
+    case kArgPair: return &k.z2;
+    case kArgPrimal: return &k.pa;
+    case kArgDual: return &k.da;
+    }
+    return nullptr;
+}
+
 LaunchCfg item_cfg(const tvfgp_handle *h, int kernel)
 {
     if (kernel == kKernFusedH) {
         LaunchCfg c = step_cfg(h, TVFGP_VARIANT_FUSED);
         c.func = reinterpret_cast<const void *>(&fgp_step_fused4<kFusedBY, kFusedZC, __half>);
+        c.args = kArgStepH;
         return c;
     }
     if (kernel == kKernScalarH) {
         LaunchCfg c = step_cfg(h, TVFGP_VARIANT_SCALAR);
         c.func = reinterpret_cast<const void *>(&fgp_step_scalar<__half>);
+        c.args = kArgStepH;
         return c;
     }
     if (kernel == kKernFusedP) {
         LaunchCfg c = step_cfg(h, TVFGP_VARIANT_FUSED);
         c.func = reinterpret_cast<const void *>(&fgp_step_fused4<kFusedBY, kFusedZC, float, 2>);
+        return c;
+    }
+    if (kernel == kKernPackStep) {
+        LaunchCfg c = step_cfg(h, TVFGP_VARIANT_FUSED);
+        c.func = reinterpret_cast<const void *>(&fgp_step_fused4<kFusedBY, kFusedZC, float, 2, true>);
         return c;
     }
     if (kernel == kKernFused2) {
@@ -354,12 +400,14 @@ LaunchCfg item_cfg(const tvfgp_handle *h, int kernel)
         c.block = dim3(zmarch_threads<__half>(), 1, 1);
         c.grid = zmarch_grid(h->zplan_h);
         c.smem = zmarch_smem_bytes<__half>();
+        c.args = kArgZmarchH;
         return c;
     }
-    if (kernel >= kKernPrimalZVec) {
+    if (kernel >= kKernPrimalZVec && kernel <= kKernDualZScalar) {
         LaunchCfg c;
         c.smem = 0;
         c.block = dim3(32, 8, 1);
+        c.args = kernel <= kKernPrimalZScalar ? kArgPrimal : kArgDual;
         const bool vec = kernel == kKernPrimalZVec || kernel == kKernDualZVec;
         c.grid = vec ? dim3((h->nx / 4 + 31) / 32, (h->ny + 7) / 8, h->nz)
                      : dim3((h->nx + 31) / 32, (h->ny + 7) / 8, h->nz);
@@ -369,19 +417,38 @@ LaunchCfg item_cfg(const tvfgp_handle *h, int kernel)
         else c.func = reinterpret_cast<const void *>(&dual_from_z_scalar);
         return c;
     }
-    if (kernel == TVFGP_VARIANT_ZMARCH2_TMA) {
+    if (kernel == TVFGP_VARIANT_ZMARCH2_TMA || kernel == kKernPairPadded) {
         LaunchCfg c;
-        c.func = zmarch2_kernel();
+        c.func = zmarch2_kernel(kernel == kKernPairPadded);
         c.block = dim3(zmarch2_threads(), 1, 1);
         c.grid = h->z2plan.grid;
         c.smem = zmarch2_smem_bytes();
+        c.args = kArgPair;
+        return c;
+    }
+    if (kernel != TVFGP_VARIANT_FUSED && kernel != TVFGP_VARIANT_ZMARCH_TMA && kernel != TVFGP_VARIANT_CUBE_TMA &&
+        kernel != TVFGP_VARIANT_SCALAR) {
+        LaunchCfg c = step_cfg(h, TVFGP_VARIANT_SCALAR);
+        c.func = nullptr;                       // unknown kernel id: never launched
         return c;
     }
     return step_cfg(h, kernel);
 }
 
-bool fill_item(const tvfgp_handle *h, const Item &it, const float *b, float lam, KArgs &k)
+bool fill_item(const tvfgp_handle *h, const Item &it, const float *b_run, float lam, KArgs &k)
 {
+    const float *b = it.b ? it.b : b_run;
+    if (it.kernel == kKernPackStep) {
+        // reads (b, p, r) on padded rows, writes dense p', r and b
+        k.a = make_args(h, b, const_cast<float *>(it.p_src), it.r_src, it.r_dst, lam, it.m0);
+        k.a.px = it.ipx;
+        k.a.N = it.in_n;
+        k.a.po = it.p_dst;
+        k.a.bo = it.b_out;
+        k.a.No = h->N;
+        k.ptrs[0] = &k.a;
+        return it.b_out != nullptr && it.ipx >= h->nx && it.in_n > 0;
+    }
     if (it.kernel == kKernFusedH || it.kernel == kKernScalarH || it.kernel == kKernZmarchH) {
         // the dual buffers of a binary16 run travel as float* in an Item
         k.ah.b = b;
@@ -431,10 +498,14 @@ bool fill_item(const tvfgp_handle *h, const Item &it, const float *b, float lam,
         k.ptrs[0] = &k.da;
         return h->zscratch != nullptr;
     }
-    if (it.kernel == TVFGP_VARIANT_ZMARCH2_TMA) {
+    if (it.kernel == TVFGP_VARIANT_ZMARCH2_TMA || it.kernel == kKernPairPadded) {
         k.ptrs[0] = &k.z2;
-        return zmarch2_fill(h->z2plan, b, it.p_src, it.p_dst, it.r_src, it.r_dst, lam, step_of(lam),
-                            it.m0, it.m1, h->nx, h->ny, h->nz, h->N, h->d_err, k.z2);
+        const bool ok = zmarch2_fill(h->z2plan, b, it.p_src, it.p_dst, it.r_src, it.r_dst, lam, step_of(lam),
+                                     it.m0, it.m1, h->nx, h->ny, h->nz, h->N, h->d_err, k.z2);
+        if (it.kernel == TVFGP_VARIANT_ZMARCH2_TMA) return ok;
+        k.z2.opx = it.opx;
+        k.z2.No = it.out_n;
+        return ok && it.opx >= h->nx && it.opx % 2 == 0 && it.out_n > 0;
     }
     k.a = make_args(h, b, it.p_dst, it.r_src, it.r_dst, lam, it.m0);
     if (it.kernel == TVFGP_VARIANT_ZMARCH_TMA) {
@@ -509,7 +580,8 @@ int launch_item(tvfgp_handle *h, const Item &it, const float *b, float lam, cuda
 {
     const LaunchCfg c = item_cfg(h, it.kernel);
     KArgs k;
-    if (!fill_item(h, it, b, lam, k)) return TVFGP_ERR_CUDA;
+    if (!fill_item(h, it, b, lam, k) || c.func == nullptr || k.ptrs[0] != arg_slot(k, c.args))
+        return TVFGP_ERR_CUDA;
     cudaError_t e = cudaLaunchKernel(c.func, c.grid, c.block, k.ptrs, c.smem, st);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -536,8 +608,8 @@ void destroy_graph(GraphEntry &g)
 bool node_params(tvfgp_handle *h, const Item &it, const float *b, float lam, KArgs &ka,
                  cudaKernelNodeParams &kp)
 {
-    const bool ok = fill_item(h, it, b, lam, ka);
     const LaunchCfg c = item_cfg(h, it.kernel);
+    const bool ok = fill_item(h, it, b, lam, ka) && c.func != nullptr && ka.ptrs[0] == arg_slot(ka, c.args);
     kp.func = const_cast<void *>(c.func);
     kp.gridDim = c.grid;
     kp.blockDim = c.block;
@@ -722,6 +794,50 @@ cudaError_t repack(tvfgp_handle *h, float *dst, const float *src, size_t rows, b
     const size_t w = sizeof(float) * static_cast<size_t>(h->nx);
     return cudaMemcpy2DAsync(dst, sizeof(float) * dp, src, sizeof(float) * sp, w, rows, cudaMemcpyDeviceToDevice,
                              st);
+}
+
+// The launches of a packed run of n >= 2 steps on padded rows, on the dense
+// shadow handle sh: the packing step (step 1: padded b, p, r in; dense b, p',
+// r out), one single dense step when the rest is odd (so that the run ends
+// on a two-step launch), then two-step launches; the last one writes p and r
+// back onto the padded rows.  p and r alternate between the packed buffers
+// and the shadow's scratch.
+void plan_packed(const tvfgp_handle *h, const tvfgp_handle *sh, const float *b, float *p, float *r,
+                 const std::vector<double> &m, std::vector<Item> &items)
+{
+    const int n = static_cast<int>(m.size());
+    const size_t v = static_cast<size_t>(sh->N);
+    float *db = h->pk, *pa = h->pk + v, *ra = h->pk + 4 * v;
+    float *pb = sh->pair_scratch, *rb = sh->scratch;
+    items.clear();
+    Item first{kKernPackStep, p, pa, r, ra, static_cast<float>(m[0]), 0.0f};
+    first.b = b;
+    first.b_out = db;
+    first.ipx = h->px;
+    first.in_n = h->N;
+    items.push_back(first);
+    float *cp = pa, *cr = ra, *op = pb, *orr = rb;
+    int k = 1;
+    if ((n - 1) % 2 == 1) {
+        Item one{TVFGP_VARIANT_ZMARCH_TMA, cp, cp, cr, orr, static_cast<float>(m[1]), 0.0f};
+        one.b = db;
+        items.push_back(one);
+        std::swap(cr, orr);
+        k = 2;
+    }
+    for (; k + 1 < n; k += 2) {
+        const bool last = k + 2 >= n;
+        Item two{last ? kKernPairPadded : TVFGP_VARIANT_ZMARCH2_TMA, cp, last ? p : op, cr, last ? r : orr,
+                 static_cast<float>(m[k]), static_cast<float>(m[k + 1])};
+        two.b = db;
+        if (last) {
+            two.opx = h->px;
+            two.out_n = h->N;
+        }
+        items.push_back(two);
+        std::swap(cp, op);
+        std::swap(cr, orr);
+    }
 }
 
 }  // namespace
@@ -938,19 +1054,41 @@ int tvfgp_run(tvfgp_t h, const float *b, float *p, float *r, float lambda, int n
         return TVFGP_OK;
     }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    // Padded rows defeat the 16-byte accesses of the fastest kernels; a run
-    // long enough is cheaper as pack -> dense run -> unpack (26 volume moves
-    // against 13 per step saved at the dense kernels' speed).  The padding
+    // Padded rows defeat the 16-byte accesses and the TMA copies of the
+    // fastest kernels (a row of 2(nx/2+1) floats is not a multiple of 16
+    // bytes), so a run long enough goes through dense buffers.  With the
+    // two-step kernel the first step packs and the last launch unpacks; the
+    // other TMA variants pack, run and unpack (26 volume moves).  The padding
     // is never written.
     const bool packed_variant = h->variant == TVFGP_VARIANT_AUTO || h->variant == TVFGP_VARIANT_ZMARCH_TMA ||
                                 h->variant == TVFGP_VARIANT_ZMARCH2_TMA || h->variant == TVFGP_VARIANT_CUBE_TMA;
     if (!dense(h) && h->nx % 4 == 0 && nsteps >= kPackMinSteps && packed_variant &&
         ensure_shadow(h) == TVFGP_OK) {
         tvfgp_handle *sh = h->shadow;
-        if ((rc = tvfgp_set_variant(sh, h->variant)) || (rc = tvfgp_set_graph(sh, h->graph_on))) return rc;
         const size_t n = static_cast<size_t>(h->nx) * h->ny * h->nz;
         const size_t rows = static_cast<size_t>(h->ny) * h->nz;
         float *db = h->pk, *dp = h->pk + n, *dr = h->pk + 4 * n;
+        // two-step kernel: the packing is fused into the first step and the
+        // unpacking into the last launch
+        if ((h->variant == TVFGP_VARIANT_AUTO || h->variant == TVFGP_VARIANT_ZMARCH2_TMA) && nsteps >= 3 &&
+            sh->pair_scratch != nullptr && pair_rows(h) && aligned8(b) && aligned8(p) && aligned8(r) &&
+            zmarch_available()) {
+            std::vector<Item> items;
+            plan_packed(h, sh, b, p, r, m, items);
+            const long long before = sh->launches;
+            if (h->graph_on) {
+                rc = run_graph(sh, kKernPackStep, b, p, r, lambda, nsteps, t0, items, false, CopySpec(), st);
+            } else {
+                for (size_t k = 0; k < items.size() && rc == TVFGP_OK; ++k)
+                    rc = launch_item(sh, items[k], db, lambda, st);
+            }
+            if (rc != TVFGP_OK) return rc;
+            h->launches += sh->launches - before;
+            h->last_variant = TVFGP_VARIANT_ZMARCH2_TMA;
+            if (t_final) *t_final = tf;
+            return TVFGP_OK;
+        }
+        if ((rc = tvfgp_set_variant(sh, h->variant)) || (rc = tvfgp_set_graph(sh, h->graph_on))) return rc;
         cudaError_t e = repack(h, db, b, rows, true, st);
         if (e == cudaSuccess) e = repack(h, dp, p, 3 * rows, true, st);
         if (e == cudaSuccess) e = repack(h, dr, r, 3 * rows, true, st);

@@ -153,8 +153,13 @@ struct Zmarch2Args {
     long long N;
     int *err;
     int zc;                                         // output planes per CTA
+    int opx;                                        // row pitch of p_dst, r_dst (nx: dense)
+    long long No;                                   // their elements per component
 };
 
+// PADDED_OUT: p_dst and r_dst have rows of opx floats (even), written as
+// 8-byte halves of quads; else they are dense.
+template <bool PADDED_OUT>
 __global__ void __launch_bounds__(Z2_THREADS, TVFGP_Z2_MINB)
 fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
 {
@@ -285,8 +290,10 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     }
     __syncthreads();
 
-    float *p0d = za.p_dst, *p1d = za.p_dst + za.N, *p2d = za.p_dst + 2 * za.N;
-    float *r0d = za.r_dst, *r1d = za.r_dst + za.N, *r2d = za.r_dst + 2 * za.N;
+    const long long No = PADDED_OUT ? za.No : za.N;
+    const int opx = PADDED_OUT ? za.opx : nx;
+    float *p0d = za.p_dst, *p1d = za.p_dst + No, *p2d = za.p_dst + 2 * No;
+    float *r0d = za.r_dst, *r1d = za.r_dst + No, *r2d = za.r_dst + 2 * No;
     float4 cP0 = f4zero(), cP1 = f4zero(), cP2 = f4zero();   // p^{k+1} of plane q-1 (tile quads)
     float4 Z1c = f4zero();                                    // z^{k+1} of plane q-1 (tile quads)
 
@@ -402,13 +409,22 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
                 const float gx3 = (x + 3 < nx - 1) ? __fsub_rn(zc.w, zx) : 0.0f;
                 const float4 G0 = make_float4(__fsub_rn(zc.x, zc.y), __fsub_rn(zc.y, zc.z), __fsub_rn(zc.z, zc.w), gx3);
                 dual_update4(R0, R1, R2, G0, G1, G2, P0, P1, P2, s, m1);
-                const long long i = x + (long long)nx * (y + (long long)ny * qd);
-                st4(p0d + i, P0);
-                st4(p1d + i, P1);
-                st4(p2d + i, P2);
-                st4(r0d + i, R0);
-                st4(r1d + i, R1);
-                st4(r2d + i, R2);
+                const long long i = x + (long long)opx * (y + (long long)ny * qd);
+                if (!PADDED_OUT) {
+                    st4(p0d + i, P0);
+                    st4(p1d + i, P1);
+                    st4(p2d + i, P2);
+                    st4(r0d + i, R0);
+                    st4(r1d + i, R1);
+                    st4(r2d + i, R2);
+                } else {
+                    stq<2>(p0d + i, P0);
+                    stq<2>(p1d + i, P1);
+                    stq<2>(p2d + i, P2);
+                    stq<2>(r0d + i, R0);
+                    stq<2>(r1d + i, R1);
+                    stq<2>(r2d + i, R2);
+                }
             }
         }
         Z1c = Z1n;
@@ -451,8 +467,10 @@ inline int zmarch2_plan(int nx, int ny, int nz, Zmarch2Plan *plan)
     plan->grid = dim3(tx, ty, (nz + plan->zc - 1) / plan->zc);
     if (!zmarch_supported(nx, ny, nz)) return 0;
     if (zm_encoder() == nullptr) return 3;
-    const void *fn = reinterpret_cast<const void *>(&fgp_step2_zmarch_tma);
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Z2_SMEM) != cudaSuccess) {
+    const void *fn = reinterpret_cast<const void *>(&fgp_step2_zmarch_tma<false>);
+    const void *fn_padded = reinterpret_cast<const void *>(&fgp_step2_zmarch_tma<true>);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Z2_SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(fn_padded, cudaFuncAttributeMaxDynamicSharedMemorySize, Z2_SMEM) != cudaSuccess) {
         cudaGetLastError();
         return 3;
     }
@@ -468,11 +486,16 @@ inline int zmarch2_plan(int nx, int ny, int nz, Zmarch2Plan *plan)
     return 0;
 }
 
-inline const void *zmarch2_kernel() { return reinterpret_cast<const void *>(&fgp_step2_zmarch_tma); }
+inline const void *zmarch2_kernel(bool padded_out = false)
+{
+    return padded_out ? reinterpret_cast<const void *>(&fgp_step2_zmarch_tma<true>)
+                      : reinterpret_cast<const void *>(&fgp_step2_zmarch_tma<false>);
+}
 inline int zmarch2_threads() { return Z2_THREADS; }
 inline size_t zmarch2_smem_bytes() { return Z2_SMEM; }
 
-// Kernel arguments of one two-step launch.
+// Kernel arguments of one two-step launch (outputs dense; a caller that
+// writes padded rows sets opx and No afterwards).
 inline bool zmarch2_fill(const Zmarch2Plan &plan, const float *b, const float *p_src, float *p_dst,
                          const float *r_src, float *r_dst, float lam, float s, float m0, float m1,
                          int nx, int ny, int nz, long long N, int *err, Zmarch2Args &za)
@@ -489,6 +512,8 @@ inline bool zmarch2_fill(const Zmarch2Plan &plan, const float *b, const float *p
     za.N = N;
     za.err = err;
     za.zc = plan.zc;
+    za.opx = nx;
+    za.No = N;
     return zm_encode(&za.tb, b, nx, ny, nz, Z2_BW, Z2_HB) &&
            zm_encode(&za.tr0, r_src, nx, ny, nz, Z2_BW, Z2_HR) &&
            zm_encode(&za.tr1, r_src + N, nx, ny, nz, Z2_BW, Z2_HR) &&

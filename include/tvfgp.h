@@ -113,11 +113,15 @@ int tvfgp_create(int nx, int ny, int nz, tvfgp_t *out);
  * TVFGP_ERR_ARG.  Padded rows are in general not 16-byte aligned, so the
  * float4 and TMA kernels cannot read them in place.  A tvfgp_run of 4 or more
  * steps on a handle set to AUTO, ZMARCH_TMA, ZMARCH2_TMA or CUBE_TMA with
- * nx % 4 == 0 therefore packs b, p and r into dense buffers, runs the dense
- * kernels of that variant on them and unpacks p and r (last_variant reports
- * the dense variant); the handle then owns a dense handle and 7*nx*ny*nz
- * more floats, allocated on that first run (if that allocation fails the
- * run proceeds in place).  Other runs and tvfgp_step work in place: the
+ * nx % 4 == 0 therefore runs on dense buffers.  On AUTO and ZMARCH2_TMA
+ * (with b, p, r 8-byte aligned and an even pitch) the first step reads the
+ * padded rows and writes dense p, r and a dense copy of b, the dense
+ * two-step kernel runs the rest, and its last launch writes p and r back
+ * onto the padded rows.  The other variants pack b, p and r, run their
+ * dense kernels and unpack p and r.  last_variant reports the dense
+ * variant.  The handle then owns a dense handle (with its own scratch) and
+ * 7*nx*ny*nz more floats, allocated on that first run (if that allocation
+ * fails the run proceeds in place).  Other runs and tvfgp_step work in place: the
  * fused kernel on 8-byte halves of quads (or on pairs when nx % 4 == 2)
  * when nx and the pitch are even and b, p and r are 8-byte aligned
  * (last_variant reports FUSED), else the scalar kernel; SCALAR and SEPARATE

@@ -33,8 +33,9 @@ def dev(a):
 
 def pitched_variant(T, nx, pitch, variant="auto", nsteps=1):
     """What a pitched handle runs.  Runs of 4 or more steps with nx % 4 == 0
-    on AUTO and the TMA variants are packed into dense buffers and run by the
-    dense kernels; otherwise the fused kernel on 8-byte halves or pairs
+    on AUTO and the TMA variants go through dense buffers and are reported as
+    the dense kernel (on AUTO and ZMARCH2_TMA with an even pitch the first
+    step packs and the last launch unpacks); otherwise the fused kernel on 8-byte halves or pairs
     (reported as FUSED) when nx and the pitch are even, else the scalar
     kernel; SCALAR and SEPARATE handles keep theirs."""
     if nsteps >= 4 and nx % 4 == 0 and variant in ("auto", "zmarch", "zmarch2", "cube"):
@@ -67,7 +68,9 @@ def test_pitched_equals_dense_oracle(T, shape, pitch, graph):
     r0 = synth.random_dual(shape, 63, scale=0.6)
     bp, pp, rp = pad(b, pitch, 1), pad(p0, pitch, 2), pad(r0, pitch, 3)
     zp = pad(np.zeros_like(b), pitch, 4)
-    for nsteps in (0, 1, 2, 5, 6):
+    # 4 and 6: packing step, one dense step, two-step launches; 5: packing
+    # step and two-step launches only
+    for nsteps in (0, 1, 2, 4, 5, 6):
         p, r, z = dev(pp), dev(rp), dev(zp)
         with T.Tvfgp(nx, ny, nz, "auto", graph, pitch=pitch) as h:
             h.run(dev(bp), p, r, 0.07, nsteps, 1.0)
