@@ -99,8 +99,10 @@ enum tvfgp_variant {
 
 /* Create a handle for an nx x ny x nz volume on the current CUDA device.
  * Allocates the scratch dual buffer (3*nx*ny*nz floats) and a device error
- * word.  1 <= nx, ny, nz <= 65535 and nx*ny*nz <= 2^31 - 1, else
- * TVFGP_ERR_ARG.  *out receives the handle (NULL on failure). */
+ * word.  1 <= nx, ny, nz <= 65535 and nx*ny*(nz+1) <= 2^31 - 1 (the
+ * kernels index voxels in 32 bits, with one plane of headroom for the
+ * addresses of the next plane), else TVFGP_ERR_ARG: at most about 8.6 GB
+ * per volume.  *out receives the handle (NULL on failure). */
 int tvfgp_create(int nx, int ny, int nz, tvfgp_t *out);
 
 /* A handle for volumes whose rows are padded: element (x, y, z) of b, of z

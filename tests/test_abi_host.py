@@ -69,6 +69,12 @@ def test_create_rejects_bad_shapes_before_touching_cuda(T):
     assert T.raw_call("tvfgp_create_ex", 4, 4, 4, 7, 0, ctypes.byref(h)) == T.TVFGP_ERR_ARG
     assert T.raw_call("tvfgp_create_ex", 4, 4, 4, 0, 1, ctypes.byref(h)) == T.TVFGP_ERR_ARG
     assert T.raw_call("tvfgp_create", 4, 4, 4, None) == T.TVFGP_ERR_ARG
+    # the size limit, nx*ny*(nz+1) <= 2^31 - 1, at its boundary
+    assert T.raw_call("tvfgp_create", 1024, 1024, 2047, ctypes.byref(h)) == T.TVFGP_ERR_ARG
+    rc = T.raw_call("tvfgp_create", 1024, 1024, 2046, ctypes.byref(h))
+    assert rc != T.TVFGP_ERR_ARG
+    if rc == T.TVFGP_OK:
+        T.raw_call("tvfgp_destroy", h)
 
 
 def test_calls_on_a_null_handle(T):
