@@ -394,8 +394,11 @@ __device__ __forceinline__ float4 zquad(float4 B, float4 R0, float4 R1, float4 R
 #ifndef TVFGP_FUSED_MINB
 #define TVFGP_FUSED_MINB 5
 #endif
-template <int BY, int ZC, typename TS = float, int VW = 4, bool PACK = false>
-__global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(const StepArgsT<TS> a)
+// IT: the voxel index type, int unless px*ny*(nz+1) exceeds its range (the
+// 64-bit instance runs one block per SM fewer, so that it does not spill).
+template <int BY, int ZC, typename TS = float, int VW = 4, bool PACK = false, typename IT = int>
+__global__ void __launch_bounds__(32 * BY, sizeof(IT) == 4 ? TVFGP_FUSED_MINB : TVFGP_FUSED_MINB - 1)
+fgp_step_fused4(const StepArgsT<TS> a)
 {
     static_assert(!PACK || (VW == 2 && sizeof(TS) == 4), "packing reads padded fp32 rows");
     const int lane = threadIdx.x;
@@ -430,8 +433,8 @@ __global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(con
     const int szo = PACK ? nx * ny : px * ny;
 
     int z = zb;
-    int i = x0 + px * (y + ny * z);
-    int io = PACK ? x0 + nx * (y + ny * z) : i;
+    IT i = x0 + (IT)px * (y + (IT)ny * z);
+    IT io = PACK ? x0 + (IT)nx * (y + (IT)ny * z) : i;
 
     // prologue: own r at plane zb and z(i) there
     float4 R0c = f4zero(), R1c = f4zero(), R2c = f4zero(), Zc;
@@ -499,7 +502,7 @@ __global__ void __launch_bounds__(32 * BY, TVFGP_FUSED_MINB) fgp_step_fused4(con
         // z(i+ex) of the last voxel: the next lane's first z
         float zx = __shfl_down_sync(kFull, Zc.x, 1);
         if (lane == 31 && x0 + 4 < nx) {
-            const int j = i + 4;
+            const IT j = i + 4;
             const float d0 = __fsub_rn(ld1_ro(r0 + j), R0c.w);
             const float d1 = __fsub_rn(ld1_ro(r1 + j), y > 0 ? ld1_ro(r1 + j - px) : 0.0f);
             const float d2 = __fsub_rn(ld1_ro(r2 + j), z > 0 ? ld1_ro(r2 + j - sz) : 0.0f);
@@ -761,7 +764,7 @@ __global__ void __launch_bounds__(32 * BY) primal_vec4(const PrimalArgsT<TS> a)
     if (y >= ny) return;
     const bool xin = x0 < nx;
     const int sz = nx * ny;
-    const int i = x0 + nx * (y + ny * z);
+    const long long i = x0 + (long long)nx * (y + (long long)ny * z);
     const TS *d0 = a.d, *d1 = a.d + a.N, *d2 = a.d + 2 * a.N;
     float4 B = f4zero(), D0 = f4zero(), D1 = f4zero(), D2 = f4zero(), D1lo = f4zero(), D2lo = f4zero();
     if (xin) {
@@ -821,7 +824,7 @@ __global__ void __launch_bounds__(32 * BY) dual_from_z_vec4(const DualArgs a)
     if (y >= ny) return;                         // whole warp: y is warp-uniform
     const bool xin = x0 < nx;
     const int sz = nx * ny;
-    const int i = x0 + nx * (y + ny * z);
+    const long long i = x0 + (long long)nx * (y + (long long)ny * z);
     const bool hasY = y + 1 < ny, hasZ = z + 1 < nz;
     float4 P0 = f4zero(), P1 = f4zero(), P2 = f4zero(), R0 = f4zero(), R1 = f4zero(), R2 = f4zero();
     float4 Zc = f4zero(), ZY = f4zero(), ZZ = f4zero();

@@ -283,12 +283,26 @@ StepArgs make_args(const tvfgp_handle *h, const float *b, float *p, const float 
     return a;
 }
 
+// Volumes whose voxel addresses (with one plane of headroom) leave the int
+// range run the 64-bit-indexed instances of the fused kernel.
+bool wide(const tvfgp_handle *h)
+{
+    return static_cast<long long>(h->px) * h->ny * (static_cast<long long>(h->nz) + 1) > INT_MAX;
+}
+
+template <typename TS, int VW, bool PACK>
+const void *fused_kernel(const tvfgp_handle *h)
+{
+    return wide(h) ? reinterpret_cast<const void *>(&fgp_step_fused4<kFusedBY, kFusedZC, TS, VW, PACK, long long>)
+                   : reinterpret_cast<const void *>(&fgp_step_fused4<kFusedBY, kFusedZC, TS, VW, PACK, int>);
+}
+
 LaunchCfg step_cfg(const tvfgp_handle *h, int variant)
 {
     LaunchCfg c;
     c.smem = 0;
     if (variant == TVFGP_VARIANT_FUSED) {
-        c.func = reinterpret_cast<const void *>(&fgp_step_fused4<kFusedBY, kFusedZC>);
+        c.func = fused_kernel<float, 4, false>(h);
         c.block = dim3(32, kFusedBY, 1);
         c.grid = dim3((h->nx / 4 + 31) / 32, (h->ny + kFusedBY - 1) / kFusedBY,
                       (h->nz + kFusedZC - 1) / kFusedZC);
@@ -365,7 +379,7 @@ LaunchCfg item_cfg(const tvfgp_handle *h, int kernel)
 {
     if (kernel == kKernFusedH) {
         LaunchCfg c = step_cfg(h, TVFGP_VARIANT_FUSED);
-        c.func = reinterpret_cast<const void *>(&fgp_step_fused4<kFusedBY, kFusedZC, __half>);
+        c.func = fused_kernel<__half, 4, false>(h);
         c.args = kArgStepH;
         return c;
     }
@@ -377,12 +391,12 @@ LaunchCfg item_cfg(const tvfgp_handle *h, int kernel)
     }
     if (kernel == kKernFusedP) {
         LaunchCfg c = step_cfg(h, TVFGP_VARIANT_FUSED);
-        c.func = reinterpret_cast<const void *>(&fgp_step_fused4<kFusedBY, kFusedZC, float, 2>);
+        c.func = fused_kernel<float, 2, false>(h);
         return c;
     }
     if (kernel == kKernPackStep) {
         LaunchCfg c = step_cfg(h, TVFGP_VARIANT_FUSED);
-        c.func = reinterpret_cast<const void *>(&fgp_step_fused4<kFusedBY, kFusedZC, float, 2, true>);
+        c.func = fused_kernel<float, 2, true>(h);
         return c;
     }
     if (kernel == kKernFused2) {
@@ -879,7 +893,7 @@ static int create_impl(int nx, int ny, int nz, int px, int variant, unsigned fla
     *out = nullptr;
     if (nx < 1 || ny < 1 || nz < 1 || nx > 65535 || ny > 65535 || nz > 65535) return TVFGP_ERR_ARG;
     if (px < nx || px > 65535) return TVFGP_ERR_ARG;
-    if (static_cast<long long>(px) * ny * (static_cast<long long>(nz) + 1) > INT_MAX) return TVFGP_ERR_ARG;
+    if (static_cast<long long>(px) * ny > INT_MAX) return TVFGP_ERR_ARG;     // a plane, in 32 bits
     if (variant < TVFGP_VARIANT_AUTO || variant > TVFGP_VARIANT_CUBE_TMA || flags != 0)
         return TVFGP_ERR_ARG;
     if ((variant == TVFGP_VARIANT_ZMARCH_TMA || variant == TVFGP_VARIANT_ZMARCH2_TMA ||

@@ -99,10 +99,13 @@ enum tvfgp_variant {
 
 /* Create a handle for an nx x ny x nz volume on the current CUDA device.
  * Allocates the scratch dual buffer (3*nx*ny*nz floats) and a device error
- * word.  1 <= nx, ny, nz <= 65535 and nx*ny*(nz+1) <= 2^31 - 1 (the
- * kernels index voxels in 32 bits, with one plane of headroom for the
- * addresses of the next plane), else TVFGP_ERR_ARG: at most about 8.6 GB
- * per volume.  *out receives the handle (NULL on failure). */
+ * word.  1 <= nx, ny, nz <= 65535 and a plane nx*ny <= 2^31 - 1, else
+ * TVFGP_ERR_ARG; the volume is bounded only by device memory.  Voxels are
+ * indexed in 64 bits where nx*ny*(nz+1) exceeds 2^31 - 1 (the TMA kernels
+ * always; the fused kernel through its 64-bit instance), so a run on a
+ * volume of several G voxels fits the 288 GB of HBM (b, p, r and the
+ * two-step path's 12 scratch volumes: 76 bytes per voxel).  *out receives
+ * the handle (NULL on failure). */
 int tvfgp_create(int nx, int ny, int nz, tvfgp_t *out);
 
 /* A handle for volumes whose rows are padded: element (x, y, z) of b, of z

@@ -63,18 +63,20 @@ def test_momentum_schedule_matches_oracle(T):
 
 def test_create_rejects_bad_shapes_before_touching_cuda(T):
     h = ctypes.c_void_p()
-    for dims in ((0, 4, 4), (4, -1, 4), (4, 4, 0), (70000, 1, 1), (2048, 2048, 1024)):
+    for dims in ((0, 4, 4), (4, -1, 4), (4, 4, 0), (70000, 1, 1), (65535, 65535, 1)):
         assert T.raw_call("tvfgp_create", *dims, ctypes.byref(h)) == T.TVFGP_ERR_ARG
         assert h.value is None
     assert T.raw_call("tvfgp_create_ex", 4, 4, 4, 7, 0, ctypes.byref(h)) == T.TVFGP_ERR_ARG
     assert T.raw_call("tvfgp_create_ex", 4, 4, 4, 0, 1, ctypes.byref(h)) == T.TVFGP_ERR_ARG
     assert T.raw_call("tvfgp_create", 4, 4, 4, None) == T.TVFGP_ERR_ARG
-    # the size limit, nx*ny*(nz+1) <= 2^31 - 1, at its boundary
-    assert T.raw_call("tvfgp_create", 1024, 1024, 2047, ctypes.byref(h)) == T.TVFGP_ERR_ARG
-    rc = T.raw_call("tvfgp_create", 1024, 1024, 2046, ctypes.byref(h))
-    assert rc != T.TVFGP_ERR_ARG
-    if rc == T.TVFGP_OK:
-        T.raw_call("tvfgp_destroy", h)
+    # the size limit, a plane nx*ny <= 2^31 - 1, at its boundary; the volume
+    # itself is bounded by device memory only (a GPU would allocate here)
+    assert T.raw_call("tvfgp_create", 65535, 32769, 1, ctypes.byref(h)) == T.TVFGP_ERR_ARG
+    for dims in ((65535, 32768, 1), (2048, 1024, 1025)):
+        rc = T.raw_call("tvfgp_create", *dims, ctypes.byref(h))
+        assert rc != T.TVFGP_ERR_ARG
+        if rc == T.TVFGP_OK:
+            T.raw_call("tvfgp_destroy", h)
 
 
 def test_calls_on_a_null_handle(T):
