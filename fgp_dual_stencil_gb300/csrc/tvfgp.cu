@@ -854,6 +854,24 @@ void plan_packed(const tvfgp_handle *h, const tvfgp_handle *sh, const float *b, 
     }
 }
 
+// How a run of nsteps goes on handle h with these buffers: directly on the
+// handle's kernels, or through dense buffers (the padded-row runs), either
+// with the packing folded into the first step and the unpacking into the
+// last two-step launch, or with copies around a dense run.  tma: the TMA
+// encoder is available.
+enum RunRoute { kRouteDirect = 0, kRoutePackFused = 1, kRoutePackCopy = 2 };
+
+RunRoute run_route(const tvfgp_handle *h, const float *b, const float *p, const float *r, int nsteps, bool tma)
+{
+    const bool packed_variant = h->variant == TVFGP_VARIANT_AUTO || h->variant == TVFGP_VARIANT_ZMARCH_TMA ||
+                                h->variant == TVFGP_VARIANT_ZMARCH2_TMA || h->variant == TVFGP_VARIANT_CUBE_TMA;
+    if (dense(h) || h->nx % 4 != 0 || nsteps < kPackMinSteps || !packed_variant) return kRouteDirect;
+    if ((h->variant == TVFGP_VARIANT_AUTO || h->variant == TVFGP_VARIANT_ZMARCH2_TMA) && nsteps >= 3 &&
+        pair_rows(h) && aligned8(b) && aligned8(p) && aligned8(r) && tma)
+        return kRoutePackFused;
+    return kRoutePackCopy;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1074,19 +1092,15 @@ int tvfgp_run(tvfgp_t h, const float *b, float *p, float *r, float lambda, int n
     // two-step kernel the first step packs and the last launch unpacks; the
     // other TMA variants pack, run and unpack (26 volume moves).  The padding
     // is never written.
-    const bool packed_variant = h->variant == TVFGP_VARIANT_AUTO || h->variant == TVFGP_VARIANT_ZMARCH_TMA ||
-                                h->variant == TVFGP_VARIANT_ZMARCH2_TMA || h->variant == TVFGP_VARIANT_CUBE_TMA;
-    if (!dense(h) && h->nx % 4 == 0 && nsteps >= kPackMinSteps && packed_variant &&
-        ensure_shadow(h) == TVFGP_OK) {
+    const RunRoute route = run_route(h, b, p, r, nsteps, zmarch_available());
+    if (route != kRouteDirect && ensure_shadow(h) == TVFGP_OK) {
         tvfgp_handle *sh = h->shadow;
         const size_t n = static_cast<size_t>(h->nx) * h->ny * h->nz;
         const size_t rows = static_cast<size_t>(h->ny) * h->nz;
         float *db = h->pk, *dp = h->pk + n, *dr = h->pk + 4 * n;
         // two-step kernel: the packing is fused into the first step and the
         // unpacking into the last launch
-        if ((h->variant == TVFGP_VARIANT_AUTO || h->variant == TVFGP_VARIANT_ZMARCH2_TMA) && nsteps >= 3 &&
-            sh->pair_scratch != nullptr && pair_rows(h) && aligned8(b) && aligned8(p) && aligned8(r) &&
-            zmarch_available()) {
+        if (route == kRoutePackFused && sh->pair_scratch != nullptr) {
             std::vector<Item> items;
             plan_packed(h, sh, b, p, r, m, items);
             const long long before = sh->launches;
@@ -1358,6 +1372,88 @@ int tvfgp_debug_fail_allocs(int skip, int count)
     std::lock_guard<std::mutex> lock(g_alloc_mutex);
     g_alloc_skip = count > 0 ? skip : 0;
     g_alloc_fail = count;
+    return TVFGP_OK;
+}
+
+int tvfgp_debug_plan(int nx, int ny, int nz, int pitch, int variant, int nsteps, double t0, int *route,
+                     int *copy_back, int *items, float *m_out, int cap, int *count)
+{
+    const int px = pitch == 0 ? nx : pitch;
+    if (nx < 1 || ny < 1 || nz < 1 || nx > 65535 || ny > 65535 || nz > 65535 || px < nx || px > 65535 ||
+        static_cast<long long>(px) * ny > INT_MAX)
+        return TVFGP_ERR_ARG;
+    if (variant < TVFGP_VARIANT_AUTO || variant > TVFGP_VARIANT_CUBE_TMA || nsteps < 0 || !std::isfinite(t0) ||
+        t0 < 1.0 || cap < 0 || route == nullptr || copy_back == nullptr || count == nullptr ||
+        (cap > 0 && (items == nullptr || m_out == nullptr)))
+        return TVFGP_ERR_ARG;
+    // Handles that are never used for CUDA: their buffers are distinct
+    // addresses that name the roles, never dereferenced.
+    auto fake = [](int role) { return reinterpret_cast<float *>(static_cast<uintptr_t>(role + 1) << 56); };
+    const long long nd = static_cast<long long>(nx) * ny * nz;
+    tvfgp_handle h{}, sh{};
+    h.nx = sh.nx = nx;
+    h.ny = sh.ny = ny;
+    h.nz = sh.nz = nz;
+    h.px = px;
+    sh.px = nx;
+    h.N = static_cast<long long>(px) * ny * nz;
+    sh.N = nd;
+    h.variant = variant;
+    sh.variant = variant;
+    const bool want_pairs = variant == TVFGP_VARIANT_ZMARCH2_TMA ||
+                            (variant == TVFGP_VARIANT_AUTO && kAutoVariant == TVFGP_VARIANT_ZMARCH2_TMA);
+    h.scratch = fake(3);
+    h.pair_scratch = want_pairs && nx % 4 == 0 && px == nx ? fake(4) : nullptr;
+    h.pk = fake(7);
+    sh.scratch = fake(10);
+    sh.pair_scratch = nx % 4 == 0 ? fake(11) : nullptr;
+    float *b = fake(0), *p = fake(1), *r = fake(2);
+    std::vector<double> m(static_cast<size_t>(nsteps));
+    tvfgp_momentum(t0, nsteps, m.data(), nullptr);
+    std::vector<Item> plan;
+    bool cb = false;
+    const RunRoute rt = nsteps == 0 ? kRouteDirect : run_route(&h, b, p, r, nsteps, true);
+    if (nsteps == 0) {
+    } else if (rt == kRoutePackFused) {
+        plan_packed(&h, &sh, b, p, r, m, plan);
+    } else if (rt == kRoutePackCopy) {
+        float *dp = h.pk + nd, *dr = h.pk + 4 * nd;
+        const int v = resolve_variant(&sh, sh.variant, nx % 4 == 0, false);
+        plan_run(&sh, v, nx % 4 == 0, dp, dr, m, plan, &cb);
+    } else {
+        const bool vec_ok = dense(&h) && nx % 4 == 0;
+        const int v = resolve_variant(&h, h.variant, vec_ok, pair_rows(&h));
+        plan_run(&h, v, vec_ok, p, r, m, plan, &cb);
+    }
+    // roles: 0 b, 1 p, 2 r (the caller's), 3 scratch dual, 4..6 the pair
+    // scratch's three dual sets, 7..9 packed b, p, r, 10 the dense handle's
+    // scratch dual, 11..13 its pair scratch's dual sets
+    const float *base[14] = {b, p, r, h.scratch, fake(4), fake(4) + 3 * h.N, fake(4) + 6 * h.N, h.pk, h.pk + nd,
+                             h.pk + 4 * nd, sh.scratch, fake(11), fake(11) + 3 * nd, fake(11) + 6 * nd};
+    auto role = [&](const float *q) {
+        if (q == nullptr) return -1;
+        for (int k = 0; k < 14; ++k)
+            if (q == base[k]) return k;
+        return -2;
+    };
+    *route = static_cast<int>(rt);
+    *copy_back = cb ? 1 : 0;
+    *count = static_cast<int>(plan.size());
+    for (size_t k = 0; k < plan.size() && static_cast<int>(k) < cap; ++k) {
+        const Item &it = plan[k];
+        int *o = items + 7 * k;
+        o[0] = public_variant(it.kernel);
+        o[1] = it.b ? role(it.b) : (rt == kRoutePackCopy ? 7 : 0);
+        o[2] = role(it.p_src);
+        o[3] = role(it.p_dst);
+        o[4] = role(it.r_src);
+        o[5] = role(it.r_dst);
+        o[6] = (it.kernel == TVFGP_VARIANT_ZMARCH2_TMA || it.kernel == kKernPairPadded ? 1 : 0) |
+               (it.kernel == kKernPackStep ? 2 : 0) | (it.kernel == kKernPairPadded ? 4 : 0) |
+               (it.kernel >= kKernPrimalZVec && it.kernel <= kKernDualZScalar ? 8 : 0);
+        m_out[2 * k] = it.m0;
+        m_out[2 * k + 1] = it.m1;
+    }
     return TVFGP_OK;
 }
 

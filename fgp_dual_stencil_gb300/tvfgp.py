@@ -69,6 +69,8 @@ def _load():
         "tvfgp_launch_count": ([vp], ll),
         "tvfgp_debug_timeout_probe": ([vp, i, vp], i),
         "tvfgp_debug_fail_allocs": ([i, i], i),
+        "tvfgp_debug_plan": ([i, i, i, i, i, i, d, ctypes.POINTER(i), ctypes.POINTER(i), ctypes.POINTER(i),
+                              ctypes.POINTER(f), i, ctypes.POINTER(i)], i),
         "tvfgp_debug_projection_check": ([i, ctypes.c_ulonglong, ctypes.c_ulonglong, vp, vp], i),
         "tvfgp_run_noalloc": ([i, i, i, vp, vp, vp, f, i, d, vp, ctypes.POINTER(d)], i),
         "tvfgp_host_alloc": ([ctypes.c_size_t, i, ctypes.POINTER(vp)], i),
@@ -260,6 +262,26 @@ def tvfgp_debug_fail_allocs(skip: int, count: int) -> None:
     """Let the library's next `skip` device allocations succeed and fail the
     `count` after them (test hook; count = 0 clears it)."""
     _ok(_lib.tvfgp_debug_fail_allocs(int(skip), int(count)), "tvfgp_debug_fail_allocs")
+
+
+def tvfgp_debug_plan(nx: int, ny: int, nz: int, pitch: int = 0, variant: int | str = TVFGP_VARIANT_AUTO,
+                     nsteps: int = 1, t0: float = 1.0):
+    """The launches tvfgp_run would enqueue (host only, no GPU): returns
+    (route, copy_back, launches), each launch a dict with the variant, the
+    buffer roles of b, p_src, p_dst, r_src, r_dst, its flags and its two
+    momentum weights (see tvfgp.h)."""
+    v = VARIANTS[variant] if isinstance(variant, str) else int(variant)
+    route, copy_back, count = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _ok(_lib.tvfgp_debug_plan(nx, ny, nz, pitch, v, nsteps, float(t0), ctypes.byref(route),
+                              ctypes.byref(copy_back), None, None, 0, ctypes.byref(count)), "tvfgp_debug_plan")
+    n = count.value
+    items = (ctypes.c_int * max(7 * n, 1))()
+    m = (ctypes.c_float * max(2 * n, 1))()
+    _ok(_lib.tvfgp_debug_plan(nx, ny, nz, pitch, v, nsteps, float(t0), ctypes.byref(route),
+                              ctypes.byref(copy_back), items, m, n, ctypes.byref(count)), "tvfgp_debug_plan")
+    keys = ("variant", "b", "p_src", "p_dst", "r_src", "r_dst", "flags")
+    launches = [dict(zip(keys, items[7 * k:7 * k + 7]), m=(m[2 * k], m[2 * k + 1])) for k in range(n)]
+    return route.value, bool(copy_back.value), launches
 
 
 def tvfgp_debug_timeout_probe(h: int, spins: int, stream=None) -> None:

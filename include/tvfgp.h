@@ -248,6 +248,25 @@ int tvfgp_debug_timeout_probe(tvfgp_t h, int spins, tvfgp_stream_t stream);
  * the hook.  Process-wide.  skip or count < 0: TVFGP_ERR_ARG. */
 int tvfgp_debug_fail_allocs(int skip, int count);
 
+/* Host only, no CUDA call: the launches that tvfgp_run would enqueue for a
+ * run of nsteps from t0 on a handle of this shape, row pitch (0: dense) and
+ * variant, given 16-byte aligned b, p, r, an available TMA encoder and
+ * scratch allocations that succeed.  *route: 0 the handle's own kernels,
+ * 1 a packing step and two-step launches on dense buffers (padded rows), 2
+ * copies into dense buffers around a dense run and back.  *copy_back: 1 if
+ * the final r is copied back from the scratch dual.  *count: the number of
+ * launches; the first min(count, cap) are written as 7 ints each to items,
+ * [variant, b, p_src, p_dst, r_src, r_dst, flags], and their momentum
+ * weights as 2 floats each (the second one of two-step launches) to m.
+ * Buffer roles: 0 b, 1 p, 2 r (the caller's), 3 the handle's scratch dual,
+ * 4-6 the three dual sets of its two-step scratch, 7-9 the packed b, p and
+ * r, 10 the dense handle's scratch dual, 11-13 its two-step scratch's dual
+ * sets, -1 none.  flags: 1 two steps, 2 reads padded rows and writes dense
+ * ones (packing step), 4 writes padded rows, 8 half of a two-kernel step.
+ * Invalid shapes or arguments: TVFGP_ERR_ARG. */
+int tvfgp_debug_plan(int nx, int ny, int nz, int pitch, int variant, int nsteps, double t0, int *route,
+                     int *copy_back, int *items, float *m, int cap, int *count);
+
 /* Self-check of the step kernels' projection onto the unit ball, which
  * evaluates q / max(1, |q|) with a hardware square-root estimate and fused
  * multiply-add corrections instead of IEEE square root and division, and
