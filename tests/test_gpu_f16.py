@@ -104,6 +104,33 @@ def test_f16_kernels_agree_bitwise(T, variant):
         assert np.array_equal(bits(p), ph) and np.array_equal(bits(r), rh), (variant, graph)
 
 
+@pytest.mark.parametrize("variant", ["auto", "fused", "scalar"])
+@pytest.mark.parametrize("lam", [0.05, 1e-17, 1e4])
+def test_f16_subnormal_and_extreme_codes(T, variant, lam):
+    """Stored duals drawn from every binary16 subnormal code, both signed
+    zeros, +-1, the smallest normal and +-65504, with half of b negative (z
+    clamps to 0) and the rest tiny; the results are full of binary16
+    subnormals.  lam = 1e-17 sends the projection to its IEEE fallback."""
+    shape = (48, 13, 9)
+    nx, ny, nz = shape
+    g = np.random.default_rng(7)
+    sub = np.arange(1, 1024, dtype=np.uint16)
+    codes = np.concatenate([sub, sub | 0x8000, np.uint16([0x7bff, 0xfbff, 0x3c00, 0xbc00, 0x0400, 0x8400, 0, 0x8000])])
+    p0 = g.choice(codes, size=(3, nz, ny, nx)).astype(np.uint16)
+    r0 = g.choice(codes, size=(3, nz, ny, nx)).astype(np.uint16)
+    b = np.where(g.uniform(size=(nz, ny, nx)) < 0.5, -1.0, g.uniform(0, 1e-4, (nz, ny, nx))).astype(np.float32)
+    ph, rh = p0.copy(), r0.copy()
+    oracle.fgp_run_h16(b, ph, rh, lam, 5, 1.0)
+    p, r = dev16(p0), dev16(r0)
+    with T.Tvfgp(*shape, variant) as h:
+        h.run_f16(dev(b), p, r, lam, 5, 1.0)
+        z = h.primal_f16(dev(b), p, lam)
+        assert h.check() == 0
+    assert np.array_equal(bits(p), ph) and np.array_equal(bits(r), rh), (variant, lam)
+    zo = oracle.primal_h16(b, ph, lam)
+    assert np.array_equal(z.cpu().numpy().view(np.uint32), zo.view(np.uint32)), (variant, lam)
+
+
 def test_f16_march_misaligned_falls_back(T):
     """A dual whose base is 8- but not 16-byte aligned cannot feed the
     tensor maps: the fused kernel runs, with the same bits."""
