@@ -63,6 +63,9 @@ namespace tvfgp {
 #ifndef TVFGP_Z2_WAVES
 #define TVFGP_Z2_WAVES 2          // fewest waves of CTAs over the resident slots
 #endif
+#ifndef TVFGP_Z2_TAPER
+#define TVFGP_Z2_TAPER 1          // the last chunk of planes split in 3 (1), 2 (2) or kept (0)
+#endif
 #ifndef TVFGP_Z2_EDGE_SPLIT
 #define TVFGP_Z2_EDGE_SPLIT 1     // boundary tests in step k only in CTAs that touch a face
 #endif
@@ -152,7 +155,9 @@ struct Zmarch2Args {
     int nx, ny, nz;
     long long N;
     int *err;
-    int zc;                                         // output planes per CTA
+    int zc;                                         // output planes per CTA ...
+    int nbig;                                       // ... for blockIdx.z < nbig; then the
+    int tap[4];                                     // pieces [tap[j], tap[j+1]) after nbig*zc
     int opx;                                        // row pitch of p_dst, r_dst (nx: dense)
     long long No;                                   // their elements per component
 };
@@ -174,8 +179,10 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     const int nx = za.nx, ny = za.ny, nz = za.nz;
     const int tid = threadIdx.x;
     const int x0 = blockIdx.x * Z2_TX, y0 = blockIdx.y * Z2_TY;
-    const int z0 = blockIdx.z * za.zc;
-    const int ze = min(z0 + za.zc, nz);        // output planes [z0, ze)
+    const int jz = blockIdx.z;
+    const int zbase = jz < za.nbig ? 0 : za.nbig * za.zc;
+    const int z0 = jz < za.nbig ? jz * za.zc : zbase + za.tap[jz - za.nbig];
+    const int ze = min(jz < za.nbig ? z0 + za.zc : zbase + za.tap[jz - za.nbig + 1], nz);   // output planes [z0, ze)
     const int f = max(z0 - 1, 0);              // first plane of step k
     const int uk_last = min(ze, nz - 1);       // last plane of step k (and of z^{k+1})
     const int last = min(ze + 1, nz - 1);      // last staged plane (z^k of plane ze+1)
@@ -455,16 +462,53 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
 // host side
 // ---------------------------------------------------------------------------
 
+// Planes per CTA: zc for z-chunks 0..nbig-1.  CTAs start in blockIdx
+// order, z-chunk last, so the last chunk's CTAs set the launch's tail.  When
+// the last round of CTAs over the resident slots is less than half full (the
+// GPU idles for most of a CTA's time), the last chunk is cut into shorter
+// pieces (tap): 512^3 with 64-plane chunks runs 12.07 rounds, and its
+// launches get 1.7% shorter; fuller last rounds lose more to the pieces'
+// prologues than the tail costs.
 struct Zmarch2Plan {
     dim3 grid;
     int zc;
+    int nbig;
+    int tap[4];
 };
+
+inline void zmarch2_chunks(int nz, long long tiles_xy, long long slots, Zmarch2Plan *plan)
+{
+    const int zc = plan->zc;
+    const int chunks = (nz + zc - 1) / zc;
+    const int last = nz - (chunks - 1) * zc;
+    plan->nbig = chunks;
+    plan->tap[0] = 0;
+    plan->tap[1] = plan->tap[2] = plan->tap[3] = 0;
+    const long long ctas = tiles_xy * chunks;
+    const bool ragged = slots > 0 && (ctas % slots) * 2 < slots;
+    int pieces = 0;
+    if (!ragged) {
+    } else if (TVFGP_Z2_TAPER == 1 && chunks > 1 && last >= 24) {
+        const int a = (last + 1) / 2, b2 = (last - a + 1) / 2;
+        plan->tap[1] = a;
+        plan->tap[2] = a + b2;
+        plan->tap[3] = last;
+        pieces = 3;
+    } else if (TVFGP_Z2_TAPER == 2 && chunks > 1 && last >= 16) {
+        plan->tap[1] = (last + 1) / 2;
+        plan->tap[2] = last;
+        pieces = 2;
+    }
+    if (pieces > 0) plan->nbig = chunks - 1;
+    plan->grid.z = plan->nbig + pieces;
+}
 
 inline int zmarch2_plan(int nx, int ny, int nz, Zmarch2Plan *plan)
 {
     const int tx = (nx + Z2_TX - 1) / Z2_TX, ty = (ny + Z2_TY - 1) / Z2_TY;
     plan->zc = 32;
     plan->grid = dim3(tx, ty, (nz + plan->zc - 1) / plan->zc);
+    zmarch2_chunks(nz, 0, 0, plan);
     if (!zmarch_supported(nx, ny, nz)) return 0;
     if (zm_encoder() == nullptr) return 3;
     const void *fn = reinterpret_cast<const void *>(&fgp_step2_zmarch_tma<false>);
@@ -481,8 +525,10 @@ inline int zmarch2_plan(int nx, int ny, int nz, Zmarch2Plan *plan)
         cudaGetLastError();
         return 3;
     }
-    plan->zc = zmarch_pick_zc(tx * ty, nz, sms * (per_sm > 0 ? per_sm : 1), TVFGP_Z2_ZC_MAX, TVFGP_Z2_WAVES);
+    const int slots = sms * (per_sm > 0 ? per_sm : 1);
+    plan->zc = zmarch_pick_zc(tx * ty, nz, slots, TVFGP_Z2_ZC_MAX, TVFGP_Z2_WAVES);
     plan->grid = dim3(tx, ty, (nz + plan->zc - 1) / plan->zc);
+    zmarch2_chunks(nz, static_cast<long long>(tx) * ty, slots, plan);
     return 0;
 }
 
@@ -512,6 +558,8 @@ inline bool zmarch2_fill(const Zmarch2Plan &plan, const float *b, const float *p
     za.N = N;
     za.err = err;
     za.zc = plan.zc;
+    za.nbig = plan.nbig;
+    for (int k = 0; k < 4; ++k) za.tap[k] = plan.tap[k];
     za.opx = nx;
     za.No = N;
     return zm_encode(&za.tb, b, nx, ny, nz, Z2_BW, Z2_HB) &&
