@@ -58,7 +58,7 @@ namespace tvfgp {
 #define TVFGP_Z2_MINB 3
 #endif
 #ifndef TVFGP_Z2_ZC_MAX
-#define TVFGP_Z2_ZC_MAX 64        // most output planes per CTA
+#define TVFGP_Z2_ZC_MAX 128       // most output planes per CTA
 #endif
 #ifndef TVFGP_Z2_WAVES
 #define TVFGP_Z2_WAVES 2          // fewest waves of CTAs over the resident slots
@@ -466,9 +466,10 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
 // order, z-chunk last, so the last chunk's CTAs set the launch's tail.  When
 // the last round of CTAs over the resident slots is less than half full (the
 // GPU idles for most of a CTA's time), the last chunk is cut into shorter
-// pieces (tap): 512^3 with 64-plane chunks runs 12.07 rounds, and its
-// launches get 1.7% shorter; fuller last rounds lose more to the pieces'
-// prologues than the tail costs.
+// pieces (tap): 512^3 with 64-plane chunks ran 12.07 rounds, and its
+// launches got 1.7% shorter; fuller last rounds lose more to the pieces'
+// prologues than the tail costs.  With the tail cut, longer chunks (up to
+// 128 planes, fewer prologues) pay: 512^3 now runs 6.04 rounds of 128.
 struct Zmarch2Plan {
     dim3 grid;
     int zc;
