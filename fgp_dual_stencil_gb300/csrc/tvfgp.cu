@@ -854,6 +854,19 @@ void plan_packed(const tvfgp_handle *h, const tvfgp_handle *sh, const float *b, 
     }
 }
 
+// True while `st` is being captured into a CUDA graph.  A run then records
+// its launches into the caller's graph one by one (the handle's own graph is
+// not replayed inside it) and allocates nothing.
+bool capturing(cudaStream_t st)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return cs != cudaStreamCaptureStatusNone;
+}
+
 // How a run of nsteps goes on handle h with these buffers: directly on the
 // handle's kernels, or through dense buffers (the padded-row runs), either
 // with the packing folded into the first step and the unpacking into the
@@ -1092,8 +1105,10 @@ int tvfgp_run(tvfgp_t h, const float *b, float *p, float *r, float lambda, int n
     // two-step kernel the first step packs and the last launch unpacks; the
     // other TMA variants pack, run and unpack (26 volume moves).  The padding
     // is never written.
+    const bool cap = capturing(st);
+    const bool use_graph = h->graph_on && !cap;
     const RunRoute route = run_route(h, b, p, r, nsteps, zmarch_available());
-    if (route != kRouteDirect && ensure_shadow(h) == TVFGP_OK) {
+    if (route != kRouteDirect && (h->shadow != nullptr || !cap) && ensure_shadow(h) == TVFGP_OK) {
         tvfgp_handle *sh = h->shadow;
         const size_t n = static_cast<size_t>(h->nx) * h->ny * h->nz;
         const size_t rows = static_cast<size_t>(h->ny) * h->nz;
@@ -1104,7 +1119,7 @@ int tvfgp_run(tvfgp_t h, const float *b, float *p, float *r, float lambda, int n
             std::vector<Item> items;
             plan_packed(h, sh, b, p, r, m, items);
             const long long before = sh->launches;
-            if (h->graph_on) {
+            if (use_graph) {
                 rc = run_graph(sh, kKernPackStep, b, p, r, lambda, nsteps, t0, items, false, CopySpec(), st);
             } else {
                 for (size_t k = 0; k < items.size() && rc == TVFGP_OK; ++k)
@@ -1143,7 +1158,7 @@ int tvfgp_run(tvfgp_t h, const float *b, float *p, float *r, float lambda, int n
     std::vector<Item> items;
     bool copy_back = false;
     plan_run(h, variant, vec_ok, p, r, m, items, &copy_back);
-    if (h->graph_on) {
+    if (use_graph) {
         rc = run_graph(h, variant, b, p, r, lambda, nsteps, t0, items, copy_back, dual_copy(h, 4), st);
     } else {
         for (size_t k = 0; k < items.size() && rc == TVFGP_OK; ++k)
@@ -1243,7 +1258,7 @@ int tvfgp_run_f16(tvfgp_t h, const float *b, unsigned short *p, unsigned short *
     }
     const bool copy_back = (nsteps % 2) == 1;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (h->graph_on) {
+    if (h->graph_on && !capturing(st)) {
         rc = run_graph(h, kern, b, pf, rf, lambda, nsteps, t0, items, copy_back, dual_copy(h, 2), st);
     } else {
         for (size_t k = 0; k < items.size() && rc == TVFGP_OK; ++k)

@@ -165,7 +165,11 @@ int tvfgp_set_graph(tvfgp_t h, int enable);
  *           continue a run);
  *   t_final NULL or receives t after the last step (host value, available
  *           on return).
- * b, p, r and the scratch buffer must not overlap.  Asynchronous on stream. */
+ * b, p, r and the scratch buffer must not overlap.  Asynchronous on stream.
+ * The call may be recorded into the caller's CUDA graph (stream capture):
+ * on a capturing stream the launches go into that graph one by one, the
+ * handle's own graph is not used and nothing is allocated (a padded-row run
+ * whose dense buffers do not exist yet runs in place). */
 int tvfgp_run(tvfgp_t h, const float *b, float *p, float *r, float lambda, int nsteps,
               double t0, tvfgp_stream_t stream, double *t_final);
 
