@@ -1,0 +1,58 @@
+"""Host logic of bench.py that decides what the JSON line reports: the kernel
+source hash that gates the recorded DRAM traffic (comment edits keep it,
+code edits drop the traffic to null) and the scaling of that traffic to a
+volume."""
+import json
+import os
+import shutil
+
+import bench
+
+
+def test_strip_comments_keeps_code_and_strings():
+    src = 'int a; // tail\n/* block\n spanning */ int b = 1; /**/\n\n  const char *s = "// not a comment";\n'
+    out = bench._strip_comments(src)
+    assert out == 'int a;\n int b = 1;\n  const char *s = "// not a comment";'
+    assert bench._strip_comments('char q = "a\\"//b"; // c') == 'char q = "a\\"//b";'
+
+
+def _tree(tmp_path):
+    """A copy of the hashed sources and of the recorded traffic in tmp_path."""
+    src = os.path.join(bench.ROOT, "fgp_dual_stencil_gb300", "csrc")
+    dst = tmp_path / "fgp_dual_stencil_gb300" / "csrc"
+    dst.mkdir(parents=True)
+    for fn in ("fgp_kernels.cuh", "zmarch_tma.cuh", "zmarch2_tma.cuh"):
+        shutil.copy(os.path.join(src, fn), dst / fn)
+    (tmp_path / "profiles").mkdir()
+    return dst
+
+
+def test_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
+    csrc = _tree(tmp_path)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = bench.kernel_source_hash()
+    rec = {"fgp_step2_zmarch_tma": {"source_hash": h, "dram_bytes_per_voxel": 54.5}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    assert bench.ncu_traffic("fgp_step2_zmarch_tma", 1000) == 54500.0
+    assert bench.ncu_traffic("fgp_step_zmarch_tma", 1000) is None          # not recorded
+
+    k = csrc / "zmarch2_tma.cuh"
+    k.write_text(k.read_text() + "\n// a comment added at the end\n")
+    assert bench.kernel_source_hash() == h                                  # comments: same
+    assert bench.ncu_traffic("fgp_step2_zmarch_tma", 1000) == 54500.0
+
+    k.write_text(k.read_text() + "\nstatic const int changed = 1;\n")
+    assert bench.kernel_source_hash() != h                                  # code: new hash
+    assert bench.ncu_traffic("fgp_step2_zmarch_tma", 1000) is None
+
+    (tmp_path / "profiles" / "traffic.json").write_text("{not json")
+    assert bench.ncu_traffic("fgp_step2_zmarch_tma", 1000) is None
+
+
+def test_committed_traffic_names_the_bench_kernels():
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)
+    for name in ("fgp_step2_zmarch_tma", "fgp_step_zmarch_tma", "fgp_step_zmarch_tma<__half>"):
+        ent = rec[name]
+        assert len(ent["source_hash"]) == 16 and ent["dram_bytes_per_voxel"] > 0
+        assert "--clock-control none" in ent["command"]
