@@ -1472,6 +1472,27 @@ int tvfgp_debug_plan(int nx, int ny, int nz, int pitch, int variant, int nsteps,
     return TVFGP_OK;
 }
 
+int tvfgp_debug_chunks(int nx, int ny, int nz, int slots, int *zc, int *z0, int *ze, int cap, int *count)
+{
+    if (nx < 1 || ny < 1 || nz < 1 || nx > 65535 || ny > 65535 || nz > 65535 || slots < 1 || zc == nullptr ||
+        count == nullptr || cap < 0 || (cap > 0 && (z0 == nullptr || ze == nullptr)))
+        return TVFGP_ERR_ARG;
+    Zmarch2Plan plan{};
+    const int tx = (nx + Z2_TX - 1) / Z2_TX, ty = (ny + Z2_TY - 1) / Z2_TY;
+    plan.zc = zmarch_pick_zc(tx * ty, nz, slots, TVFGP_Z2_ZC_MAX, TVFGP_Z2_WAVES);
+    plan.grid = dim3(tx, ty, (nz + plan.zc - 1) / plan.zc);
+    zmarch2_chunks(nz, static_cast<long long>(tx) * ty, slots, &plan);
+    *zc = plan.zc;
+    *count = static_cast<int>(plan.grid.z);
+    // the output planes [z0, ze) of blockIdx.z = j, by the kernel's expressions
+    for (int j = 0; j < *count && j < cap; ++j) {
+        const int zbase = j < plan.nbig ? 0 : plan.nbig * plan.zc;
+        z0[j] = j < plan.nbig ? j * plan.zc : zbase + plan.tap[j - plan.nbig];
+        ze[j] = std::min(j < plan.nbig ? z0[j] + plan.zc : zbase + plan.tap[j - plan.nbig + 1], nz);
+    }
+    return TVFGP_OK;
+}
+
 int tvfgp_debug_timeout_probe(tvfgp_t h, int spins, tvfgp_stream_t stream)
 {
     if (!valid(h) || spins < 1 || spins > (1 << 24)) return TVFGP_ERR_ARG;

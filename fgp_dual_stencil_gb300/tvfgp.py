@@ -71,6 +71,8 @@ def _load():
         "tvfgp_debug_fail_allocs": ([i, i], i),
         "tvfgp_debug_plan": ([i, i, i, i, i, i, d, ctypes.POINTER(i), ctypes.POINTER(i), ctypes.POINTER(i),
                               ctypes.POINTER(f), i, ctypes.POINTER(i)], i),
+        "tvfgp_debug_chunks": ([i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i), ctypes.POINTER(i), i,
+                                ctypes.POINTER(i)], i),
         "tvfgp_debug_projection_check": ([i, ctypes.c_ulonglong, ctypes.c_ulonglong, vp, vp], i),
         "tvfgp_run_noalloc": ([i, i, i, vp, vp, vp, f, i, d, vp, ctypes.POINTER(d)], i),
         "tvfgp_host_alloc": ([ctypes.c_size_t, i, ctypes.POINTER(vp)], i),
@@ -282,6 +284,19 @@ def tvfgp_debug_plan(nx: int, ny: int, nz: int, pitch: int = 0, variant: int | s
     keys = ("variant", "b", "p_src", "p_dst", "r_src", "r_dst", "flags")
     launches = [dict(zip(keys, items[7 * k:7 * k + 7]), m=(m[2 * k], m[2 * k + 1])) for k in range(n)]
     return route.value, bool(copy_back.value), launches
+
+
+def tvfgp_debug_chunks(nx: int, ny: int, nz: int, slots: int):
+    """(zc, [(z0, ze), ...]): the two-step kernel's split of the planes among
+    its CTAs with `slots` resident CTAs (host only, no GPU)."""
+    zc, count = ctypes.c_int(), ctypes.c_int()
+    _ok(_lib.tvfgp_debug_chunks(nx, ny, nz, slots, ctypes.byref(zc), None, None, 0, ctypes.byref(count)),
+        "tvfgp_debug_chunks")
+    n = count.value
+    z0, ze = (ctypes.c_int * max(n, 1))(), (ctypes.c_int * max(n, 1))()
+    _ok(_lib.tvfgp_debug_chunks(nx, ny, nz, slots, ctypes.byref(zc), z0, ze, n, ctypes.byref(count)),
+        "tvfgp_debug_chunks")
+    return zc.value, [(z0[j], ze[j]) for j in range(n)]
 
 
 def tvfgp_debug_timeout_probe(h: int, spins: int, stream=None) -> None:

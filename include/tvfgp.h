@@ -271,6 +271,14 @@ int tvfgp_debug_fail_allocs(int skip, int count);
 int tvfgp_debug_plan(int nx, int ny, int nz, int pitch, int variant, int nsteps, double t0, int *route,
                      int *copy_back, int *items, float *m, int cap, int *count);
 
+/* Host only, no CUDA call: how the two-step kernel splits the planes of an
+ * nx x ny x nz volume among its CTAs when `slots` CTAs are resident at once
+ * (SMs x CTAs per SM).  *zc: the planes of a full chunk; *count: the grid's
+ * z extent; z0[j], ze[j] for j < min(count, cap): the output planes [z0, ze)
+ * of the CTAs with blockIdx.z = j, by the kernel's own expressions.  Invalid
+ * arguments: TVFGP_ERR_ARG. */
+int tvfgp_debug_chunks(int nx, int ny, int nz, int slots, int *zc, int *z0, int *ze, int cap, int *count);
+
 /* Self-check of the step kernels' projection onto the unit ball, which
  * evaluates q / max(1, |q|) with a hardware square-root estimate and fused
  * multiply-add corrections instead of IEEE square root and division, and

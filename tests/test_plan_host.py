@@ -2,7 +2,9 @@
 variant and step count, the launches tvfgp_run would enqueue must take p and
 r from the caller's buffers back to them, never read a buffer they write in
 the same launch, apply the momentum weights of the schedule in order, and
-use the packing and padded-output launches exactly where the header says."""
+use the packing and padded-output launches exactly where the header says;
+and the two-step kernel's split of the planes among its CTAs must cover
+every plane once."""
 import itertools
 
 import numpy as np
@@ -106,3 +108,29 @@ def test_plan_argument_checks():
                  (65535, 65535, 1, 0, "auto", 1)]:
         with pytest.raises(T.TvfgpError):
             T.tvfgp_debug_plan(*args)
+
+
+def test_two_step_chunks_partition_the_planes():
+    """The two-step kernel's split of the planes among its CTAs covers every
+    plane once, no chunk is empty or longer than zc, and the last chunk is
+    cut into three pieces exactly when the last round of CTAs over the
+    resident slots is less than half full."""
+    cand = (128, 96, 64, 48, 32, 24, 16, 12, 8)
+    for nx, ny in [(512, 512), (1000, 600), (256, 256), (64, 26), (33, 5), (2048, 1024)]:
+        tiles = -(-nx // 32) * -(-ny // 12)
+        for nz in list(range(1, 70)) + [127, 128, 129, 255, 256, 257, 300, 511, 512, 513, 1100]:
+            for slots in (1, 152, 304, 456, 608):
+                zc, chunks = T.tvfgp_debug_chunks(nx, ny, nz, slots)
+                assert zc in cand
+                assert [z for a, b in chunks for z in range(a, b)] == list(range(nz)), (nx, ny, nz, slots)
+                assert all(0 < b - a <= zc for a, b in chunks)
+                whole = -(-nz // zc)
+                last = nz - (whole - 1) * zc
+                rem = tiles * whole % slots
+                tapered = len(chunks) != whole
+                assert tapered == (whole > 1 and last >= 24 and rem * 2 < slots), (nx, ny, nz, slots)
+                if tapered:
+                    sizes = [b - a for a, b in chunks[-3:]]
+                    assert len(chunks) == whole + 2 and sum(sizes) == last and sizes[0] >= sizes[1] >= sizes[2]
+    with pytest.raises(T.TvfgpError):
+        T.tvfgp_debug_chunks(8, 8, 8, 0)
