@@ -52,6 +52,7 @@ struct CubeArgs {
     CUtensorMap tb, t0, t1, t2;   // b, and r0, r1, r2 of the r read by this step
     StepArgs a;
     int *err;
+    int max_polls;                // bound of the wait for data (the drain keeps ZM_MAX_POLLS)
 };
 
 __global__ void __launch_bounds__(CB_THREADS) fgp_step_cube_tma(const __grid_constant__ CubeArgs ca)
@@ -96,7 +97,7 @@ __global__ void __launch_bounds__(CB_THREADS) fgp_step_cube_tma(const __grid_con
         P2 = ld_once4(a.p + 2 * a.N + i);
     }
     __syncthreads();                                  // the barrier is initialised
-    if (!mbar_wait_tma(bar, 0)) *abort_flag = 1;
+    if (!mbar_wait_tma(bar, 0, ca.max_polls)) *abort_flag = 1;
     __syncthreads();
     if (*abort_flag) {
         if (tid == 0) {
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(CB_THREADS) fgp_step_cube_tma(const __grid_con
             const int c = 4 * k;
             const float4 Z = zquad(lds4(Bs + bo + c), lds4(R0s + ro + c), lds4(R1s + ro + c), lds4(R2s + ro + c),
                                    R0s[ro + c - 1], lds4(R1s + ro + c - CB_RX), lds4(R2s + ro + c - CB_RX * CB_RY),
-                                   a.lam);
+                                   a.lam, neg_zero(a.lam));
             *reinterpret_cast<float4 *>(Zs + bo + c) = Z;
         } else {
             const int c = CB_TX;
@@ -151,7 +152,7 @@ __global__ void __launch_bounds__(CB_THREADS) fgp_step_cube_tma(const __grid_con
         G2.z = __fsub_rn(zc.z, zz.z); G2.w = __fsub_rn(zc.w, zz.w);
     }
     float4 R0 = lds4(R0s + ro), R1 = lds4(R1s + ro), R2 = lds4(R2s + ro);
-    dual_update4(R0, R1, R2, G0, G1, G2, P0, P1, P2, a.s, a.m);
+    dual_update4(R0, R1, R2, G0, G1, G2, P0, P1, P2, a.s, a.m, neg_zero(a.lam));
     st4(a.p + i, P0);
     st4(a.p + a.N + i, P1);
     st4(a.p + 2 * a.N + i, P2);
@@ -188,6 +189,7 @@ inline bool cube_fill(const StepArgs &a, int *err, CubeArgs &ca)
 {
     ca.a = a;
     ca.err = err;
+    ca.max_polls = ZM_MAX_POLLS;
     const float *r = a.rs;
     return cube_encode(&ca.tb, a.b, a.nx, a.ny, a.nz, CB_BX, CB_BY, CB_BZ) &&
            cube_encode(&ca.t0, r, a.nx, a.ny, a.nz, CB_RX, CB_RY, CB_RZ) &&

@@ -68,6 +68,109 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kErrTimeout = 5;   // value written to the device error word
 
 // ---------------------------------------------------------------------------
+// packed fp32 pairs (sm_100 and later)
+// ---------------------------------------------------------------------------
+//
+// One packed instruction rounds two independent lanes, each exactly as the
+// scalar __fadd_rn / __fsub_rn / __fmul_rn / __fmaf_rn would (IEEE binary32,
+// nearest even, subnormals kept).  A quad (x, y, z, w) of four x voxels is
+// the two aligned register pairs (x, y) and (z, w) of its float4, so every
+// per-voxel operation of the step that pairs voxels lane for lane runs as two
+// packed instructions instead of four scalar ones, with the same bits.  Only
+// the x differences inside a quad (voxel minus its x-1 neighbour) do not pair
+// lane for lane; they stay scalar.
+
+__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
+__device__ __forceinline__ float4 join2(float2 a, float2 b) { return make_float4(a.x, a.y, b.x, b.y); }
+__device__ __forceinline__ float4 splat4(float v) { return make_float4(v, v, v, v); }
+
+// Each packed operation is written as PTX with an explicit .rn rounding
+// modifier: like the scalar __f*_rn intrinsics, such an add or multiply is
+// never contracted with a neighbouring operation into a fused multiply-add.
+__device__ __forceinline__ float2 add2_rn(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\t"
+        "mov.b64 pb, {%4, %5};\n\t"
+        "add.rn.f32x2 pd, pa, pb;\n\t"
+        "mov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 sub2_rn(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\t"
+        "mov.b64 pb, {%4, %5};\n\t"
+        "sub.rn.f32x2 pd, pa, pb;\n\t"
+        "mov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\t"
+        "mov.b64 pb, {%4, %5};\n\t"
+        "mul.rn.f32x2 pd, pa, pb;\n\t"
+        "mov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c)   // a*b + c, one rounding
+{
+    float2 d;
+    asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\t"
+        "mov.b64 pb, {%4, %5};\n\t"
+        "mov.b64 pc, {%6, %7};\n\t"
+        "fma.rn.f32x2 pd, pa, pb, pc;\n\t"
+        "mov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float4 add4_rn(float4 a, float4 b)
+{
+    return join2(add2_rn(lo2(a), lo2(b)), add2_rn(hi2(a), hi2(b)));
+}
+__device__ __forceinline__ float4 sub4_rn(float4 a, float4 b)
+{
+    return join2(sub2_rn(lo2(a), lo2(b)), sub2_rn(hi2(a), hi2(b)));
+}
+__device__ __forceinline__ float4 mul4_rn(float4 a, float4 b)
+{
+    return join2(mul2_rn(lo2(a), lo2(b)), mul2_rn(hi2(a), hi2(b)));
+}
+__device__ __forceinline__ float4 fma4_rn(float4 a, float4 b, float4 c)   // a*b + c, one rounding
+{
+    return join2(fma2_rn(lo2(a), lo2(b), lo2(c)), fma2_rn(hi2(a), hi2(b), hi2(c)));
+}
+__device__ __forceinline__ float4 neg4(float4 a) { return make_float4(-a.x, -a.y, -a.z, -a.w); }
+
+// A product that feeds a packed add or subtract.  ptxas merges a packed
+// multiply whose only use is a packed add or subtract into one fused
+// multiply-add, even when both are written with an explicit .rn (measured
+// with nvcc 13.0 for sm_103a: a third of random products then round
+// differently), which would change the step's bits.  The product is
+// therefore formed as a fused multiply-add with a -0 addend,
+// RN(a*b + (-0)) = RN(a*b) for every a and b, signed zeros included, which
+// is not merged further.  nz must be -0 at run time, made from a kernel
+// argument by neg_zero(): a -0 literal would be folded back into a multiply.
+__device__ __forceinline__ float4 prod4_rn(float4 a, float4 b, float4 nz) { return fma4_rn(a, b, nz); }
+
+// -0.0f from a kernel argument x that the host has checked to be finite and
+// positive (lambda, or the step 1/(12 lambda)).
+__device__ __forceinline__ float neg_zero(float x) { return __fmul_rn(-0.0f, x); }
+
+// ---------------------------------------------------------------------------
 // scalar pieces of the step (the single definition every kernel uses)
 // ---------------------------------------------------------------------------
 
@@ -97,7 +200,7 @@ __device__ __forceinline__ float zval(float b, float lam, float d0, float d1, fl
 // Dev. 34(1), 1990; the FMA-based division of Muller et al., "Handbook of
 // Floating-Point Arithmetic"): when y = RN(1/n) and c is within one ulp of
 // q/n, w is exact and d = RN(q/n), as long as nothing under- or overflows.
-// That n = RN(sqrt(nn)) and y = RN(1/n) for every float nn in (1, 2^100) is
+// That n = RN(sqrt(nn)) and y = RN(1/n) for every float nn in [1, 2^100) is
 // not a theorem about the estimates but a measured fact (a reciprocal
 // corrected from k instead of from its own estimate misses 200 of them):
 // tvfgp_debug_projection_check compares all of them with __fsqrt_rn and
@@ -122,7 +225,7 @@ __device__ __forceinline__ float rcp_estimate(float x)
     return y;
 }
 
-// n = RN(sqrt(nn)) and y = RN(1/n), for nn in (1, 2^100).
+// n = RN(sqrt(nn)) and y = RN(1/n), for nn in [1, 2^100).
 __device__ __forceinline__ void sqrt_recip_rn(float nn, float &n, float &y)
 {
     const float k = rsqrt_estimate(nn);
@@ -143,12 +246,11 @@ __device__ __forceinline__ float div_by_recip_rn(float q, float n, float y)
 }
 
 // A component outside the fast path's range: non-zero and below 2^-75 in
-// magnitude.  (2|q| as bits) - 2 wraps to the top for q = +-0.
-__device__ __forceinline__ bool tiny_nonzero(float q)
-{
-    constexpr uint32_t kLim = 0x1a000000u * 2u - 2u;    // 2^-75 has the bits 0x1a000000
-    return (__float_as_uint(q) << 1) - 2u < kLim;
-}
+// magnitude.  (2|q| as bits) - 2 wraps to the top for q = +-0, so the key
+// of a component is below kTinyLim exactly when it is tiny and non-zero.
+constexpr uint32_t kTinyLim = 0x1a000000u * 2u - 2u;    // 2^-75 has the bits 0x1a000000
+__device__ __forceinline__ uint32_t tiny_key(float q) { return (__float_as_uint(q) << 1) - 2u; }
+__device__ __forceinline__ bool tiny_nonzero(float q) { return tiny_key(q) < kTinyLim; }
 
 // The canonical IEEE projection (also the reference of the self-check).
 __device__ __forceinline__ void project_unit_ball_ieee(float &q0, float &q1, float &q2, float nn)
@@ -199,60 +301,72 @@ __device__ __forceinline__ void dual_update(float &r0, float &r1, float &r2,
     p2 = q2;
 }
 
+// RN(q / n) for the four voxels of a quad, given Y = RN(1/n) (packed form of
+// div_by_recip_rn, the same three roundings per lane).
+__device__ __forceinline__ float4 div4_by_recip_rn(float4 Q, float4 N, float4 Y)
+{
+    const float4 C = mul4_rn(Q, Y);
+    const float4 W = fma4_rn(C, N, neg4(Q));
+    return fma4_rn(neg4(W), Y, C);
+}
+
 // dual_update on the four voxels of a quad (component a of the quad in Ra,
-// Ga, Pa): the same operations per voxel, arranged for instruction-level
-// parallelism: q and |q|^2 of all four first, one branch to the projection
-// when any of the four needs it (the others pass through it unchanged, with
-// n = y = 1), one to the IEEE operations when any lies outside the fast
-// path's range, then the four extrapolations.
+// Ga, Pa): the same operations per voxel, as packed pairs where the lanes
+// pair up.  q and |q|^2 of all four first; one branch to the projection when
+// any of the four needs it, one to the IEEE operations when any value of the
+// quad lies outside the fast path's range; then the four extrapolations.
+// The fast path divides every voxel by RN(sqrt(max(1, |q|^2))): the voxels
+// with |q|^2 <= 1 get n = RN(sqrt(1)) = 1 and y = 1 (checked on the GPU with
+// the other square roots), and c = q*1, w = c*1 - q = +0, d = c - 0*1 return
+// their q unchanged, signed zeros and subnormals included.  nzero: -0 at run
+// time (neg_zero).
 __device__ __forceinline__ void dual_update4(float4 &R0, float4 &R1, float4 &R2, float4 G0, float4 G1,
                                              float4 G2, float4 &P0, float4 &P1, float4 &P2, float s,
-                                             float m)
+                                             float m, float nzero)
 {
-    float *r0 = &R0.x, *r1 = &R1.x, *r2 = &R2.x, *p0 = &P0.x, *p1 = &P1.x, *p2 = &P2.x;
-    const float *g0 = &G0.x, *g1 = &G1.x, *g2 = &G2.x;
-    float q0[4], q1[4], q2[4], nn[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        q0[e] = __fadd_rn(r0[e], __fmul_rn(g0[e], s));
-        q1[e] = __fadd_rn(r1[e], __fmul_rn(g1[e], s));
-        q2[e] = __fadd_rn(r2[e], __fmul_rn(g2[e], s));
-        nn[e] = __fadd_rn(__fadd_rn(__fmul_rn(q0[e], q0[e]), __fmul_rn(q1[e], q1[e])), __fmul_rn(q2[e], q2[e]));
-    }
-    bool any_big = false, any_slow = false;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const bool big = nn[e] > 1.0f;
-        any_big |= big;
-        any_slow |= big && (!(nn[e] < 0x1p100f) || (tiny_nonzero(q0[e]) | tiny_nonzero(q1[e]) | tiny_nonzero(q2[e])));
-    }
-    if (any_big) {
-        if (!any_slow) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float n, y;
-                sqrt_recip_rn(nn[e], n, y);
-                const bool big = nn[e] > 1.0f;
-                n = big ? n : 1.0f;
-                y = big ? y : 1.0f;
-                q0[e] = div_by_recip_rn(q0[e], n, y);
-                q1[e] = div_by_recip_rn(q1[e], n, y);
-                q2[e] = div_by_recip_rn(q2[e], n, y);
-            }
+    const float4 S = splat4(s), NZ = splat4(nzero);
+    float4 Q0 = add4_rn(R0, prod4_rn(G0, S, NZ));
+    float4 Q1 = add4_rn(R1, prod4_rn(G1, S, NZ));
+    float4 Q2 = add4_rn(R2, prod4_rn(G2, S, NZ));
+    const float4 NN = add4_rn(add4_rn(prod4_rn(Q0, Q0, NZ), prod4_rn(Q1, Q1, NZ)), prod4_rn(Q2, Q2, NZ));
+    const float4 NC = make_float4(fmaxf(NN.x, 1.0f), fmaxf(NN.y, 1.0f), fmaxf(NN.z, 1.0f), fmaxf(NN.w, 1.0f));
+    if (fmaxf(fmaxf(NC.x, NC.y), fmaxf(NC.z, NC.w)) > 1.0f) {
+        // The fast path's range for the whole quad: the rounded sum of the
+        // four |q|^2 (none of which exceeds it; NaN if one is NaN) below
+        // 2^100, and every component zero or at least 2^-75.
+        const float2 half = add2_rn(lo2(NN), hi2(NN));
+        const float sum = __fadd_rn(half.x, half.y);
+        uint32_t key = min(min(tiny_key(Q0.x), tiny_key(Q0.y)), min(tiny_key(Q0.z), tiny_key(Q0.w)));
+        key = min(key, min(min(tiny_key(Q1.x), tiny_key(Q1.y)), min(tiny_key(Q1.z), tiny_key(Q1.w))));
+        key = min(key, min(min(tiny_key(Q2.x), tiny_key(Q2.y)), min(tiny_key(Q2.z), tiny_key(Q2.w))));
+        if (sum < 0x1p100f && key >= kTinyLim) {
+            // sqrt_recip_rn on the four voxels, packed where the lanes pair up
+            const float4 K = make_float4(rsqrt_estimate(NC.x), rsqrt_estimate(NC.y), rsqrt_estimate(NC.z),
+                                         rsqrt_estimate(NC.w));
+            const float4 Gq = mul4_rn(NC, K);
+            const float4 E = fma4_rn(neg4(Gq), Gq, NC);
+            const float4 N = fma4_rn(E, mul4_rn(splat4(0.5f), K), Gq);
+            const float4 V = make_float4(rcp_estimate(N.x), rcp_estimate(N.y), rcp_estimate(N.z),
+                                         rcp_estimate(N.w));
+            const float4 T = fma4_rn(neg4(N), V, splat4(1.0f));
+            const float4 Y = fma4_rn(T, V, V);
+            Q0 = div4_by_recip_rn(Q0, N, Y);
+            Q1 = div4_by_recip_rn(Q1, N, Y);
+            Q2 = div4_by_recip_rn(Q2, N, Y);
         } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) project_unit_ball(q0[e], q1[e], q2[e], nn[e]);
+            project_unit_ball(Q0.x, Q1.x, Q2.x, NN.x);
+            project_unit_ball(Q0.y, Q1.y, Q2.y, NN.y);
+            project_unit_ball(Q0.z, Q1.z, Q2.z, NN.z);
+            project_unit_ball(Q0.w, Q1.w, Q2.w, NN.w);
         }
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        r0[e] = __fadd_rn(q0[e], __fmul_rn(m, __fsub_rn(q0[e], p0[e])));
-        r1[e] = __fadd_rn(q1[e], __fmul_rn(m, __fsub_rn(q1[e], p1[e])));
-        r2[e] = __fadd_rn(q2[e], __fmul_rn(m, __fsub_rn(q2[e], p2[e])));
-        p0[e] = q0[e];
-        p1[e] = q1[e];
-        p2[e] = q2[e];
-    }
+    const float4 M = splat4(m);
+    R0 = add4_rn(Q0, prod4_rn(M, sub4_rn(Q0, P0), NZ));
+    R1 = add4_rn(Q1, prod4_rn(M, sub4_rn(Q1, P1), NZ));
+    R2 = add4_rn(Q2, prod4_rn(M, sub4_rn(Q2, P2), NZ));
+    P0 = Q0;
+    P1 = Q1;
+    P2 = Q2;
 }
 
 // ---------------------------------------------------------------------------
@@ -359,16 +473,18 @@ template <int VW> __device__ __forceinline__ void stvq(__half *p, float4 v)
 
 
 // z at four consecutive x voxels from their b and r, the r0 of the voxel left
-// of the first one, and r1, r2 of the lower neighbours in y and z.
+// of the first one, and r1, r2 of the lower neighbours in y and z (nzero: -0
+// at run time, neg_zero(lam)).
 __device__ __forceinline__ float4 zquad(float4 B, float4 R0, float4 R1, float4 R2, float r0left,
-                                        float4 R1lo, float4 R2lo, float lam)
+                                        float4 R1lo, float4 R2lo, float lam, float nzero)
 {
-    float4 z;
-    z.x = zval(B.x, lam, __fsub_rn(R0.x, r0left), __fsub_rn(R1.x, R1lo.x), __fsub_rn(R2.x, R2lo.x));
-    z.y = zval(B.y, lam, __fsub_rn(R0.y, R0.x), __fsub_rn(R1.y, R1lo.y), __fsub_rn(R2.y, R2lo.y));
-    z.z = zval(B.z, lam, __fsub_rn(R0.z, R0.y), __fsub_rn(R1.z, R1lo.z), __fsub_rn(R2.z, R2lo.z));
-    z.w = zval(B.w, lam, __fsub_rn(R0.w, R0.z), __fsub_rn(R1.w, R1lo.w), __fsub_rn(R2.w, R2lo.w));
-    return z;
+    // zval on each voxel: the x differences pair a voxel with its left
+    // neighbour (scalar); the rest runs as packed pairs, in the same order
+    const float4 D0 = make_float4(__fsub_rn(R0.x, r0left), __fsub_rn(R0.y, R0.x), __fsub_rn(R0.z, R0.y),
+                                  __fsub_rn(R0.w, R0.z));
+    const float4 L = add4_rn(add4_rn(D0, sub4_rn(R1, R1lo)), sub4_rn(R2, R2lo));
+    const float4 t = sub4_rn(B, prod4_rn(splat4(lam), L, splat4(nzero)));
+    return make_float4(fmaxf(t.x, 0.0f), fmaxf(t.y, 0.0f), fmaxf(t.z, 0.0f), fmaxf(t.w, 0.0f));
 }
 
 // ---------------------------------------------------------------------------
@@ -413,6 +529,7 @@ fgp_step_fused4(const StepArgsT<TS> a)
     const bool hasY = (y + 1 < ny);              // warp-uniform
     const int sz = px * ny;
     const float lam = a.lam, s = a.s, m = a.m;
+    const float nzero = neg_zero(lam);
 
     const float *__restrict__ b = a.b;
     const TS *__restrict__ r0 = a.rs;
@@ -450,7 +567,7 @@ fgp_step_fused4(const StepArgsT<TS> a)
         }
         float left = __shfl_up_sync(kFull, R0c.w, 1);
         if (lane == 0) left = (x0 > 0) ? ld1_ro(r0 + i - 1) : 0.0f;
-        Zc = zquad(Bc, R0c, R1c, R2c, left, R1lo, R2lo, lam);
+        Zc = zquad(Bc, R0c, R1c, R2c, left, R1lo, R2lo, lam, nzero);
         if (PACK && xin) stq<4>(a.bo + io, Bc);
     }
     // r2 of row y+1 one plane below (the z-lower neighbour of z(i+ey))
@@ -490,14 +607,14 @@ fgp_step_fused4(const StepArgsT<TS> a)
         if (hasY) {
             float left = __shfl_up_sync(kFull, R0y.w, 1);
             if (lane == 0) left = (x0 > 0) ? ld1_ro(r0 + i + px - 1) : 0.0f;
-            ZY = zquad(By, R0y, R1y, R2y, left, R1c, R2yp, lam);
+            ZY = zquad(By, R0y, R1y, R2y, left, R1c, R2yp, lam, nzero);
         }
         // z(i+ez)
         float4 ZZ = f4zero();
         if (hasZ) {
             float left = __shfl_up_sync(kFull, R0n.w, 1);
             if (lane == 0) left = (x0 > 0) ? ld1_ro(r0 + i + sz - 1) : 0.0f;
-            ZZ = zquad(Bn, R0n, R1n, R2n, left, R1lon, R2c, lam);
+            ZZ = zquad(Bn, R0n, R1n, R2n, left, R1lon, R2c, lam, nzero);
         }
         // z(i+ex) of the last voxel: the next lane's first z
         float zx = __shfl_down_sync(kFull, Zc.x, 1);
@@ -777,7 +894,7 @@ __global__ void __launch_bounds__(32 * BY) primal_vec4(const PrimalArgsT<TS> a)
     }
     float left = __shfl_up_sync(kFull, D0.w, 1);
     if (lane == 0) left = (x0 > 0) ? ld1_ro(d0 + i - 1) : 0.0f;
-    const float4 Z = zquad(B, D0, D1, D2, left, D1lo, D2lo, a.lam);
+    const float4 Z = zquad(B, D0, D1, D2, left, D1lo, D2lo, a.lam, neg_zero(a.lam));
     if (xin) st4(a.z + i, Z);
 }
 

@@ -2,7 +2,7 @@
 // fgp_kernels.cuh) against CUDA's correctly rounded operations, on the GPU
 // that runs it.  Plain grid-stride loops: no waits, every index in range.
 //
-//   mode 0  every float nn in (1, 2^100): the fast n equals __fsqrt_rn(nn)
+//   mode 0  every float nn in [1, 2^100): the fast n equals __fsqrt_rn(nn)
 //           and the fast y equals __frcp_rn(n);
 //   mode 1  `count` pseudo-random triples q: project_unit_ball equals
 //           project_unit_ball_ieee bit for bit (components spread over
@@ -22,7 +22,7 @@
 
 namespace tvfgp {
 
-constexpr uint32_t kNnFirst = 0x3f800001u;   // the float after 1
+constexpr uint32_t kNnFirst = 0x3f800000u;   // 1
 constexpr uint32_t kNnEnd = 0x71800000u;     // 2^100 (excluded)
 
 __device__ __forceinline__ uint64_t splitmix64(uint64_t x)
@@ -117,7 +117,7 @@ __global__ void projection_check(int mode, unsigned long long count, unsigned lo
             const float sc = make_float(0, static_cast<int>(splitmix64(~seed ^ i) % 5) + 1, 0u);   // s: 2 .. 32
             const float m = 0.25f;
             float4 R0 = v[0], R1 = v[1], R2 = v[2], P0 = v[6], P1 = v[7], P2 = v[8];
-            dual_update4(R0, R1, R2, v[3], v[4], v[5], P0, P1, P2, sc, m);
+            dual_update4(R0, R1, R2, v[3], v[4], v[5], P0, P1, P2, sc, m, neg_zero(sc));
             bool same = true;
             const float *g0 = &v[3].x, *g1 = &v[4].x, *g2 = &v[5].x;
             const float *o[6] = {&R0.x, &R1.x, &R2.x, &P0.x, &P1.x, &P2.x};

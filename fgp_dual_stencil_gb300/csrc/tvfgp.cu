@@ -24,6 +24,7 @@
 #include <cstdlib>
 #include <mutex>
 #include <new>
+#include <utility>
 #include <vector>
 
 using namespace tvfgp;
@@ -151,6 +152,7 @@ struct tvfgp_handle {
     // staging buffers (b, p, r: 7*nx*ny*nz floats), made on first use
     tvfgp_handle *shadow;
     float *pk;
+    int poll_limit;                // bound of the TMA kernels' waits for data (test hook)
 };
 
 namespace {
@@ -479,7 +481,9 @@ bool fill_item(const tvfgp_handle *h, const Item &it, const float *b_run, float 
         k.ah.px = h->px;
         if (it.kernel == kKernZmarchH) {
             k.ptrs[0] = &k.zah;
-            return zmarch_fill(h->zplan_h, k.ah, h->d_err, k.zah);
+            const bool ok = zmarch_fill(h->zplan_h, k.ah, h->d_err, k.zah);
+            k.zah.max_polls = h->poll_limit;
+            return ok;
         }
         k.ptrs[0] = &k.ah;
         return true;
@@ -516,6 +520,7 @@ bool fill_item(const tvfgp_handle *h, const Item &it, const float *b_run, float 
         k.ptrs[0] = &k.z2;
         const bool ok = zmarch2_fill(h->z2plan, b, it.p_src, it.p_dst, it.r_src, it.r_dst, lam, step_of(lam),
                                      it.m0, it.m1, h->nx, h->ny, h->nz, h->N, h->d_err, k.z2);
+        k.z2.max_polls = h->poll_limit;
         if (it.kernel == TVFGP_VARIANT_ZMARCH2_TMA) return ok;
         k.z2.opx = it.opx;
         k.z2.No = it.out_n;
@@ -524,11 +529,15 @@ bool fill_item(const tvfgp_handle *h, const Item &it, const float *b_run, float 
     k.a = make_args(h, b, it.p_dst, it.r_src, it.r_dst, lam, it.m0);
     if (it.kernel == TVFGP_VARIANT_ZMARCH_TMA) {
         k.ptrs[0] = &k.za;
-        return zmarch_fill(h->zplan, k.a, h->d_err, k.za);
+        const bool ok = zmarch_fill(h->zplan, k.a, h->d_err, k.za);
+        k.za.max_polls = h->poll_limit;
+        return ok;
     }
     if (it.kernel == TVFGP_VARIANT_CUBE_TMA) {
         k.ptrs[0] = &k.cb;
-        return cube_fill(k.a, h->d_err, k.cb);
+        const bool ok = cube_fill(k.a, h->d_err, k.cb);
+        k.cb.max_polls = h->poll_limit;
+        return ok;
     }
     k.ptrs[0] = &k.a;
     return true;
@@ -950,6 +959,7 @@ static int create_impl(int nx, int ny, int nz, int px, int variant, unsigned fla
     h->d_err = nullptr;
     h->shadow = nullptr;
     h->pk = nullptr;
+    h->poll_limit = ZM_MAX_POLLS;
     cudaError_t e = dev_alloc(&h->scratch, sizeof(float) * 3 * static_cast<size_t>(h->N));
     if (e == cudaSuccess) e = dev_alloc(&h->d_err, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(int));
@@ -1381,6 +1391,17 @@ int tvfgp_debug_projection_check(int mode, unsigned long long count, unsigned lo
     return e == cudaSuccess ? TVFGP_OK : from_cuda(e);
 }
 
+int tvfgp_debug_set_poll_limit(tvfgp_t h, int polls)
+{
+    if (!valid(h) || polls > ZM_MAX_POLLS) return TVFGP_ERR_ARG;
+    const int lim = polls < 0 ? ZM_MAX_POLLS : polls;
+    for (tvfgp_handle *x = h; x != nullptr; x = x->shadow) {
+        x->poll_limit = lim;
+        for (auto &g : x->graphs) destroy_graph(g);       // rebuilt with the new limit on next use
+    }
+    return TVFGP_OK;
+}
+
 int tvfgp_debug_fail_allocs(int skip, int count)
 {
     if (skip < 0 || count < 0) return TVFGP_ERR_ARG;
@@ -1519,35 +1540,88 @@ static __device__ __align__(256) float g_noalloc_r[3 * static_cast<size_t>(TVFGP
 
 namespace {
 
-// Device address of g_noalloc_r, looked up once per device.  The name
-// g_noalloc_r is only a host-side stand-in in host code, never an address a
-// kernel may be given.
+// Device address of g_noalloc_r.  The name g_noalloc_r is only a host-side
+// stand-in in host code, never an address a kernel may be given.  Outside
+// stream capture the address is looked up on every call, with the calling
+// device current, and remembered per device together with the unique id of
+// the CUDA context it belongs to.  Under capture the lookup (which may load
+// the module) is not made: the remembered address is used only if it was
+// taken in the context that is current now, else the call is refused.  So a
+// reset device or another context never gets a stale address.
 constexpr int kNoallocMaxDevices = 64;
-float *g_noalloc_addr[kNoallocMaxDevices] = {};
+struct NoallocSlot {
+    float *addr = nullptr;
+    unsigned long long ctx_id = 0;
+    bool valid = false;
+};
+NoallocSlot g_noalloc_slot[kNoallocMaxDevices];
 std::mutex g_noalloc_mu;
 
-int noalloc_scratch(float **out)
+// Unique id of the current CUDA context (ids are never reused within a
+// process), from the driver's cuCtxGetCurrent and cuCtxGetId.
+bool current_context_id(unsigned long long *id)
+{
+    static const auto fns = [] {
+        void *get = nullptr, *gid = nullptr;
+        cudaDriverEntryPointQueryResult q1, q2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &get, 12000, cudaEnableDefault, &q1) !=
+                cudaSuccess || q1 != cudaDriverEntryPointSuccess)
+            get = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &gid, 12000, cudaEnableDefault, &q2) !=
+                cudaSuccess || q2 != cudaDriverEntryPointSuccess)
+            gid = nullptr;
+        cudaGetLastError();
+        return std::make_pair(reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(get),
+                              reinterpret_cast<PFN_cuCtxGetId_v12000>(gid));
+    }();
+    if (fns.first == nullptr || fns.second == nullptr) return false;
+    CUcontext ctx = nullptr;
+    if (fns.first(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return fns.second(ctx, id) == CUDA_SUCCESS;
+}
+
+int noalloc_scratch(cudaStream_t st, float **out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoallocMaxDevices) {
         cudaGetLastError();
         return TVFGP_ERR_CUDA;
     }
+    const bool cap = capturing(st);
+    unsigned long long id = 0;
+    const bool have_id = current_context_id(&id);
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (g_noalloc_addr[dev] == nullptr) {
-        void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_r);
-        if (e != cudaSuccess || p == nullptr) {
-            cudaGetLastError();
-            return TVFGP_ERR_CUDA;
-        }
-        g_noalloc_addr[dev] = static_cast<float *>(p);
+    NoallocSlot &slot = g_noalloc_slot[dev];
+    if (cap) {
+        if (!slot.valid || !have_id || slot.ctx_id != id) return TVFGP_ERR_ARG;
+        *out = slot.addr;
+        return TVFGP_OK;
     }
-    *out = g_noalloc_addr[dev];
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_r);
+    if (e != cudaSuccess || p == nullptr) {
+        cudaGetLastError();
+        return TVFGP_ERR_CUDA;
+    }
+    slot.addr = static_cast<float *>(p);
+    slot.ctx_id = id;
+    slot.valid = have_id;
+    *out = slot.addr;
     return TVFGP_OK;
 }
 
 }  // namespace
+
+extern "C" int tvfgp_debug_noalloc_scratch(void **addr, unsigned long long *bytes)
+{
+    if (addr == nullptr || bytes == nullptr) return TVFGP_ERR_ARG;
+    float *p = nullptr;
+    const int rc = noalloc_scratch(nullptr, &p);
+    if (rc) return rc;
+    *addr = p;
+    *bytes = sizeof(g_noalloc_r);
+    return TVFGP_OK;
+}
 
 extern "C" int tvfgp_run_noalloc(int nx, int ny, int nz, const float *b, float *p, float *r,
                                  float lambda, int nsteps, double t0, tvfgp_stream_t stream,
@@ -1563,16 +1637,17 @@ extern "C" int tvfgp_run_noalloc(int nx, int ny, int nz, const float *b, float *
     const size_t v = sizeof(float) * static_cast<size_t>(N);
     if (overlap(b, v, p, 3 * v) || overlap(b, v, r, 3 * v) || overlap(p, 3 * v, r, 3 * v))
         return TVFGP_ERR_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     float *scratch = nullptr;
-    if ((rc = noalloc_scratch(&scratch))) return rc;
-    if (overlap(b, v, scratch, 3 * v) || overlap(p, 3 * v, scratch, 3 * v) ||
-        overlap(r, 3 * v, scratch, 3 * v))
+    if ((rc = noalloc_scratch(st, &scratch))) return rc;
+    // a caller buffer anywhere in the array would be overwritten by some call
+    const size_t whole = sizeof(g_noalloc_r);
+    if (overlap(b, v, scratch, whole) || overlap(p, 3 * v, scratch, whole) || overlap(r, 3 * v, scratch, whole))
         return TVFGP_ERR_ARG;
 
     // Same launches as tvfgp_run's eager path, with the momentum schedule
     // evaluated step by step (no host buffer either).
     const bool vec_ok = (nx % 4 == 0) && aligned16(b) && aligned16(p) && aligned16(r);
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     StepArgs a;
     a.b = b;
     a.p = p;

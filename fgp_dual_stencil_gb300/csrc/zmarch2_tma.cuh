@@ -160,6 +160,7 @@ struct Zmarch2Args {
     int tap[4];                                     // pieces [tap[j], tap[j+1]) after nbig*zc
     int opx;                                        // row pitch of p_dst, r_dst (nx: dense)
     long long No;                                   // their elements per component
+    int max_polls;                                  // bound of the waits for data (drain: ZM_MAX_POLLS)
 };
 
 // PADDED_OUT: p_dst and r_dst have rows of opx floats (even), written as
@@ -187,6 +188,7 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     const int uk_last = min(ze, nz - 1);       // last plane of step k (and of z^{k+1})
     const int last = min(ze + 1, nz - 1);      // last staged plane (z^k of plane ze+1)
     const float lam = za.lam, s = za.s, m0 = za.m0, m1 = za.m1;
+    const float nzero = neg_zero(lam);
 
     if (tid == 0) {
         for (int k = 0; k <= Z2_STAGES; ++k) mbar_init(&bars[k], 1);
@@ -258,7 +260,7 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
         const float left = my_c > 0 ? R0[rr - 1] : 0.0f;
         const float4 r2lo = lo ? lds4(lo + rr) : f4zero();
         const float4 Z = zquad(lds4(F(st, Z2_OFF_B) + my_row * Z2_BW + my_c), lds4(R0 + rr), lds4(R1 + rr),
-                               lds4(F(st, Z2_OFF_R2) + rr), left, lds4(R1 + rr - Z2_BW), r2lo, lam);
+                               lds4(F(st, Z2_OFF_R2) + rr), left, lds4(R1 + rr - Z2_BW), r2lo, lam, nzero);
         *reinterpret_cast<float4 *>(zkp(q) + my_row * Z2_PK + my_c) = Z;
         return Z;
     };
@@ -268,7 +270,7 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
         const int mo = (ly + 1) * Z2_PK + c + 4;                     // r^{k+1} at (lx = c, ly)
         const float4 Z = zquad(lds4(F(stage(q), Z2_OFF_B) + (ly + 1) * Z2_BW + c + 4), lds4(M0 + mo),
                                lds4(M1 + mo), lds4(M2 + mo), M0[mo - 1], lds4(M1 + mo - Z2_PK),
-                               q > 0 ? lds4(mrp(q - 1, 2) + mo) : f4zero(), lam);
+                               q > 0 ? lds4(mrp(q - 1, 2) + mo) : f4zero(), lam, nzero);
         *reinterpret_cast<float4 *>(z1p(q) + ly * Z2_P1 + c) = Z;
         return Z;
     };
@@ -286,8 +288,8 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     // prologue: z^k of plane f
     {
         bool ok = true;
-        if (f > 0) ok = mbar_wait_tma(&bars[Z2_STAGES], 0);
-        ok = ok && mbar_wait_tma(&bars[slot(f)], parity(f));
+        if (f > 0) ok = mbar_wait_tma(&bars[Z2_STAGES], 0, za.max_polls);
+        ok = ok && mbar_wait_tma(&bars[slot(f)], parity(f), za.max_polls);
         if (ok) {
             if (doA)
                 ZKc = zk_quad(f, stage(f), f > 0 ? reinterpret_cast<const float *>(smem + Z2_OFF_PREV) : nullptr);
@@ -310,7 +312,7 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
         // ---- A: z^k of plane q+1 -------------------------------------------
         float4 ZKn = f4zero();
         if (q + 1 <= last) {
-            if (mbar_wait_tma(&bars[slot(q + 1)], parity(q + 1))) {
+            if (mbar_wait_tma(&bars[slot(q + 1)], parity(q + 1), za.max_polls)) {
                 if (doA) ZKn = zk_quad(q + 1, stage(q + 1), F(stage(q), Z2_OFF_R2));
             } else {
                 *abort_flag = 1;
@@ -336,23 +338,17 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
             float4 P0 = lds4(F(st, Z2_OFF_P0) + po), P1 = lds4(F(st, Z2_OFF_P1) + po),
                    P2 = lds4(F(st, Z2_OFF_P2) + po);
             const bool gy = y < ny - 1;
-            const float zcv[5] = {zc.x, zc.y, zc.z, zc.w, zx};
-            const float zyv[4] = {zy.x, zy.y, zy.z, zy.w};
-            const float zzv[4] = {zz.x, zz.y, zz.z, zz.w};
-            float4 G0, G1, G2;
-            float *g0 = &G0.x, *g1 = &G1.x, *g2 = &G2.x;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                g0[e] = __fsub_rn(zcv[e], zcv[e + 1]);
-                g1[e] = gy ? __fsub_rn(zcv[e], zyv[e]) : 0.0f;
-                g2[e] = hasZ ? __fsub_rn(zcv[e], zzv[e]) : 0.0f;
-            }
+            float4 G0 = make_float4(__fsub_rn(zc.x, zc.y), __fsub_rn(zc.y, zc.z), __fsub_rn(zc.z, zc.w),
+                                    __fsub_rn(zc.w, zx));
+            const float4 G1 = gy ? sub4_rn(zc, zy) : f4zero();
+            const float4 G2 = hasZ ? sub4_rn(zc, zz) : f4zero();
             if (edge) {
+                float *g0 = &G0.x;
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     if (!(x + e < nx - 1)) g0[e] = 0.0f;
             }
-            dual_update4(R0, R1, R2, G0, G1, G2, P0, P1, P2, s, m0);
+            dual_update4(R0, R1, R2, G0, G1, G2, P0, P1, P2, s, m0, nzero);
             // voxels of the ring outside the volume: r^{k+1} = 0, the r(-1) = 0
             // boundary of step k+1 (their p is never used)
             if (edge) {
@@ -404,18 +400,11 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
                 float4 R0 = lds4(mrp(qd, 0) + mo), R1 = lds4(mrp(qd, 1) + mo), R2 = lds4(mrp(qd, 2) + mo);
                 float4 P0 = cP0, P1 = cP1, P2 = cP2;
                 const bool gy = y < ny - 1;
-                float4 G1 = f4zero(), G2 = f4zero();
-                if (gy) {
-                    G1.x = __fsub_rn(zc.x, zy.x); G1.y = __fsub_rn(zc.y, zy.y);
-                    G1.z = __fsub_rn(zc.z, zy.z); G1.w = __fsub_rn(zc.w, zy.w);
-                }
-                if (hasZ) {
-                    G2.x = __fsub_rn(zc.x, zz.x); G2.y = __fsub_rn(zc.y, zz.y);
-                    G2.z = __fsub_rn(zc.z, zz.z); G2.w = __fsub_rn(zc.w, zz.w);
-                }
+                const float4 G1 = gy ? sub4_rn(zc, zy) : f4zero();
+                const float4 G2 = hasZ ? sub4_rn(zc, zz) : f4zero();
                 const float gx3 = (x + 3 < nx - 1) ? __fsub_rn(zc.w, zx) : 0.0f;
                 const float4 G0 = make_float4(__fsub_rn(zc.x, zc.y), __fsub_rn(zc.y, zc.z), __fsub_rn(zc.z, zc.w), gx3);
-                dual_update4(R0, R1, R2, G0, G1, G2, P0, P1, P2, s, m1);
+                dual_update4(R0, R1, R2, G0, G1, G2, P0, P1, P2, s, m1, nzero);
                 const long long i = x + (long long)opx * (y + (long long)ny * qd);
                 if (!PADDED_OUT) {
                     st4(p0d + i, P0);
@@ -563,6 +552,7 @@ inline bool zmarch2_fill(const Zmarch2Plan &plan, const float *b, const float *p
     for (int k = 0; k < 4; ++k) za.tap[k] = plan.tap[k];
     za.opx = nx;
     za.No = N;
+    za.max_polls = ZM_MAX_POLLS;
     return zm_encode(&za.tb, b, nx, ny, nz, Z2_BW, Z2_HB) &&
            zm_encode(&za.tr0, r_src, nx, ny, nz, Z2_BW, Z2_HR) &&
            zm_encode(&za.tr1, r_src + N, nx, ny, nz, Z2_BW, Z2_HR) &&

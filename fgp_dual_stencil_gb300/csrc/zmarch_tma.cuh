@@ -75,7 +75,8 @@ namespace tvfgp {
 #ifndef TVFGP_ZM_L2PROMO
 #define TVFGP_ZM_L2PROMO CU_TENSOR_MAP_L2_PROMOTION_L2_256B
 #endif
-constexpr int ZM_MAX_POLLS = 1 << 22;     // bound of every barrier wait
+constexpr int ZM_MAX_POLLS = 1 << 22;     // bound of every barrier wait, in polls ...
+constexpr unsigned long long ZM_MAX_WAIT_NS = 1000000000ull;   // ... and in time (1 s)
 
 constexpr int zm_round128(int v) { return (v + 127) / 128 * 128; }
 
@@ -150,6 +151,7 @@ struct ZmarchArgsT {
     StepArgsT<TS> a;
     int *err;
     int zc;                       // planes per CTA (grid.z = ceil(nz / zc))
+    int max_polls;                // bound of the waits for data (the drain after a timeout keeps ZM_MAX_POLLS)
 };
 using ZmarchArgs = ZmarchArgsT<float>;
 
@@ -177,10 +179,29 @@ __device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_wait_tma(uint64_t *bar, uint32_t parity)
+__device__ __forceinline__ unsigned long long globaltimer_ns()
 {
-    for (int k = 0; k < ZM_MAX_POLLS; ++k)
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase with the given parity, at most `polls` polls (a poll
+// may suspend the thread for a hardware-defined time) and, from the 256th
+// poll on, at most ZM_MAX_WAIT_NS of wall-clock time.  False: gave up.
+__device__ __forceinline__ bool mbar_wait_tma(uint64_t *bar, uint32_t parity, int polls = ZM_MAX_POLLS)
+{
+    unsigned long long start = 0;
+    for (int k = 0; k < polls; ++k) {
         if (mbar_try(bar, parity)) return true;
+        if ((k & 255) == 255) {
+            const unsigned long long now = globaltimer_ns();
+            if (k == 255)
+                start = now;
+            else if (now - start > ZM_MAX_WAIT_NS)
+                return false;
+        }
+    }
     return false;
 }
 
@@ -216,7 +237,7 @@ __device__ __forceinline__ void zm_quad(const unsigned char *st, int row, int qx
     R1 = lds4(S1 + (row + 1) * L::RW + c);
     const float4 R1lo = lds4(S1 + row * L::RW + c);
     R2 = lds4(S2 + row * L::RW + c);
-    Z = zquad(Bq, R0, R1, R2, left, R1lo, r2lo, lam);
+    Z = zquad(Bq, R0, R1, R2, left, R1lo, r2lo, lam, neg_zero(lam));
 }
 
 // z at column x0+TX of a row (the x+1 neighbour of the tile's last quad).
@@ -308,12 +329,12 @@ __global__ void __launch_bounds__(ZmLayout<TS>::THREADS, ZmLayout<TS>::MINB)
         float4 r2lo = f4zero();
         float r2lo_h = 0.0f;
         if (z0 > 0) {
-            ok = mbar_wait_tma(&bars[L::STAGES], 0);
+            ok = mbar_wait_tma(&bars[L::STAGES], 0, za.max_polls);
             const TS *P2 = reinterpret_cast<const TS *>(smem + L::OFF_PREV);
             r2lo = lds4(P2 + row * L::RW + 4 * qx);
             if (do_halo) r2lo_h = lds1(P2 + hrow * L::RW + L::TX);
         }
-        ok = ok && mbar_wait_tma(&bars[0], 0);
+        ok = ok && mbar_wait_tma(&bars[0], 0, za.max_polls);
         if (ok) {
             const unsigned char *st = stage_of(z0);
             zm_quad<TS>(st, row, qx, r2lo, lam, Rc0, Rc1, Rc2, Zc);
@@ -339,7 +360,7 @@ __global__ void __launch_bounds__(ZmLayout<TS>::THREADS, ZmLayout<TS>::MINB)
         float4 Rn0 = f4zero(), Rn1 = f4zero(), Rn2 = f4zero(), Zn = f4zero();
         float r2halo_n = 0.0f;
         if (hasZ) {
-            if (mbar_wait_tma(&bars[(z + 1 - z0) % L::STAGES], parity_of(z + 1))) {
+            if (mbar_wait_tma(&bars[(z + 1 - z0) % L::STAGES], parity_of(z + 1), za.max_polls)) {
                 const unsigned char *st = stage_of(z + 1);
                 zm_quad<TS>(st, row, qx, Rc2, lam, Rn0, Rn1, Rn2, Zn);
                 float *zr = zrow(z + 1, row);
@@ -379,7 +400,7 @@ __global__ void __launch_bounds__(ZmLayout<TS>::THREADS, ZmLayout<TS>::MINB)
             }
             float4 N0 = Rc0, N1 = Rc1, N2 = Rc2;
             const float4 G0 = make_float4(__fsub_rn(Zc.x, Zc.y), __fsub_rn(Zc.y, Zc.z), __fsub_rn(Zc.z, Zc.w), gx3);
-            dual_update4(N0, N1, N2, G0, G1, G2, P0, P1, P2, s, m);
+            dual_update4(N0, N1, N2, G0, G1, G2, P0, P1, P2, s, m, neg_zero(lam));
             stv(p0 + i, P0);
             stv(p1 + i, P1);
             stv(p2 + i, P2);
@@ -508,6 +529,7 @@ inline bool zmarch_fill(const ZmarchPlan &plan, const StepArgsT<TS> &a, int *err
     za.a = a;
     za.err = err;
     za.zc = plan.zc;
+    za.max_polls = ZM_MAX_POLLS;
     const TS *r = a.rs;
     return zm_encode(&za.tp0, a.p, a.nx, a.ny, a.nz, L::TX, L::TY) &&
            zm_encode(&za.tp1, a.p + a.N, a.nx, a.ny, a.nz, L::TX, L::TY) &&

@@ -68,6 +68,7 @@ def _load():
         "tvfgp_last_variant": ([vp], i),
         "tvfgp_launch_count": ([vp], ll),
         "tvfgp_debug_timeout_probe": ([vp, i, vp], i),
+        "tvfgp_debug_set_poll_limit": ([vp, i], i),
         "tvfgp_debug_fail_allocs": ([i, i], i),
         "tvfgp_debug_plan": ([i, i, i, i, i, i, d, ctypes.POINTER(i), ctypes.POINTER(i), ctypes.POINTER(i),
                               ctypes.POINTER(f), i, ctypes.POINTER(i)], i),
@@ -75,6 +76,7 @@ def _load():
                                 ctypes.POINTER(i)], i),
         "tvfgp_debug_projection_check": ([i, ctypes.c_ulonglong, ctypes.c_ulonglong, vp, vp], i),
         "tvfgp_run_noalloc": ([i, i, i, vp, vp, vp, f, i, d, vp, ctypes.POINTER(d)], i),
+        "tvfgp_debug_noalloc_scratch": ([ctypes.POINTER(vp), ctypes.POINTER(ctypes.c_ulonglong)], i),
         "tvfgp_host_alloc": ([ctypes.c_size_t, i, ctypes.POINTER(vp)], i),
         "tvfgp_run_f16": ([vp, vp, vp, vp, f, i, d, vp, ctypes.POINTER(d)], i),
         "tvfgp_primal_f16": ([vp, vp, vp, f, vp, vp], i),
@@ -303,6 +305,12 @@ def tvfgp_debug_timeout_probe(h: int, spins: int, stream=None) -> None:
     _ok(_lib.tvfgp_debug_timeout_probe(h, int(spins), _stream(stream)), "tvfgp_debug_timeout_probe")
 
 
+def tvfgp_debug_set_poll_limit(h: int, polls: int) -> None:
+    """Polls each wait for data of the TMA kernels makes before giving up
+    (0: at once; < 0: the default).  Test hook; no work of h in flight."""
+    _ok(_lib.tvfgp_debug_set_poll_limit(h, int(polls)), "tvfgp_debug_set_poll_limit")
+
+
 TVFGP_NOALLOC_MAX_VOXELS = 2097152
 
 
@@ -347,6 +355,15 @@ def host_tensor(shape, write_combined: bool = False):
     arr = np.ctypeslib.as_array((ctypes.c_float * n).from_address(addr)).reshape(tuple(shape))
     weakref.finalize(arr, _lib.tvfgp_host_free, addr)
     return torch.from_numpy(arr)
+
+
+def tvfgp_debug_noalloc_scratch() -> tuple[int, int]:
+    """(device address, bytes) of tvfgp_run_noalloc's built-in array on the
+    current device (test hook)."""
+    addr, size = ctypes.c_void_p(), ctypes.c_ulonglong()
+    _ok(_lib.tvfgp_debug_noalloc_scratch(ctypes.byref(addr), ctypes.byref(size)),
+        "tvfgp_debug_noalloc_scratch")
+    return int(addr.value or 0), int(size.value)
 
 
 def raw_call(name: str, *args) -> int:

@@ -245,6 +245,18 @@ int tvfgp_host_free(void *p);
  * reports TVFGP_ERR_TIMEOUT.  1 <= spins <= 2^24. */
 int tvfgp_debug_timeout_probe(tvfgp_t h, int spins, tvfgp_stream_t stream);
 
+/* Test hook (no counterpart on the page): the number of polls every wait
+ * for data of the TMA kernels (ZMARCH_TMA, ZMARCH2_TMA, CUBE_TMA, and the
+ * binary16 z-march) makes before it gives up, for later calls on h (and its
+ * padded-row shadow).  0 makes the first wait of every CTA give up at once,
+ * so a test can drive the kernels' own timeout path: the CTA records
+ * TVFGP_ERR_TIMEOUT in the handle's error word (read by tvfgp_check), waits
+ * for its copies still in flight with the full bound and returns; the
+ * outputs of that call are invalid.  polls < 0 restores the default (2^22
+ * polls, and at most one second, per wait); polls > 2^22 is TVFGP_ERR_ARG.
+ * Drops the handle's cached graphs: call it with no work of h in flight. */
+int tvfgp_debug_set_poll_limit(tvfgp_t h, int polls);
+
 /* Test hook for allocation failures: of the library's next device
  * allocations (handle scratch, error word, extra dual sets, z volume,
  * packed staging), the first `skip` succeed and the `count` after them fail
@@ -285,7 +297,7 @@ int tvfgp_debug_chunks(int nx, int ny, int nz, int slots, int *zc, int *z0, int 
  * must give the same bits (the page's step is defined by the exact
  * operations; this check has no counterpart there).  Enqueues one kernel on
  * `stream`:
- *   mode 0: all floats nn in (1, 2^100): its square root and reciprocal
+ *   mode 0: all floats nn in [1, 2^100): its square root and reciprocal
  *           against __fsqrt_rn and __frcp_rn (count is ignored);
  *   mode 1: `count` pseudo-random triples q (from `seed`): the whole
  *           projection against the IEEE one;
@@ -326,13 +338,24 @@ int tvfgp_debug_projection_check(int mode, unsigned long long count, unsigned lo
  *     value before the next step reads it), but calls whose work overlaps on
  *     the GPU (different streams, or different host threads) race on it and
  *     must be serialised by the caller;
- *   - the first call on a device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture is begun on the calling thread.
+ *   - outside stream capture every call looks up the array's device address
+ *     in the current device and context and remembers it with that
+ *     context's id; a call whose stream is being captured does not look it
+ *     up (the lookup may load the module) and uses the remembered address
+ *     only if it belongs to the context current now.  So the first call in
+ *     a context (after a cudaDeviceReset too) must come outside capture:
+ *     under capture it returns TVFGP_ERR_ARG and enqueues nothing;
+ *   - b, p or r overlapping the array returns TVFGP_ERR_ARG.
  * The vector kernel runs when nx % 4 == 0 and b, p, r are 16-byte aligned,
  * the scalar kernel otherwise. */
 int tvfgp_run_noalloc(int nx, int ny, int nz, const float *b, float *p, float *r, float lambda,
                       int nsteps, double t0, tvfgp_stream_t stream, double *t_final);
+
+/* Test hook (no counterpart on the page): the device address and size in
+ * bytes of tvfgp_run_noalloc's built-in array on the current device, looked
+ * up as an uncaptured tvfgp_run_noalloc call does.  NULL arguments:
+ * TVFGP_ERR_ARG; a failed lookup: TVFGP_ERR_CUDA. */
+int tvfgp_debug_noalloc_scratch(void **addr, unsigned long long *bytes);
 
 /* Static description of a status code. */
 const char *tvfgp_strerror(int code);

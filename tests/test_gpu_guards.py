@@ -8,11 +8,9 @@ import pytest
 
 import oracle
 from fgp_dual_stencil_gb300 import synth
+from gpu_util import Guarded
 
 pytestmark = pytest.mark.gpu
-
-GUARD = 16384                                    # elements on each side
-CANARY = np.uint32(0x7FC0BEEF)
 
 
 @pytest.fixture(scope="module")
@@ -21,34 +19,6 @@ def T():
     assert torch.cuda.is_available()
     from fgp_dual_stencil_gb300 import tvfgp
     return tvfgp
-
-
-class Guarded:
-    """A CUDA buffer of n elements inside canary margins."""
-
-    def __init__(self, values, dtype_bits=32):
-        import torch
-        flat = np.ascontiguousarray(values).reshape(-1)
-        self.n = flat.size
-        word = np.uint16 if dtype_bits == 16 else np.uint32
-        canary = word(0x7E5F) if dtype_bits == 16 else CANARY
-        host = np.full(self.n + 2 * GUARD, canary, dtype=word)
-        host[GUARD:GUARD + self.n] = flat.view(word)
-        self.all = torch.from_numpy(host.view(np.int16 if dtype_bits == 16 else np.int32)).cuda()
-        self.view_dtype = torch.float16 if dtype_bits == 16 else torch.float32
-        self.canary = canary
-        self.word = word
-
-    @property
-    def t(self):
-        return self.all[GUARD:GUARD + self.n].view(self.view_dtype)
-
-    def intact(self):
-        host = self.all.cpu().numpy().view(self.word)
-        return bool((host[:GUARD] == self.canary).all() and (host[GUARD + self.n:] == self.canary).all())
-
-    def values(self):
-        return self.all.cpu().numpy().view(self.word)[GUARD:GUARD + self.n]
 
 
 SHAPES = [(5, 3, 7), (36, 13, 9), (68, 27, 21), (132, 9, 11)]

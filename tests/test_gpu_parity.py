@@ -262,6 +262,62 @@ def test_bounded_wait_reports_timeout_and_context_survives(T):
     assert max_diff(host(p), po) == 0.0
 
 
+@pytest.mark.parametrize("variant,steps,f16", [("zmarch2", 6, False), ("zmarch2", 5, False), ("zmarch", 3, False),
+                                               ("cube", 3, False), ("auto", 4, True)])
+def test_step_kernels_own_timeout_path(T, variant, steps, f16):
+    """With a poll limit of 0 every CTA of the TMA kernels gives up at its
+    first wait for data: it must record the timeout, wait for its copies in
+    flight and return, leaving the context usable; with the default limit
+    restored the same handle runs bit for bit as the oracle."""
+    import torch
+    shape = (72, 40, 37)
+    nx, ny, nz = shape
+    lam = 0.06
+    b = synth.random_case(shape, 71)
+    p0 = synth.random_dual(shape, 72, scale=0.4)
+    r0 = synth.random_dual(shape, 73, scale=0.6)
+    if f16:
+        p0, r0 = oracle.float_to_half(p0), oracle.float_to_half(r0)
+
+    def fresh():
+        if f16:
+            return (torch.from_numpy(p0.view(np.float16)).cuda(), torch.from_numpy(r0.view(np.float16)).cuda())
+        return dev(p0), dev(r0)
+
+    bd = dev(b)
+    with T.Tvfgp(nx, ny, nz, variant) as h:
+        run = h.run_f16 if f16 else h.run
+        T.tvfgp_debug_set_poll_limit(h.h, 0)
+        p, r = fresh()
+        run(bd, p, r, lam, steps, 1.0)
+        assert h.check() == T.TVFGP_ERR_TIMEOUT
+        assert h.check() == T.TVFGP_OK
+        T.tvfgp_debug_set_poll_limit(h.h, -1)
+        p, r = fresh()
+        run(bd, p, r, lam, steps, 1.0)
+        assert h.check() == T.TVFGP_OK
+        used = h.last_variant
+    want = {"zmarch2": (T.TVFGP_VARIANT_ZMARCH2_TMA, T.TVFGP_VARIANT_ZMARCH_TMA),
+            "zmarch": (T.TVFGP_VARIANT_ZMARCH_TMA,), "cube": (T.TVFGP_VARIANT_CUBE_TMA,),
+            "auto": (T.TVFGP_VARIANT_ZMARCH_TMA,)}[variant]
+    assert used in want, used
+    po, ro = p0.copy(), r0.copy()
+    if f16:
+        oracle.fgp_run_h16(b, po, ro, lam, steps, 1.0)
+        assert np.array_equal(p.cpu().numpy().view(np.uint16), po)
+        assert np.array_equal(r.cpu().numpy().view(np.uint16), ro)
+    else:
+        oracle.fgp_run(b, po, ro, lam, steps, 1.0)
+        assert np.array_equal(host(p), po) and np.array_equal(host(r), ro)
+
+
+def test_poll_limit_arguments(T):
+    with T.Tvfgp(8, 4, 4) as h:
+        assert T.raw_call("tvfgp_debug_set_poll_limit", h.h, (1 << 22) + 1) == T.TVFGP_ERR_ARG
+        assert T.raw_call("tvfgp_debug_set_poll_limit", None, 0) == T.TVFGP_ERR_ARG
+        assert T.raw_call("tvfgp_debug_set_poll_limit", h.h, 1 << 22) == T.TVFGP_OK
+
+
 @pytest.mark.parametrize("wc", [False, True])
 def test_host_staging_memory_round_trip(T, wc):
     """Pinned (and write-combined) host memory from the library as the source

@@ -28,7 +28,7 @@ def run_check(T, mode, count, seed):
 
 def test_sqrt_and_reciprocal_exhaustive(T):
     bad, first = run_check(T, 0, 0, 0)
-    assert bad == 0, "%d values of |q|^2 in (1, 2^100) differ, the first at %#x" % (bad, 0x3f800001 + first)
+    assert bad == 0, "%d values of |q|^2 in [1, 2^100) differ, the first at %#x" % (bad, 0x3f800000 + first)
 
 
 @pytest.mark.parametrize("seed", [1, 0x5eed])
