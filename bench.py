@@ -118,7 +118,7 @@ class ClockSampler:
     def __init__(self, gpu_id: str | None):
         self.proc = None
         self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
-        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "200"]
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "50"]
         if gpu_id:
             cmd += ["-i", gpu_id]
         try:
@@ -230,6 +230,36 @@ def ncu_traffic(kernel_name: str, nvox: int):
     return float(ent["dram_bytes_per_voxel"]) * nvox
 
 
+def roofline_entry(kname, alg_bytes, launch_s, peak, peak_kind, traffic, steps_per_launch, per_voxel_step,
+                   f16=False):
+    """The bench line's roofline object for the step kernel.  frac: the
+    page's traffic model (algorithmic bytes of one launch) over the launch
+    time, against the measured copy peak; above 1 when a launch does more
+    than one FGP step per pass over memory.  dram_frac: the DRAM bytes ncu
+    measured for one launch (traffic) over the same launch time: the share of
+    HBM bandwidth the kernel actually draws."""
+    achieved = alg_bytes / launch_s / 1e9
+    dram = None if traffic is None else traffic / launch_s / 1e9
+    return {
+        "bound": "hbm",
+        "kernel": kname,
+        "achieved": round(achieved, 1),
+        "peak": peak,
+        "unit": "GB/s",
+        "frac": round(achieved / peak, 4),
+        "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs, copy burst)" % peak_kind
+        if peak_kind == "measured" else "fallback 6.8 TB/s",
+        "traffic": None if traffic is None else round(traffic),
+        "algorithmic_bytes_per_launch": round(alg_bytes),
+        "model": ("28 B per voxel and FGP step (b fp32, p and r binary16)" if f16 else
+                  "52 B per voxel and FGP step (13 fp32 volumes)") + " x voxel-steps per launch",
+        "model_frac": round(achieved / peak, 4),
+        "model_frac_basis": "%g FGP step(s) per launch, %d B per voxel and step" % (steps_per_launch, per_voxel_step),
+        "dram_achieved": None if dram is None else round(dram, 1),
+        "dram_frac": None if dram is None else round(dram / peak, 4),
+    }
+
+
 # ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
@@ -329,7 +359,6 @@ def gpu_arm(args, world, rank, local_rank, dist):
     # launch processes
     per_voxel_step = 28 if f16 else (72 if separate else BYTES_PER_VOXEL_STEP)
     alg_bytes = per_voxel_step * N * steps_per_launch
-    achieved = alg_bytes / launch_s / 1e9
     kname = {T.TVFGP_VARIANT_FUSED: "fgp_step_fused4", T.TVFGP_VARIANT_SCALAR: "fgp_step_scalar",
              T.TVFGP_VARIANT_ZMARCH_TMA: "fgp_step_zmarch_tma",
              T.TVFGP_VARIANT_ZMARCH2_TMA: "fgp_step2_zmarch_tma",
@@ -401,29 +430,8 @@ def gpu_arm(args, world, rank, local_rank, dist):
             "vs_baseline_ref": "RTX 5070 fused kernel, 12.607 ms per FGP step at 512^3 (page figure; "
                                "other hardware, context only)",
         },
-        "roofline": {
-            "bound": "hbm",
-            "kernel": kname,
-            "achieved": round(achieved, 1),
-            "peak": peak,
-            "unit": "GB/s",
-            "frac": round(achieved / peak, 4),
-            "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs, copy burst)" % peak_kind
-            if peak_kind == "measured" else "fallback 6.8 TB/s",
-            "traffic": None if traffic is None else round(traffic),
-            "algorithmic_bytes_per_launch": round(alg_bytes),
-            "model": ("28 B per voxel and FGP step (b fp32, p and r binary16)" if f16 else
-                      "52 B per voxel and FGP step (13 fp32 volumes)") + " x voxel-steps per launch",
-            # frac is the page's traffic model over the launch time: above 1
-            # when a launch does more than one FGP step per pass over memory.
-            # dram_frac is the DRAM bytes ncu measured for one launch over the
-            # same launch time: the fraction of HBM bandwidth actually used.
-            "model_frac": round(achieved / peak, 4),
-            "model_frac_basis": "%g FGP step(s) per launch, %d B per voxel and step"
-                                % (steps_per_launch, per_voxel_step),
-            "dram_achieved": None if traffic is None else round(traffic / launch_s / 1e9, 1),
-            "dram_frac": None if traffic is None else round(traffic / launch_s / 1e9 / peak, 4),
-        },
+        "roofline": roofline_entry(kname, alg_bytes, launch_s, peak, peak_kind, traffic, steps_per_launch,
+                                   per_voxel_step, f16),
         "gpu_launches": launches,
         "e2e": e2e,
         "clocks": clocks,

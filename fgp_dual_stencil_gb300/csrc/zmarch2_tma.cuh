@@ -112,9 +112,11 @@ constexpr int Z2_TASKS_D = Z2_QD * Z2_TY;
 // [0, TASKS_D) own the tile's quads (row-major, QD per row) and run all four
 // phases on them; threads [TASKS_D, TASKS_B) own the ring of the grown tile
 // (its first and last rows, then its left and right quad columns) and run z^k
-// and step k; threads [TASKS_B, TASKS_A) own z^k's extra last row.  The quads
-// of z^{k+1}'s x+1 column and y+1 row go to the threads from TASKS_D on, which
-// are free after the barrier.
+// and step k; threads [TASKS_B, TASKS_A) own z^k's extra last row.  Each
+// z^{k+1} quad (the tile, its x+1 column and its y+1 row) is computed by the
+// thread that computed z^k at the same place one plane earlier, which keeps
+// that quad's b in registers: phase C reads no staged plane, so a stage is
+// free for the next copy right after the first barrier.
 constexpr int Z2_THREADS = (Z2_TASKS_A + 31) / 32 * 32;
 // The thread that issues the copies of the next planes: the last one, in the
 // warp with the least work (none of the tile's four phases).
@@ -123,10 +125,8 @@ constexpr int Z2_THREADS = (Z2_TASKS_A + 31) / 32 * 32;
 #endif
 constexpr int Z2_PRODUCER = TVFGP_Z2_PRODUCER;
 constexpr int Z2_RING_B = Z2_TASKS_B - Z2_TASKS_D;        // 2 QA + 2 TY
-constexpr int Z2_HALO_C = (Z2_TY + 1) + Z2_QD;            // z^{k+1} quads outside the tile
-constexpr int Z2_HALO_T = Z2_THREADS - Z2_TASKS_D;        // threads that take them
 static_assert(Z2_RING_B == 2 * Z2_QA + 2 * Z2_TY && Z2_TASKS_A - Z2_TASKS_B == Z2_QA, "thread roles");
-static_assert(Z2_TASKS_B <= Z2_THREADS && Z2_HALO_T > 0, "thread roles");
+static_assert(Z2_TASKS_B <= Z2_THREADS && Z2_TASKS_A <= Z2_THREADS, "thread roles");
 
 // shared rings, two slots each (a plane is written two iterations after the
 // slot was last read, with a barrier in between); pitches in floats
@@ -136,16 +136,19 @@ constexpr int Z2_RING_ZK = (Z2_TY + 3) * Z2_PK;           // floats per slot
 constexpr int Z2_MR_COMP = (Z2_TY + 2) * Z2_PK;
 constexpr int Z2_RING_MR = 3 * Z2_MR_COMP;
 constexpr int Z2_RING_Z1 = (Z2_TY + 1) * Z2_P1;
-constexpr int Z2_OFF_PREV = Z2_STAGES * Z2_STAGE_STRIDE;  // r2^k of the plane below the first
-constexpr int Z2_OFF_ZK = zm_round128(Z2_OFF_PREV + Z2_BYTES_R);
+constexpr int Z2_OFF_ZK = Z2_STAGES * Z2_STAGE_STRIDE;
 constexpr int Z2_OFF_MR = zm_round128(Z2_OFF_ZK + 2 * Z2_RING_ZK * 4);
 constexpr int Z2_OFF_Z1 = zm_round128(Z2_OFF_MR + 2 * Z2_RING_MR * 4);
+// r2^k of the plane below the first: read only by the prologue, before the
+// z^{k+1} ring is first written, so it shares that ring's memory
+constexpr int Z2_OFF_PREV = Z2_OFF_Z1;
 constexpr int Z2_OFF_BAR = zm_round128(Z2_OFF_Z1 + 2 * Z2_RING_Z1 * 4);
 constexpr int Z2_OFF_FLAG = Z2_OFF_BAR + 8 * (Z2_STAGES + 1);
 constexpr int Z2_SMEM = Z2_OFF_FLAG + 16 + 128;
 
 static_assert(Z2_TX % 4 == 0 && Z2_BW <= 256 && Z2_HR <= 256, "TMA box limits");
 static_assert(Z2_STAGES >= 2, "two stages at least");
+static_assert(Z2_BYTES_R <= 2 * Z2_RING_Z1 * 4, "the prologue's r2 box fits in the z^{k+1} ring");
 static_assert(Z2_SMEM * TVFGP_Z2_MINB <= 227 * 1024, "CTAs per SM must fit in shared memory");
 
 struct Zmarch2Args {
@@ -242,6 +245,9 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     const bool doA = tid < Z2_TASKS_A;
     const bool doB = tid < Z2_TASKS_B;
     const bool my_tile = tid < Z2_TASKS_D;
+    // z^{k+1} runs on lx 0..TX, ly 0..TY: the z^k quads of columns c >= 4
+    // and rows 1..TY+1 (the tile, the ring's right column and its last row)
+    const bool doC = doA && my_c >= 4 && my_row >= 1 && my_row <= Z2_TY + 1;
     // Step k's quads cover lx -4..TX+3, ly -1..TY.  When all of them lie
     // inside the volume and none touches the upper x face, step k needs no
     // per-voxel boundary test (most CTAs of a large volume).
@@ -253,24 +259,25 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
 
     // z^k of plane q for this thread's quad, from the staged plane st and the
     // r2 of the plane below (lo: a staged r2 box, or nullptr at plane 0);
-    // stored for the neighbours and returned
-    auto zk_quad = [&](int q, const unsigned char *st, const float *lo) {
+    // stored for the neighbours and returned, with the quad's b in Bq
+    auto zk_quad = [&](int q, const unsigned char *st, const float *lo, float4 &Bq) {
         const int rr = (my_row + 1) * Z2_BW + my_c;                  // r box row of ly
         const float *R0 = F(st, Z2_OFF_R0), *R1 = F(st, Z2_OFF_R1);
         const float left = my_c > 0 ? R0[rr - 1] : 0.0f;
         const float4 r2lo = lo ? lds4(lo + rr) : f4zero();
-        const float4 Z = zquad(lds4(F(st, Z2_OFF_B) + my_row * Z2_BW + my_c), lds4(R0 + rr), lds4(R1 + rr),
-                               lds4(F(st, Z2_OFF_R2) + rr), left, lds4(R1 + rr - Z2_BW), r2lo, lam, nzero);
+        Bq = lds4(F(st, Z2_OFF_B) + my_row * Z2_BW + my_c);
+        const float4 Z = zquad(Bq, lds4(R0 + rr), lds4(R1 + rr), lds4(F(st, Z2_OFF_R2) + rr), left,
+                               lds4(R1 + rr - Z2_BW), r2lo, lam, nzero);
         *reinterpret_cast<float4 *>(zkp(q) + my_row * Z2_PK + my_c) = Z;
         return Z;
     };
-    // z^{k+1} of plane q for the quad at (c = lx, ly), stored and returned
-    auto z1_quad = [&](int q, int c, int ly) {
+    // z^{k+1} of plane q for the quad at (c = lx, ly) whose b is Bq,
+    // stored and returned
+    auto z1_quad = [&](int q, int c, int ly, float4 Bq) {
         const float *M0 = mrp(q, 0), *M1 = mrp(q, 1), *M2 = mrp(q, 2);
         const int mo = (ly + 1) * Z2_PK + c + 4;                     // r^{k+1} at (lx = c, ly)
-        const float4 Z = zquad(lds4(F(stage(q), Z2_OFF_B) + (ly + 1) * Z2_BW + c + 4), lds4(M0 + mo),
-                               lds4(M1 + mo), lds4(M2 + mo), M0[mo - 1], lds4(M1 + mo - Z2_PK),
-                               q > 0 ? lds4(mrp(q - 1, 2) + mo) : f4zero(), lam, nzero);
+        const float4 Z = zquad(Bq, lds4(M0 + mo), lds4(M1 + mo), lds4(M2 + mo), M0[mo - 1],
+                               lds4(M1 + mo - Z2_PK), q > 0 ? lds4(mrp(q - 1, 2) + mo) : f4zero(), lam, nzero);
         *reinterpret_cast<float4 *>(z1p(q) + ly * Z2_P1 + c) = Z;
         return Z;
     };
@@ -285,6 +292,7 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     int next_issue = f + Z2_STAGES;
 
     float4 ZKc = f4zero();                      // z^k of this quad, current plane
+    float4 Bc = f4zero();                       // b of this quad, current plane
     // prologue: z^k of plane f
     {
         bool ok = true;
@@ -292,7 +300,8 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
         ok = ok && mbar_wait_tma(&bars[slot(f)], parity(f), za.max_polls);
         if (ok) {
             if (doA)
-                ZKc = zk_quad(f, stage(f), f > 0 ? reinterpret_cast<const float *>(smem + Z2_OFF_PREV) : nullptr);
+                ZKc = zk_quad(f, stage(f), f > 0 ? reinterpret_cast<const float *>(smem + Z2_OFF_PREV) : nullptr,
+                              Bc);
         } else {
             *abort_flag = 1;
         }
@@ -310,10 +319,10 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     for (int q = f; q <= ze && *abort_flag == 0; ++q) {
         qlast = q;
         // ---- A: z^k of plane q+1 -------------------------------------------
-        float4 ZKn = f4zero();
+        float4 ZKn = f4zero(), Bn = f4zero();
         if (q + 1 <= last) {
             if (mbar_wait_tma(&bars[slot(q + 1)], parity(q + 1), za.max_polls)) {
-                if (doA) ZKn = zk_quad(q + 1, stage(q + 1), F(stage(q), Z2_OFF_R2));
+                if (doA) ZKn = zk_quad(q + 1, stage(q + 1), F(stage(q), Z2_OFF_R2), Bn);
             } else {
                 *abort_flag = 1;
             }
@@ -371,18 +380,21 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
         ZKc = ZKn;
         __syncthreads();
         if (*abort_flag) break;
+        // every read of plane q's stage is done (phase C takes b from
+        // registers): the slot takes the next plane
+        if (tid == Z2_PRODUCER && next_issue <= last && q <= uk_last) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(next_issue++);
+        }
 
         // ---- C: z^{k+1} of plane q on the tile, its x+1 column and y+1 row ---
+        // (each quad by the thread that computed z^k there, which holds its b)
         float4 Z1n = f4zero();
-        if (q >= z0 && q <= uk_last) {
-            if (my_tile) Z1n = z1_quad(q, my_c - 4, my_row - 1);
-            for (int h = tid - Z2_TASKS_D; h >= 0 && h < Z2_HALO_C; h += Z2_HALO_T) {
-                if (h <= Z2_TY)
-                    z1_quad(q, Z2_TX, h);                            // x+1 column, rows 0..TY
-                else
-                    z1_quad(q, 4 * (h - Z2_TY - 1), Z2_TY);          // y+1 row
-            }
+        if (q >= z0 && q <= uk_last && doC) {
+            const float4 Z = z1_quad(q, my_c - 4, my_row - 1, Bc);
+            if (my_tile) Z1n = Z;
         }
+        Bc = Bn;
         // ---- D: step k+1 on plane q-1 over the tile -> p^{k+2}, r^{k+2} -----
         const int qd = q - 1;
         if (my_tile && qd >= z0 && qd < ze) {
@@ -428,11 +440,6 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
         cP1 = nP1;
         cP2 = nP2;
         __syncthreads();
-        // every read of plane q's stage is done: the slot takes the next plane
-        if (tid == Z2_PRODUCER && next_issue <= last && q <= uk_last) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue(next_issue++);
-        }
     }
 
     if (*abort_flag) {

@@ -56,3 +56,17 @@ def test_committed_traffic_names_the_bench_kernels():
         ent = rec[name]
         assert len(ent["source_hash"]) == 16 and ent["dram_bytes_per_voxel"] > 0
         assert "--clock-control none" in ent["command"]
+
+
+def test_roofline_reports_the_model_and_the_measured_dram_fraction():
+    # a two-step launch of 512^3 voxels: 104 B per voxel by the model, 52.8 B measured
+    n = 512 ** 3
+    r = bench.roofline_entry("fgp_step2_zmarch_tma", 104 * n, 1.25e-3, 6795.5, "measured", 52.8 * n, 2.0, 52)
+    assert r["frac"] == r["model_frac"] == round(104 * n / 1.25e-3 / 1e9 / 6795.5, 4)
+    assert r["frac"] > 1.0 and r["model_frac_basis"].startswith("2 FGP step(s) per launch, 52 B")
+    assert r["dram_achieved"] == round(52.8 * n / 1.25e-3 / 1e9, 1)
+    assert r["dram_frac"] == round(52.8 * n / 1.25e-3 / 1e9 / 6795.5, 4) and r["dram_frac"] < 1.0
+    assert r["traffic"] == round(52.8 * n) and r["bound"] == "hbm" and r["unit"] == "GB/s"
+    none = bench.roofline_entry("fgp_step2_zmarch_tma", 104 * n, 1.25e-3, 6800.0, "fallback", None, 2.0, 52)
+    assert none["traffic"] is None and none["dram_frac"] is None and none["dram_achieved"] is None
+    assert none["peak_source"] == "fallback 6.8 TB/s"
