@@ -52,7 +52,8 @@ struct CubeArgs {
     CUtensorMap tb, t0, t1, t2;   // b, and r0, r1, r2 of the r read by this step
     StepArgs a;
     int *err;
-    int max_polls;                // bound of the wait for data (the drain keeps ZM_MAX_POLLS)
+    int max_polls;                // bound of the wait for data (the drain keeps ZM_MAX_POLLS), ...
+    int poll_from;                // ... if poll_from <= 0 (a CTA waits once, for its only tile)
 };
 
 __global__ void __launch_bounds__(CB_THREADS) fgp_step_cube_tma(const __grid_constant__ CubeArgs ca)
@@ -97,7 +98,7 @@ __global__ void __launch_bounds__(CB_THREADS) fgp_step_cube_tma(const __grid_con
         P2 = ld_once4(a.p + 2 * a.N + i);
     }
     __syncthreads();                                  // the barrier is initialised
-    if (!mbar_wait_tma(bar, 0, ca.max_polls)) *abort_flag = 1;
+    if (!mbar_wait_tma(bar, 0, ca.poll_from <= 0 ? ca.max_polls : ZM_MAX_POLLS)) *abort_flag = 1;
     __syncthreads();
     if (*abort_flag) {
         if (tid == 0) {
@@ -190,6 +191,7 @@ inline bool cube_fill(const StepArgs &a, int *err, CubeArgs &ca)
     ca.a = a;
     ca.err = err;
     ca.max_polls = ZM_MAX_POLLS;
+    ca.poll_from = 0;
     const float *r = a.rs;
     return cube_encode(&ca.tb, a.b, a.nx, a.ny, a.nz, CB_BX, CB_BY, CB_BZ) &&
            cube_encode(&ca.t0, r, a.nx, a.ny, a.nz, CB_RX, CB_RY, CB_RZ) &&

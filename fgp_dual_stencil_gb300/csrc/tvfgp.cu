@@ -152,7 +152,8 @@ struct tvfgp_handle {
     // staging buffers (b, p, r: 7*nx*ny*nz floats), made on first use
     tvfgp_handle *shadow;
     float *pk;
-    int poll_limit;                // bound of the TMA kernels' waits for data (test hook)
+    int poll_limit;                // bound of the TMA kernels' waits for data (test hook) ...
+    int poll_from;                 // ... for the planes of a CTA from this one on
 };
 
 namespace {
@@ -483,6 +484,7 @@ bool fill_item(const tvfgp_handle *h, const Item &it, const float *b_run, float 
             k.ptrs[0] = &k.zah;
             const bool ok = zmarch_fill(h->zplan_h, k.ah, h->d_err, k.zah);
             k.zah.max_polls = h->poll_limit;
+            k.zah.poll_from = h->poll_from;
             return ok;
         }
         k.ptrs[0] = &k.ah;
@@ -521,6 +523,7 @@ bool fill_item(const tvfgp_handle *h, const Item &it, const float *b_run, float 
         const bool ok = zmarch2_fill(h->z2plan, b, it.p_src, it.p_dst, it.r_src, it.r_dst, lam, step_of(lam),
                                      it.m0, it.m1, h->nx, h->ny, h->nz, h->N, h->d_err, k.z2);
         k.z2.max_polls = h->poll_limit;
+        k.z2.poll_from = h->poll_from;
         if (it.kernel == TVFGP_VARIANT_ZMARCH2_TMA) return ok;
         k.z2.opx = it.opx;
         k.z2.No = it.out_n;
@@ -531,12 +534,14 @@ bool fill_item(const tvfgp_handle *h, const Item &it, const float *b_run, float 
         k.ptrs[0] = &k.za;
         const bool ok = zmarch_fill(h->zplan, k.a, h->d_err, k.za);
         k.za.max_polls = h->poll_limit;
+        k.za.poll_from = h->poll_from;
         return ok;
     }
     if (it.kernel == TVFGP_VARIANT_CUBE_TMA) {
         k.ptrs[0] = &k.cb;
         const bool ok = cube_fill(k.a, h->d_err, k.cb);
         k.cb.max_polls = h->poll_limit;
+        k.cb.poll_from = h->poll_from;
         return ok;
     }
     k.ptrs[0] = &k.a;
@@ -960,6 +965,7 @@ static int create_impl(int nx, int ny, int nz, int px, int variant, unsigned fla
     h->shadow = nullptr;
     h->pk = nullptr;
     h->poll_limit = ZM_MAX_POLLS;
+    h->poll_from = 0;
     cudaError_t e = dev_alloc(&h->scratch, sizeof(float) * 3 * static_cast<size_t>(h->N));
     if (e == cudaSuccess) e = dev_alloc(&h->d_err, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(int));
@@ -1391,12 +1397,13 @@ int tvfgp_debug_projection_check(int mode, unsigned long long count, unsigned lo
     return e == cudaSuccess ? TVFGP_OK : from_cuda(e);
 }
 
-int tvfgp_debug_set_poll_limit(tvfgp_t h, int polls)
+int tvfgp_debug_set_poll_limit(tvfgp_t h, int polls, int from_plane)
 {
-    if (!valid(h) || polls > ZM_MAX_POLLS) return TVFGP_ERR_ARG;
+    if (!valid(h) || polls > ZM_MAX_POLLS || from_plane < 0) return TVFGP_ERR_ARG;
     const int lim = polls < 0 ? ZM_MAX_POLLS : polls;
     for (tvfgp_handle *x = h; x != nullptr; x = x->shadow) {
         x->poll_limit = lim;
+        x->poll_from = polls < 0 ? 0 : from_plane;
         for (auto &g : x->graphs) destroy_graph(g);       // rebuilt with the new limit on next use
     }
     return TVFGP_OK;

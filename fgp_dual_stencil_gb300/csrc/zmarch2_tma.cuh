@@ -163,7 +163,8 @@ struct Zmarch2Args {
     int tap[4];                                     // pieces [tap[j], tap[j+1]) after nbig*zc
     int opx;                                        // row pitch of p_dst, r_dst (nx: dense)
     long long No;                                   // their elements per component
-    int max_polls;                                  // bound of the waits for data (drain: ZM_MAX_POLLS)
+    int max_polls;                                  // bound of the waits for data (drain: ZM_MAX_POLLS) ...
+    int poll_from;                                  // ... for planes >= the CTA's first + poll_from
 };
 
 // PADDED_OUT: p_dst and r_dst have rows of opx floats (even), written as
@@ -204,6 +205,7 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     auto slot = [&](int q) { return (q - f) % Z2_STAGES; };
     auto stage = [&](int q) { return smem + slot(q) * Z2_STAGE_STRIDE; };
     auto parity = [&](int q) { return static_cast<uint32_t>(((q - f) / Z2_STAGES) & 1); };
+    auto polls = [&](int q) { return q - f >= za.poll_from ? za.max_polls : ZM_MAX_POLLS; };
     auto issue = [&](int q) {                   // the producer thread only
         unsigned char *st = stage(q);
         uint64_t *bar = &bars[slot(q)];
@@ -296,8 +298,8 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     // prologue: z^k of plane f
     {
         bool ok = true;
-        if (f > 0) ok = mbar_wait_tma(&bars[Z2_STAGES], 0, za.max_polls);
-        ok = ok && mbar_wait_tma(&bars[slot(f)], parity(f), za.max_polls);
+        if (f > 0) ok = mbar_wait_tma(&bars[Z2_STAGES], 0, polls(f));
+        ok = ok && mbar_wait_tma(&bars[slot(f)], parity(f), polls(f));
         if (ok) {
             if (doA)
                 ZKc = zk_quad(f, stage(f), f > 0 ? reinterpret_cast<const float *>(smem + Z2_OFF_PREV) : nullptr,
@@ -321,7 +323,7 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
         // ---- A: z^k of plane q+1 -------------------------------------------
         float4 ZKn = f4zero(), Bn = f4zero();
         if (q + 1 <= last) {
-            if (mbar_wait_tma(&bars[slot(q + 1)], parity(q + 1), za.max_polls)) {
+            if (mbar_wait_tma(&bars[slot(q + 1)], parity(q + 1), polls(q + 1))) {
                 if (doA) ZKn = zk_quad(q + 1, stage(q + 1), F(stage(q), Z2_OFF_R2), Bn);
             } else {
                 *abort_flag = 1;
@@ -443,8 +445,12 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     }
 
     if (*abort_flag) {
+        // A wait gave up.  Record it, then drain (bounded) every copy this
+        // CTA issued that is still in flight: plane qlast+1 (whose wait
+        // failed, or f when the prologue failed) and every later plane
+        // issued.  The producer issued them and alone knows how many.
         __syncthreads();
-        if (tid == 0) {
+        if (tid == Z2_PRODUCER) {
             atomicExch(za.err, kErrTimeout);
             if (f > 0 && qlast < f) mbar_wait_tma(&bars[Z2_STAGES], 0);
             for (int q = qlast + 1; q < next_issue && q <= last; ++q)
@@ -560,6 +566,7 @@ inline bool zmarch2_fill(const Zmarch2Plan &plan, const float *b, const float *p
     za.opx = nx;
     za.No = N;
     za.max_polls = ZM_MAX_POLLS;
+    za.poll_from = 0;
     return zm_encode(&za.tb, b, nx, ny, nz, Z2_BW, Z2_HB) &&
            zm_encode(&za.tr0, r_src, nx, ny, nz, Z2_BW, Z2_HR) &&
            zm_encode(&za.tr1, r_src + N, nx, ny, nz, Z2_BW, Z2_HR) &&

@@ -151,7 +151,8 @@ struct ZmarchArgsT {
     StepArgsT<TS> a;
     int *err;
     int zc;                       // planes per CTA (grid.z = ceil(nz / zc))
-    int max_polls;                // bound of the waits for data (the drain after a timeout keeps ZM_MAX_POLLS)
+    int max_polls;                // bound of the waits for data (the drain after a timeout keeps ZM_MAX_POLLS) ...
+    int poll_from;                // ... for planes >= the CTA's first + poll_from
 };
 using ZmarchArgs = ZmarchArgsT<float>;
 
@@ -329,12 +330,12 @@ __global__ void __launch_bounds__(ZmLayout<TS>::THREADS, ZmLayout<TS>::MINB)
         float4 r2lo = f4zero();
         float r2lo_h = 0.0f;
         if (z0 > 0) {
-            ok = mbar_wait_tma(&bars[L::STAGES], 0, za.max_polls);
+            ok = mbar_wait_tma(&bars[L::STAGES], 0, za.poll_from <= 0 ? za.max_polls : ZM_MAX_POLLS);
             const TS *P2 = reinterpret_cast<const TS *>(smem + L::OFF_PREV);
             r2lo = lds4(P2 + row * L::RW + 4 * qx);
             if (do_halo) r2lo_h = lds1(P2 + hrow * L::RW + L::TX);
         }
-        ok = ok && mbar_wait_tma(&bars[0], 0, za.max_polls);
+        ok = ok && mbar_wait_tma(&bars[0], 0, za.poll_from <= 0 ? za.max_polls : ZM_MAX_POLLS);
         if (ok) {
             const unsigned char *st = stage_of(z0);
             zm_quad<TS>(st, row, qx, r2lo, lam, Rc0, Rc1, Rc2, Zc);
@@ -360,7 +361,8 @@ __global__ void __launch_bounds__(ZmLayout<TS>::THREADS, ZmLayout<TS>::MINB)
         float4 Rn0 = f4zero(), Rn1 = f4zero(), Rn2 = f4zero(), Zn = f4zero();
         float r2halo_n = 0.0f;
         if (hasZ) {
-            if (mbar_wait_tma(&bars[(z + 1 - z0) % L::STAGES], parity_of(z + 1), za.max_polls)) {
+            if (mbar_wait_tma(&bars[(z + 1 - z0) % L::STAGES], parity_of(z + 1),
+                              z + 1 - z0 >= za.poll_from ? za.max_polls : ZM_MAX_POLLS)) {
                 const unsigned char *st = stage_of(z + 1);
                 zm_quad<TS>(st, row, qx, Rc2, lam, Rn0, Rn1, Rn2, Zn);
                 float *zr = zrow(z + 1, row);
@@ -530,6 +532,7 @@ inline bool zmarch_fill(const ZmarchPlan &plan, const StepArgsT<TS> &a, int *err
     za.err = err;
     za.zc = plan.zc;
     za.max_polls = ZM_MAX_POLLS;
+    za.poll_from = 0;
     const TS *r = a.rs;
     return zm_encode(&za.tp0, a.p, a.nx, a.ny, a.nz, L::TX, L::TY) &&
            zm_encode(&za.tp1, a.p + a.N, a.nx, a.ny, a.nz, L::TX, L::TY) &&

@@ -68,7 +68,7 @@ def _load():
         "tvfgp_last_variant": ([vp], i),
         "tvfgp_launch_count": ([vp], ll),
         "tvfgp_debug_timeout_probe": ([vp, i, vp], i),
-        "tvfgp_debug_set_poll_limit": ([vp, i], i),
+        "tvfgp_debug_set_poll_limit": ([vp, i, i], i),
         "tvfgp_debug_fail_allocs": ([i, i], i),
         "tvfgp_debug_plan": ([i, i, i, i, i, i, d, ctypes.POINTER(i), ctypes.POINTER(i), ctypes.POINTER(i),
                               ctypes.POINTER(f), i, ctypes.POINTER(i)], i),
@@ -305,10 +305,11 @@ def tvfgp_debug_timeout_probe(h: int, spins: int, stream=None) -> None:
     _ok(_lib.tvfgp_debug_timeout_probe(h, int(spins), _stream(stream)), "tvfgp_debug_timeout_probe")
 
 
-def tvfgp_debug_set_poll_limit(h: int, polls: int) -> None:
+def tvfgp_debug_set_poll_limit(h: int, polls: int, from_plane: int = 0) -> None:
     """Polls each wait for data of the TMA kernels makes before giving up
-    (0: at once; < 0: the default).  Test hook; no work of h in flight."""
-    _ok(_lib.tvfgp_debug_set_poll_limit(h, int(polls)), "tvfgp_debug_set_poll_limit")
+    (0: at once; < 0: the default), for each CTA's planes from from_plane on.
+    Test hook; no work of h in flight."""
+    _ok(_lib.tvfgp_debug_set_poll_limit(h, int(polls), int(from_plane)), "tvfgp_debug_set_poll_limit")
 
 
 TVFGP_NOALLOC_MAX_VOXELS = 2097152

@@ -245,17 +245,20 @@ int tvfgp_host_free(void *p);
  * reports TVFGP_ERR_TIMEOUT.  1 <= spins <= 2^24. */
 int tvfgp_debug_timeout_probe(tvfgp_t h, int spins, tvfgp_stream_t stream);
 
-/* Test hook (no counterpart on the page): the number of polls every wait
- * for data of the TMA kernels (ZMARCH_TMA, ZMARCH2_TMA, CUBE_TMA, and the
- * binary16 z-march) makes before it gives up, for later calls on h (and its
- * padded-row shadow).  0 makes the first wait of every CTA give up at once,
- * so a test can drive the kernels' own timeout path: the CTA records
- * TVFGP_ERR_TIMEOUT in the handle's error word (read by tvfgp_check), waits
- * for its copies still in flight with the full bound and returns; the
- * outputs of that call are invalid.  polls < 0 restores the default (2^22
- * polls, and at most one second, per wait); polls > 2^22 is TVFGP_ERR_ARG.
- * Drops the handle's cached graphs: call it with no work of h in flight. */
-int tvfgp_debug_set_poll_limit(tvfgp_t h, int polls);
+/* Test hook (no counterpart on the page): the number of polls a wait for
+ * data of the TMA kernels (ZMARCH_TMA, ZMARCH2_TMA, CUBE_TMA, and the
+ * binary16 z-march) makes before it gives up, for the planes of each CTA
+ * from its from_plane-th on (a cube CTA has one wait, for plane 0), for
+ * later calls on h (and its padded-row shadow).  polls = 0 makes those
+ * waits give up at once, so a test can drive the kernels' own timeout path,
+ * at the first wait (from_plane 0) or in the middle of a march with copies
+ * in flight: the CTA records TVFGP_ERR_TIMEOUT in the handle's error word
+ * (read by tvfgp_check), waits for its copies still in flight with the full
+ * bound and returns; the outputs of that call are invalid.  polls < 0
+ * restores the default (2^22 polls, and at most one second, per wait);
+ * polls > 2^22 or from_plane < 0 is TVFGP_ERR_ARG.  Drops the handle's
+ * cached graphs: call it with no work of h in flight. */
+int tvfgp_debug_set_poll_limit(tvfgp_t h, int polls, int from_plane);
 
 /* Test hook for allocation failures: of the library's next device
  * allocations (handle scratch, error word, extra dual sets, z volume,

@@ -262,13 +262,17 @@ def test_bounded_wait_reports_timeout_and_context_survives(T):
     assert max_diff(host(p), po) == 0.0
 
 
-@pytest.mark.parametrize("variant,steps,f16", [("zmarch2", 6, False), ("zmarch2", 5, False), ("zmarch", 3, False),
-                                               ("cube", 3, False), ("auto", 4, True)])
-def test_step_kernels_own_timeout_path(T, variant, steps, f16):
+@pytest.mark.parametrize("variant,steps,f16,from_plane", [
+    ("zmarch2", 6, False, 0), ("zmarch2", 5, False, 0), ("zmarch2", 6, False, 4), ("zmarch2", 4, False, 6),
+    ("zmarch", 3, False, 0), ("zmarch", 3, False, 5), ("cube", 3, False, 0), ("auto", 4, True, 0),
+    ("auto", 4, True, 3)])
+def test_step_kernels_own_timeout_path(T, variant, steps, f16, from_plane):
     """With a poll limit of 0 every CTA of the TMA kernels gives up at its
-    first wait for data: it must record the timeout, wait for its copies in
-    flight and return, leaving the context usable; with the default limit
-    restored the same handle runs bit for bit as the oracle."""
+    first wait for data of plane from_plane or later (the first wait, or in
+    the middle of the march with copies of later planes in flight): it must
+    record the timeout, wait for its copies in flight and return, leaving the
+    context usable; with the default limit restored the same handle runs bit
+    for bit as the oracle."""
     import torch
     shape = (72, 40, 37)
     nx, ny, nz = shape
@@ -287,7 +291,7 @@ def test_step_kernels_own_timeout_path(T, variant, steps, f16):
     bd = dev(b)
     with T.Tvfgp(nx, ny, nz, variant) as h:
         run = h.run_f16 if f16 else h.run
-        T.tvfgp_debug_set_poll_limit(h.h, 0)
+        T.tvfgp_debug_set_poll_limit(h.h, 0, from_plane)
         p, r = fresh()
         run(bd, p, r, lam, steps, 1.0)
         assert h.check() == T.TVFGP_ERR_TIMEOUT
@@ -313,9 +317,11 @@ def test_step_kernels_own_timeout_path(T, variant, steps, f16):
 
 def test_poll_limit_arguments(T):
     with T.Tvfgp(8, 4, 4) as h:
-        assert T.raw_call("tvfgp_debug_set_poll_limit", h.h, (1 << 22) + 1) == T.TVFGP_ERR_ARG
-        assert T.raw_call("tvfgp_debug_set_poll_limit", None, 0) == T.TVFGP_ERR_ARG
-        assert T.raw_call("tvfgp_debug_set_poll_limit", h.h, 1 << 22) == T.TVFGP_OK
+        assert T.raw_call("tvfgp_debug_set_poll_limit", h.h, (1 << 22) + 1, 0) == T.TVFGP_ERR_ARG
+        assert T.raw_call("tvfgp_debug_set_poll_limit", h.h, 0, -1) == T.TVFGP_ERR_ARG
+        assert T.raw_call("tvfgp_debug_set_poll_limit", None, 0, 0) == T.TVFGP_ERR_ARG
+        assert T.raw_call("tvfgp_debug_set_poll_limit", h.h, 1 << 22, 3) == T.TVFGP_OK
+        assert T.raw_call("tvfgp_debug_set_poll_limit", h.h, -1, 0) == T.TVFGP_OK
 
 
 @pytest.mark.parametrize("wc", [False, True])

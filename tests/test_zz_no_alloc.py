@@ -9,9 +9,10 @@ its second r buffer in a fixed array compiled into the library.
 These tests check, over two calls in a row, that its results equal the CPU
 oracle's and tvfgp_run's bit for bit and that the calls leave the free device
 memory unchanged; that a volume above the fixed capacity is refused; that
-buffers overlapping the built-in array are refused before anything runs; and
-that a first call in a process made under stream capture is refused.  The
-file is named to be collected last."""
+buffers overlapping the built-in array are refused before anything runs;
+that it writes nothing outside the caller's buffers (guard bands); and that
+a first call in a process made under stream capture is refused.  The file is
+named to be collected last."""
 import ctypes
 import os
 import subprocess
@@ -128,6 +129,31 @@ def test_noalloc_refuses_buffers_inside_its_array():
             assert fn(16, 8, 4, *args, 0.05, 3, 1.0, stream, ctypes.byref(tf)) == T.TVFGP_ERR_ARG
     torch.cuda.synchronize()
     assert torch.equal(p, before[0]) and torch.equal(r, before[1])
+
+
+@pytest.mark.parametrize("shape", [(36, 13, 9), (5, 3, 7)])
+def test_noalloc_writes_nothing_outside_the_buffers(shape):
+    """Guard bands with a NaN canary around b, p and r; two calls in a row
+    (vector kernel for nx % 4 == 0, scalar kernel otherwise)."""
+    from gpu_util import Guarded
+    T, fn = c_entry()
+    nx, ny, nz = shape
+    b = synth.random_case(shape, 91)
+    p0 = synth.random_dual(shape, 92, scale=0.4)
+    r0 = synth.random_dual(shape, 93, scale=0.6)
+    gb, gp, gr = Guarded(b), Guarded(p0), Guarded(r0)
+    tf = ctypes.c_double(0.0)
+    assert fn(nx, ny, nz, gb.t.data_ptr(), gp.t.data_ptr(), gr.t.data_ptr(), 0.07, 5, 1.0, None,
+              ctypes.byref(tf)) == T.TVFGP_OK
+    assert fn(nx, ny, nz, gb.t.data_ptr(), gp.t.data_ptr(), gr.t.data_ptr(), 0.07, 2, tf.value, None,
+              ctypes.byref(tf)) == T.TVFGP_OK
+    for name, g in (("b", gb), ("p", gp), ("r", gr)):
+        assert g.intact(), "%s: a canary was overwritten (%s)" % (name, shape)
+    po, ro = p0.copy(), r0.copy()
+    t = oracle.fgp_run(b, po, ro, 0.07, 5, 1.0)
+    oracle.fgp_run(b, po, ro, 0.07, 2, t)
+    assert np.array_equal(gp.values().view(np.float32), po.reshape(-1))
+    assert np.array_equal(gr.values().view(np.float32), ro.reshape(-1))
 
 
 CAPTURE_FIRST = r"""
