@@ -63,6 +63,9 @@ def parse_args():
                     help="page-locked host staging of b for the end-to-end run: write-combined or cached")
     ap.add_argument("--z-host", default="pinned", choices=["wc", "pinned"],
                     help="page-locked host memory receiving z in the end-to-end run: write-combined or cached")
+    ap.add_argument("--copy-streams", type=int, default=1,
+                    help="end-to-end run: each step's H2D of b and D2H of z split into this many chunks "
+                         "along z, each on its own stream (so several copy engines work at once)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -376,11 +379,12 @@ def gpu_arm(args, world, rank, local_rank, dist):
     e2e = None
     if not args.no_e2e:
         e2e_s = end_to_end(torch, h, w, b_host, p, r, stream, dev, K, dist, run, primal,
-                           z_wc=args.z_host == "wc")
+                           z_wc=args.z_host == "wc", copy_streams=args.copy_streams)
         e2e = {"value": round(world * N * w.steps * K / e2e_s / 1e9, 3), "unit": UNIT,
                "h2d_bytes_per_step": 4 * w.ny * w.nz * pitch, "d2h_bytes_per_step": 4 * w.ny * w.nz * pitch,
                "ms_per_step": round(e2e_s * 1e3 / K, 4),
-               "overlap": "H2D of step j+1 and D2H of step j on two copy streams, double-buffered",
+               "overlap": "H2D of step j+1 and D2H of step j, each split along z into %d chunks on %d "
+                          "streams, double-buffered" % (args.copy_streams, args.copy_streams),
                "host_memory": "b from %s, z to %s page-locked memory (tvfgp_host_alloc)"
                               % ("write-combined" if args.b_host == "wc" else "cached",
                                  "write-combined" if args.z_host == "wc" else "cached")}
@@ -440,28 +444,35 @@ def gpu_arm(args, world, rank, local_rank, dist):
     return out
 
 
-def end_to_end(torch, h, w, b_host, p, r, stream, dev, K, dist, run, primal, z_wc=False):
+def end_to_end(torch, h, w, b_host, p, r, stream, dev, K, dist, run, primal, z_wc=False, copy_streams=4):
     """Wall time of K outer iterations where each step's b comes from pinned
-    host memory and its z goes back to pinned host memory."""
+    host memory and its z goes back to pinned host memory.  Each copy is
+    split along z into copy_streams chunks, one stream per chunk, so that
+    several copy engines move it at once; compute waits for all chunks of its
+    b, and z's chunks wait for the step that wrote z."""
     n_b = len(b_host)
     shape = tuple(b_host[0].shape)
+    C = max(1, min(int(copy_streams), shape[0]))
+    cuts = [shape[0] * c // C for c in range(C + 1)]
     b_in = [torch.empty(shape, device=dev) for _ in range(2)]
     z_out = [torch.empty(shape, device=dev) for _ in range(2)]
     from fgp_dual_stencil_gb300 import tvfgp as T
     z_host = [T.host_tensor(shape, write_combined=z_wc) for _ in range(2)]
-    s_in = torch.cuda.Stream(dev)
-    s_out = torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]       # b_in[s] filled
-    ev_done = [torch.cuda.Event() for _ in range(2)]     # step using slot s finished
-    ev_out = [torch.cuda.Event() for _ in range(2)]      # z_host[s] filled, z_out[s] free
+    s_in = [torch.cuda.Stream(dev) for _ in range(C)]
+    s_out = [torch.cuda.Stream(dev) for _ in range(C)]
+    ev_in = [[torch.cuda.Event() for _ in range(C)] for _ in range(2)]    # b_in[s] chunk filled
+    ev_done = [torch.cuda.Event() for _ in range(2)]                       # step using slot s finished
+    ev_out = [[torch.cuda.Event() for _ in range(C)] for _ in range(2)]   # z_host[s] chunk filled
 
     def h2d(j):
         s = j % 2
-        with torch.cuda.stream(s_in):
-            if j >= 2:
-                s_in.wait_event(ev_done[s])              # b_in[s] no longer read
-            b_in[s].copy_(b_host[j % n_b], non_blocking=True)
-            ev_in[s].record(s_in)
+        for c in range(C):
+            lo, hi = cuts[c], cuts[c + 1]
+            with torch.cuda.stream(s_in[c]):
+                if j >= 2:
+                    s_in[c].wait_event(ev_done[s])           # b_in[s] no longer read
+                b_in[s][lo:hi].copy_(b_host[j % n_b][lo:hi], non_blocking=True)
+                ev_in[s][c].record(s_in[c])
 
     barrier(dist)
     torch.cuda.synchronize(dev)
@@ -471,16 +482,19 @@ def end_to_end(torch, h, w, b_host, p, r, stream, dev, K, dist, run, primal, z_w
         s = j % 2
         if j + 1 < K:
             h2d(j + 1)
-        stream.wait_event(ev_in[s])
-        if j >= 2:
-            stream.wait_event(ev_out[s])                 # z_out[s] copied out
+        for c in range(C):
+            stream.wait_event(ev_in[s][c])
+            if j >= 2:
+                stream.wait_event(ev_out[s][c])              # z_out[s] copied out
         run(b_in[s], p, r, w.lam, w.steps, w.t0, stream)
         primal(b_in[s], p, w.lam, z_out[s], stream)
         ev_done[s].record(stream)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_done[s])
-            z_host[s].copy_(z_out[s], non_blocking=True)
-            ev_out[s].record(s_out)
+        for c in range(C):
+            lo, hi = cuts[c], cuts[c + 1]
+            with torch.cuda.stream(s_out[c]):
+                s_out[c].wait_event(ev_done[s])
+                z_host[s][lo:hi].copy_(z_out[s][lo:hi], non_blocking=True)
+                ev_out[s][c].record(s_out[c])
     torch.cuda.synchronize(dev)
     dt = max_over_ranks(dist, time.perf_counter() - t0)
     barrier(dist)

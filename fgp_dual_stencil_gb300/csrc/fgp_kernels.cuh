@@ -638,10 +638,8 @@ fgp_step_fused4(const StepArgsT<TS> a)
                 G2.z = __fsub_rn(Zc.z, ZZ.z); G2.w = __fsub_rn(Zc.w, ZZ.w);
             }
             float4 N0 = R0c, N1 = R1c, N2 = R2c;
-            dual_update(N0.x, N1.x, N2.x, __fsub_rn(Zc.x, Zc.y), G1.x, G2.x, P0.x, P1.x, P2.x, s, m);
-            dual_update(N0.y, N1.y, N2.y, __fsub_rn(Zc.y, Zc.z), G1.y, G2.y, P0.y, P1.y, P2.y, s, m);
-            dual_update(N0.z, N1.z, N2.z, __fsub_rn(Zc.z, Zc.w), G1.z, G2.z, P0.z, P1.z, P2.z, s, m);
-            dual_update(N0.w, N1.w, N2.w, gx3, G1.w, G2.w, P0.w, P1.w, P2.w, s, m);
+            const float4 G0 = make_float4(__fsub_rn(Zc.x, Zc.y), __fsub_rn(Zc.y, Zc.z), __fsub_rn(Zc.z, Zc.w), gx3);
+            dual_update4(N0, N1, N2, G0, G1, G2, P0, P1, P2, s, m, nzero);
             stvq<VO>(q0 + io, P0);
             stvq<VO>(q1 + io, P1);
             stvq<VO>(q2 + io, P2);
