@@ -18,7 +18,7 @@
 //     A  z^k     of plane q+1 on x0-1..x0+TX+1, y0-1..y0+TY+1   (staged b, r^k)
 //     B  step k  of plane q   on x0-1..x0+TX,   y0-1..y0+TY     (-> r^{k+1} shared, p^{k+1} registers)
 //     -- barrier
-//     C  z^{k+1} of plane q   on x0..x0+TX,     y0..y0+TY       (b, r^{k+1})
+//     C  z^{k+1} of plane q   on x0..x0+TX,     y0..y0+TY       (b in registers, r^{k+1})
 //     D  step k+1 of plane q-1 on the tile                      (-> p^{k+2}, r^{k+2} in HBM)
 //     -- barrier
 //
