@@ -20,7 +20,16 @@
 //     -- barrier
 //     C  z^{k+1} of plane q   on x0..x0+TX,     y0..y0+TY       (b in registers, r^{k+1})
 //     D  step k+1 of plane q-1 on the tile                      (-> p^{k+2}, r^{k+2} in HBM)
-//     -- barrier
+//
+// One barrier per plane suffices.  Across it every phase reads what the
+// phases before it wrote.  Without a second one, a thread may already run
+// A and B of plane q+1 while another still runs C and D of plane q, so what
+// the latter read must not be overwritten by the former: step k+1 takes its
+// own r^{k+1} and p^{k+1} from the registers of the thread that made them
+// (one plane earlier), C reads r^{k+1} of plane q and r_z^{k+1} of plane q-1,
+// and B of plane q+1 writes r^{k+1} into a third slot for r_z (two for
+// r_x, r_y).  The z rings, the stages and the abort flags are written only
+// at points that one barrier already separates from their readers.
 //
 // Each thread owns one quad (four x voxels) and runs A and B, and C and D,
 // on it: the voxel's own z^k, z^{k+1} and p^{k+1} stay in its registers from
@@ -128,22 +137,22 @@ constexpr int Z2_RING_B = Z2_TASKS_B - Z2_TASKS_D;        // 2 QA + 2 TY
 static_assert(Z2_RING_B == 2 * Z2_QA + 2 * Z2_TY && Z2_TASKS_A - Z2_TASKS_B == Z2_QA, "thread roles");
 static_assert(Z2_TASKS_B <= Z2_THREADS && Z2_TASKS_A <= Z2_THREADS, "thread roles");
 
-// shared rings, two slots each (a plane is written two iterations after the
-// slot was last read, with a barrier in between); pitches in floats
+// shared rings (z^k, z^{k+1}: two slots; r^{k+1}: two slots for r_x, r_y and
+// three for r_z, see above); pitches in floats
 constexpr int Z2_PK = Z2_BW;                              // z^k and r^{k+1}: columns lx+4
 constexpr int Z2_P1 = Z2_TX + 4;                          // z^{k+1}: columns lx
 constexpr int Z2_RING_ZK = (Z2_TY + 3) * Z2_PK;           // floats per slot
 constexpr int Z2_MR_COMP = (Z2_TY + 2) * Z2_PK;
-constexpr int Z2_RING_MR = 3 * Z2_MR_COMP;
+constexpr int Z2_MR_SLOTS = 2 + 2 + 3;                    // r_x, r_y: 2 slots each; r_z: 3
 constexpr int Z2_RING_Z1 = (Z2_TY + 1) * Z2_P1;
 constexpr int Z2_OFF_ZK = Z2_STAGES * Z2_STAGE_STRIDE;
 constexpr int Z2_OFF_MR = zm_round128(Z2_OFF_ZK + 2 * Z2_RING_ZK * 4);
-constexpr int Z2_OFF_Z1 = zm_round128(Z2_OFF_MR + 2 * Z2_RING_MR * 4);
+constexpr int Z2_OFF_Z1 = zm_round128(Z2_OFF_MR + Z2_MR_SLOTS * Z2_MR_COMP * 4);
 // r2^k of the plane below the first: read only by the prologue, before the
 // z^{k+1} ring is first written, so it shares that ring's memory
 constexpr int Z2_OFF_PREV = Z2_OFF_Z1;
 constexpr int Z2_OFF_BAR = zm_round128(Z2_OFF_Z1 + 2 * Z2_RING_Z1 * 4);
-constexpr int Z2_OFF_FLAG = Z2_OFF_BAR + 8 * (Z2_STAGES + 1);
+constexpr int Z2_OFF_FLAG = Z2_OFF_BAR + 8 * (Z2_STAGES + 1);   // two abort flags (plane parity)
 constexpr int Z2_SMEM = Z2_OFF_FLAG + 16 + 128;
 
 static_assert(Z2_TX % 4 == 0 && Z2_BW <= 256 && Z2_HR <= 256, "TMA box limits");
@@ -176,6 +185,9 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     extern __shared__ unsigned char z2_raw[];
     unsigned char *smem = z2_raw + ((128 - (smem_addr(z2_raw) & 127)) & 127);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Z2_OFF_BAR);   // [STAGES] + prev
+    // abort flags: the prologue and the planes of even count from f use [0],
+    // the others [1], so that a thread setting the flag of plane q+1 never
+    // changes the one another thread still reads after plane q's barrier
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Z2_OFF_FLAG);
     float *ZK = reinterpret_cast<float *>(smem + Z2_OFF_ZK);
     float *MR = reinterpret_cast<float *>(smem + Z2_OFF_MR);
@@ -196,7 +208,7 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
 
     if (tid == 0) {
         for (int k = 0; k <= Z2_STAGES; ++k) mbar_init(&bars[k], 1);
-        *abort_flag = 0;
+        abort_flag[0] = abort_flag[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -224,7 +236,9 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
 
     auto F = [](const unsigned char *st, int off) { return reinterpret_cast<const float *>(st + off); };
     auto zkp = [&](int q) { return ZK + (q & 1) * Z2_RING_ZK; };
-    auto mrp = [&](int q, int a) { return MR + (q & 1) * Z2_RING_MR + a * Z2_MR_COMP; };
+    auto mrp = [&](int q, int a) {
+        return MR + (a < 2 ? (q & 1) * 2 + a : 4 + q % 3) * Z2_MR_COMP;
+    };
     auto z1p = [&](int q) { return Z1 + (q & 1) * Z2_RING_Z1; };
 
     // this thread's quad in the z^k / step-k grid (c = lx + 4, row = ly + 1)
@@ -305,32 +319,35 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
                 ZKc = zk_quad(f, stage(f), f > 0 ? reinterpret_cast<const float *>(smem + Z2_OFF_PREV) : nullptr,
                               Bc);
         } else {
-            *abort_flag = 1;
+            abort_flag[0] = 1;
         }
     }
     __syncthreads();
+    bool aborted = abort_flag[0] != 0;
 
     const long long No = PADDED_OUT ? za.No : za.N;
     const int opx = PADDED_OUT ? za.opx : nx;
     float *p0d = za.p_dst, *p1d = za.p_dst + No, *p2d = za.p_dst + 2 * No;
     float *r0d = za.r_dst, *r1d = za.r_dst + No, *r2d = za.r_dst + 2 * No;
     float4 cP0 = f4zero(), cP1 = f4zero(), cP2 = f4zero();   // p^{k+1} of plane q-1 (tile quads)
+    float4 cR0 = f4zero(), cR1 = f4zero(), cR2 = f4zero();   // r^{k+1} of plane q-1 (tile quads)
     float4 Z1c = f4zero();                                    // z^{k+1} of plane q-1 (tile quads)
 
     int qlast = f - 1;                          // planes <= qlast+1 were waited for
-    for (int q = f; q <= ze && *abort_flag == 0; ++q) {
+    for (int q = f; q <= ze && !aborted; ++q) {
         qlast = q;
+        volatile int *flag = abort_flag + ((q - f + 1) & 1);
         // ---- A: z^k of plane q+1 -------------------------------------------
         float4 ZKn = f4zero(), Bn = f4zero();
         if (q + 1 <= last) {
             if (mbar_wait_tma(&bars[slot(q + 1)], parity(q + 1), polls(q + 1))) {
                 if (doA) ZKn = zk_quad(q + 1, stage(q + 1), F(stage(q), Z2_OFF_R2), Bn);
             } else {
-                *abort_flag = 1;
+                *flag = 1;
             }
         }
         // ---- B: step k on plane q over the grown tile ----------------------
-        float4 nP0 = f4zero(), nP1 = f4zero(), nP2 = f4zero();
+        float4 nP0 = f4zero(), nP1 = f4zero(), nP2 = f4zero(), nR0 = f4zero(), nR1 = f4zero(), nR2 = f4zero();
         if (q <= uk_last && doB) {
             const unsigned char *st = stage(q);
             const bool hasZ = q + 1 < nz;
@@ -378,10 +395,16 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
             nP0 = P0;
             nP1 = P1;
             nP2 = P2;
+            nR0 = R0;
+            nR1 = R1;
+            nR2 = R2;
         }
         ZKc = ZKn;
         __syncthreads();
-        if (*abort_flag) break;
+        if (*flag) {
+            aborted = true;
+            break;
+        }
         // every read of plane q's stage is done (phase C takes b from
         // registers): the slot takes the next plane
         if (tid == Z2_PRODUCER && next_issue <= last && q <= uk_last) {
@@ -410,8 +433,7 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
                 const float zx = Zd[zo + 4];
                 const float4 zy = lds4(Zd + zo + Z2_P1);
                 const float4 zz = hasZ ? Z1n : f4zero();
-                const int mo = (ly + 1) * Z2_PK + c + 4;
-                float4 R0 = lds4(mrp(qd, 0) + mo), R1 = lds4(mrp(qd, 1) + mo), R2 = lds4(mrp(qd, 2) + mo);
+                float4 R0 = cR0, R1 = cR1, R2 = cR2;
                 float4 P0 = cP0, P1 = cP1, P2 = cP2;
                 const bool gy = y < ny - 1;
                 const float4 G1 = gy ? sub4_rn(zc, zy) : f4zero();
@@ -441,10 +463,12 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
         cP0 = nP0;
         cP1 = nP1;
         cP2 = nP2;
-        __syncthreads();
+        cR0 = nR0;
+        cR1 = nR1;
+        cR2 = nR2;
     }
 
-    if (*abort_flag) {
+    if (aborted) {
         // A wait gave up.  Record it, then drain (bounded) every copy this
         // CTA issued that is still in flight: plane qlast+1 (whose wait
         // failed, or f when the prologue failed) and every later plane
