@@ -32,10 +32,10 @@
 // at points that one barrier already separates from their readers.
 //
 // Each thread owns one quad (four x voxels) and runs A and B, and C and D,
-// on it: the voxel's own z^k, z^{k+1} and p^{k+1} stay in its registers from
-// the phase that makes them to the phase that uses them, and only the x+1 /
-// y+1 neighbours' z and the r^{k+1} halo go through shared memory (rings of
-// two planes), so two barriers per plane suffice.  Voxels of the ring that
+// on it: the voxel's own z^k, z^{k+1}, p^{k+1} and r^{k+1} stay in its
+// registers from the phase that makes them to the phase that uses them, and
+// only the x+1 / y+1 neighbours' z and the r^{k+1} halo go through shared
+// memory (rings of two or three planes).  Voxels of the ring that
 // lie outside the volume get r^{k+1} = 0: that is the r(-1) = 0 boundary step
 // k+1 sees.
 // Every value is computed by the same expressions, in the same order, as in
