@@ -420,17 +420,13 @@ def gpu_arm(args, world, rank, local_rank, dist):
         if args.workload == "c4" and not f16 else None,
         "dtype": "f32 (dual stored as f16)" if f16 else "f32",
         "data": "synthetic",
-        "config": {
-            "workload": "%dx%dx%d fp32 TV-dual FGP, %d outers x %d steps, warm p/r, t0=1 per outer, "
-                        "lambda %g; one bench step = one outer (%d FGP steps + primal)"
-                        % (w.nx, w.ny, w.nz, w.outers, w.steps, w.lam, w.steps),
-            "nx": w.nx, "ny": w.ny, "nz": w.nz, "fgp_steps_per_bench_step": w.steps,
+        "config": workload_config(w, world),
+        # how this arm ran the workload; kept out of "config" so that both
+        # arms describe the same workload with the same dictionary
+        "impl_config": {
             "variant": names.get(variant_used, str(variant_used)),
             "launch": "eager" if args.eager else "cuda_graph",
             "row_pitch": pitch,
-            "l2": "inputs larger than L2 (%.1f GB of live buffers vs 126 MB L2)" % (11 * 4 * N / 1e9)
-            if 4 * N > 129e6 else "working set fits in L2: GB/s is not an HBM figure",
-            "parallelism": "replicas" if world > 1 else "single_gpu",
             "vs_baseline_ref": "RTX 5070 fused kernel, 12.607 ms per FGP step at 512^3 (page figure; "
                                "other hardware, context only)",
         },
@@ -558,6 +554,21 @@ def cpu_baseline(w, base, threads=(), budget_s=10.0):
 # the reference arm: the CPU oracle on the same workload
 # ---------------------------------------------------------------------------
 
+def workload_config(w, world):
+    """The bench line's "config": the workload alone, identical for the
+    library's arm and the oracle's, so that their lines compare."""
+    n = w.nvox
+    return {
+        "workload": "%dx%dx%d fp32 TV-dual FGP, %d outers x %d steps, warm p/r, t0=1 per outer, "
+                    "lambda %g; one bench step = one outer (%d FGP steps + primal)"
+                    % (w.nx, w.ny, w.nz, w.outers, w.steps, w.lam, w.steps),
+        "nx": w.nx, "ny": w.ny, "nz": w.nz, "fgp_steps_per_bench_step": w.steps,
+        "l2": "inputs larger than L2 (%.1f GB of live buffers vs 126 MB L2)" % (11 * 4 * n / 1e9)
+        if 4 * n > 129e6 else "working set fits in L2: GB/s is not an HBM figure",
+        "parallelism": "replicas" if world > 1 else "single_gpu",
+    }
+
+
 def reference_arm(args, world, rank):
     """The CPU oracle, as it stands, on the GPU arm's workload and metric:
     each bench step is one outer iteration on the full volume (a fresh b, t
@@ -601,10 +612,8 @@ def reference_arm(args, world, rank):
         "ms_per_fgp_step": round(dt * 1e3 / K / w.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": "%dx%dx%d fp32 TV-dual FGP, %d outers x %d steps, warm p/r, t0=1 per outer, "
-                               "lambda %g; one bench step = one outer (%d FGP steps + primal)"
-                               % (w.nx, w.ny, w.nz, w.outers, w.steps, w.lam, w.steps),
-                   "nx": w.nx, "ny": w.ny, "nz": w.nz, "fgp_steps_per_bench_step": w.steps},
+        "config": workload_config(w, world),
+        "impl_config": {"variant": "oracle (plain C, fp64 schedule, fp32 arithmetic)", "launch": "host threads"},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": oracle.get_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

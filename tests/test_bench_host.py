@@ -1,7 +1,7 @@
 """Host logic of bench.py that decides what the JSON line reports: the kernel
 source hash that gates the recorded DRAM traffic (comment edits keep it,
 code edits drop the traffic to null) and the scaling of that traffic to a
-volume."""
+volume; the workload description both arms share."""
 import json
 import os
 import shutil
@@ -70,3 +70,20 @@ def test_roofline_reports_the_model_and_the_measured_dram_fraction():
     none = bench.roofline_entry("fgp_step2_zmarch_tma", 104 * n, 1.25e-3, 6800.0, "fallback", None, 2.0, 52)
     assert none["traffic"] is None and none["dram_frac"] is None and none["dram_achieved"] is None
     assert none["peak_source"] == "fallback 6.8 TB/s"
+
+
+def test_reference_arm_reports_the_same_config_as_the_library_arm(monkeypatch):
+    """The oracle's arm runs on the small workload here and must describe the
+    workload with the very dictionary the library's arm puts in "config"."""
+    import sys
+    from fgp_dual_stencil_gb300 import synth
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--workload", "c1",
+                                      "--steps", "1", "--warmup", "0"])
+    line = bench.reference_arm(bench.parse_args(), 1, 0)
+    assert line["impl"] == "reference" and line["gpu_launches"] == 0
+    assert line["config"] == bench.workload_config(synth.WORKLOADS["c1"], 1)
+    assert line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    for wl in synth.WORKLOADS.values():
+        cfg = bench.workload_config(wl, 1)
+        assert set(cfg) == {"workload", "nx", "ny", "nz", "fgp_steps_per_bench_step", "l2", "parallelism"}
+        assert cfg["nx"] * cfg["ny"] * cfg["nz"] == wl.nvox
