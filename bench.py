@@ -156,7 +156,81 @@ class ClockSampler:
         reasons = sorted({n for r in inside for n, v in zip(self.NAMES, r[3]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(r[1] for r in inside),
                 "sm_max_mhz": max(r[2] for r in inside),
-                "reasons": reasons, "samples": len(inside)}
+                "reasons": reasons, "samples": len(inside), "source": "nvidia-smi every 50 ms"}
+
+
+class NvmlSampler:
+    """The SM clock and the active clock-event reasons, read through NVML
+    (read-only queries) on a host thread every `period_s` seconds: a short
+    timed region still gets a dozen samples or more.  `lib` is the NVML
+    library (a stand-in in the host tests).  `ok` is False when NVML or the
+    device cannot be opened; the caller then falls back to nvidia-smi."""
+    CLOCK_SM = 1                                   # nvmlClockType_t NVML_CLOCK_SM
+    BITS = (("sw_power_cap", 0x4), ("hw_slowdown", 0x8), ("sw_thermal_slowdown", 0x20),
+            ("hw_thermal_slowdown", 0x40))
+
+    def __init__(self, uuid: str | None, period_s: float = 0.01, lib=None):
+        import ctypes
+        import threading
+        self.rows, self.ok, self.period = [], False, period_s
+        self.max_mhz = None
+        self._ct = ctypes
+        try:
+            self.lib = lib if lib is not None else ctypes.CDLL("libnvidia-ml.so.1")
+            if not uuid or self.lib.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+                self.lib.nvmlShutdown()
+                return
+            self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint(0)
+            if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+        except (OSError, AttributeError):
+            return
+        self.ok = True
+        self._stop = threading.Event()
+        self._thread = threading.Thread(target=self._loop, daemon=True)
+        self._thread.start()
+
+    def _loop(self):
+        ct = self._ct
+        mhz, rs = ct.c_uint(0), ct.c_ulonglong(0)
+        while not self._stop.is_set():
+            t = time.time()
+            if (self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, ct.byref(mhz)) == 0
+                    and self.reasons_fn(self.h, ct.byref(rs)) == 0):
+                self.rows.append((t, float(mhz.value), int(rs.value)))
+            self._stop.wait(self.period)
+
+    def stop(self, t0: float, t1: float):
+        if not self.ok:
+            return None
+        self._stop.set()
+        self._thread.join(timeout=5)
+        self.lib.nvmlShutdown()
+        return self.summary(self.rows, t0, t1, self.max_mhz, self.period)
+
+    @classmethod
+    def summary(cls, rows, t0: float, t1: float, max_mhz, period_s: float):
+        """Median SM clock and the union of the throttle reasons over the
+        samples taken inside [t0, t1]."""
+        inside = [r for r in rows if t0 <= r[0] <= t1] or [r for r in rows if t0 - 0.1 <= r[0] <= t1 + 0.1]
+        if not inside:
+            return None
+        reasons = sorted({n for r in inside for n, bit in cls.BITS if r[2] & bit})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max_mhz if max_mhz is not None else max(r[1] for r in inside),
+                "reasons": reasons, "samples": len(inside),
+                "source": "NVML every %g ms on a host thread" % (period_s * 1e3)}
+
+
+def start_clock_sampler(uuid: str | None):
+    """NVML sampling when it can be opened, else nvidia-smi every 50 ms."""
+    nv = NvmlSampler(uuid)
+    return nv if nv.ok else ClockSampler(uuid)
 
 
 def gpu_id_for(torch, dev) -> str | None:
@@ -319,9 +393,9 @@ def gpu_arm(args, world, rank, local_rank, dist):
     variant_used = h.last_variant
     launches0 = h.launch_count
 
-    sampler = ClockSampler(gpu_id_for(torch, dev)) if not args.no_clocks else None
-    if sampler is not None:
-        time.sleep(0.6)                       # let the sampler start before the timed region
+    sampler = start_clock_sampler(gpu_id_for(torch, dev)) if not args.no_clocks else None
+    if isinstance(sampler, ClockSampler):
+        time.sleep(0.6)                       # let nvidia-smi start before the timed region
     ev_start = torch.cuda.Event(enable_timing=True)
     ev_end = torch.cuda.Event(enable_timing=True)
     ev_run = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))

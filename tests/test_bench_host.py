@@ -87,3 +87,61 @@ def test_reference_arm_reports_the_same_config_as_the_library_arm(monkeypatch):
         cfg = bench.workload_config(wl, 1)
         assert set(cfg) == {"workload", "nx", "ny", "nz", "fgp_steps_per_bench_step", "l2", "parallelism"}
         assert cfg["nx"] * cfg["ny"] * cfg["nz"] == wl.nvox
+
+
+class FakeNvml:
+    """NVML stand-in: a fixed SM clock, and the power-cap reason bit set
+    from the third clock query on."""
+
+    def __init__(self, mhz=1965, max_mhz=2070, uuid_ok=True):
+        self.mhz, self.max_mhz, self.uuid_ok = mhz, max_mhz, uuid_ok
+        self.queries, self.shut = 0, False
+
+    def nvmlInit_v2(self):
+        return 0
+
+    def nvmlShutdown(self):
+        self.shut = True
+        return 0
+
+    def nvmlDeviceGetHandleByUUID(self, uuid, ref):
+        ref._obj.value = 1234
+        return 0 if self.uuid_ok and uuid.startswith(b"GPU-") else 13
+
+    def nvmlDeviceGetMaxClockInfo(self, h, kind, ref):
+        ref._obj.value = self.max_mhz
+        return 0
+
+    def nvmlDeviceGetClockInfo(self, h, kind, ref):
+        assert kind == 1
+        self.queries += 1
+        ref._obj.value = self.mhz
+        return 0
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h, ref):
+        ref._obj.value = 0x4 | 0x1 if self.queries >= 3 else 0x1
+        return 0
+
+
+def test_nvml_clock_sampler_with_a_stand_in_library():
+    import time
+    fake = FakeNvml()
+    t0 = time.time()
+    s = bench.NvmlSampler("GPU-0000", period_s=0.002, lib=fake)
+    assert s.ok
+    time.sleep(0.05)
+    out = s.stop(t0, time.time())
+    assert fake.shut and fake.queries >= 3
+    assert out["sm_mhz"] == 1965 and out["sm_max_mhz"] == 2070
+    assert out["reasons"] == ["sw_power_cap"] and out["samples"] >= 3
+    # an unknown device: no sampler (the bench then uses nvidia-smi)
+    assert not bench.NvmlSampler("GPU-0000", lib=FakeNvml(uuid_ok=False)).ok
+    assert not bench.NvmlSampler(None, lib=FakeNvml()).ok
+
+
+def test_clock_summary_decodes_the_reason_bits():
+    rows = [(1.0, 2070.0, 0x0), (1.1, 2055.0, 0x8), (1.2, 2070.0, 0x40 | 0x20), (5.0, 300.0, 0x4)]
+    out = bench.NvmlSampler.summary(rows, 0.9, 1.3, 2070.0, 0.01)
+    assert out["sm_mhz"] == 2070.0 and out["samples"] == 3
+    assert out["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
+    assert bench.NvmlSampler.summary(rows, 10.0, 11.0, 2070.0, 0.01) is None
