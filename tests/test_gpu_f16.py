@@ -235,3 +235,33 @@ def test_f16_1000x600x300_exact(T):
         assert h.check() == 0
     oracle.fgp_run_h16(b, ph, rh, w.lam, 30, w.t0)
     assert np.array_equal(bits(p), ph) and np.array_equal(bits(r), rh)
+
+
+def random_f16_shapes(count, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for k in range(count):
+        nx = int(rng.integers(1, 25)) * 8 if k % 3 else int(rng.integers(1, 120))
+        out.append((nx, int(rng.integers(1, 70)), int(rng.integers(1, 100))))
+    return out
+
+
+@pytest.mark.parametrize("shape", random_f16_shapes(8, 20261204))
+def test_random_shapes_exact(T, shape):
+    nx, ny, nz = shape
+    seed = (nx * 131 + ny) * 197 + nz
+    rng = np.random.default_rng(seed)
+    nsteps = int(rng.integers(1, 10))
+    lam = float(rng.uniform(0.01, 0.2))
+    b = synth.random_case(shape, seed)
+    p0 = oracle.float_to_half(synth.random_dual(shape, seed + 1, scale=0.5))
+    r0 = oracle.float_to_half(synth.random_dual(shape, seed + 2, scale=0.7))
+    p, r = dev16(p0), dev16(r0)
+    with T.Tvfgp(nx, ny, nz) as h:
+        h.run_f16(dev(b), p, r, lam, nsteps, 1.0)
+        assert h.last_variant == expected_variant(T, nx, "auto")
+        assert h.check() == 0
+    ph, rh = p0.copy(), r0.copy()
+    oracle.fgp_run_h16(b, ph, rh, lam, nsteps, 1.0)
+    assert np.array_equal(bits(p), ph), (shape, nsteps, lam)
+    assert np.array_equal(bits(r), rh), (shape, nsteps, lam)

@@ -341,3 +341,44 @@ def test_host_staging_memory_round_trip(T, wc):
     out.copy_(d * 2, non_blocking=True)
     torch.cuda.synchronize()
     assert np.array_equal(out.numpy(), 2 * b)
+
+
+# ---------------------------------------------------------------------------
+# seeded random shapes: tile, chunk and tail boundaries anywhere
+# ---------------------------------------------------------------------------
+
+def random_shapes(count, seed):
+    """Shapes drawn so that x is a multiple of 4 in most cases (the vector
+    and TMA kernels) and not in the rest (the scalar fallback), with y and
+    z anywhere from one plane to several tiles and chunks."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for k in range(count):
+        nx = int(rng.integers(1, 50)) * 4 if k % 4 else int(rng.integers(1, 200))
+        ny = int(rng.integers(1, 90))
+        nz = int(rng.integers(1, 160))
+        out.append((nx, ny, nz))
+    return out
+
+
+@pytest.mark.parametrize("shape", random_shapes(12, 20261202))
+@pytest.mark.parametrize("variant", ["auto", "zmarch2", "zmarch", "cube"])
+def test_random_shapes_match_the_oracle(T, shape, variant):
+    nx, ny, nz = shape
+    seed = (nx * 131 + ny) * 197 + nz
+    rng = np.random.default_rng(seed)
+    nsteps = int(rng.integers(4, 10))
+    lam = float(rng.uniform(0.01, 0.2))
+    b = synth.random_case(shape, seed)
+    p0 = synth.random_dual(shape, seed + 1, scale=0.5)
+    r0 = synth.random_dual(shape, seed + 2, scale=0.7)
+    p, r, bd = dev(p0), dev(r0), dev(b)
+    with T.Tvfgp(nx, ny, nz, variant) as h:
+        tf = h.run(bd, p, r, lam, nsteps, 1.0)
+        zp = h.primal(bd, p, lam)
+        assert h.check() == 0
+    po, ro = p0.copy(), r0.copy()
+    assert tf == oracle.fgp_run(b, po, ro, lam, nsteps, 1.0)
+    assert max_diff(host(p), po) == 0.0, (shape, variant, nsteps, lam, "p")
+    assert max_diff(host(r), ro) == 0.0, (shape, variant, nsteps, lam, "r")
+    assert max_diff(host(zp), oracle.primal(b, po, lam)) == 0.0, (shape, variant, nsteps, lam, "z")

@@ -225,3 +225,41 @@ def test_pitched_single_step(T, shape, pitch):
     check(p, po, pp, nx, "p")
     check(rd, ro, rdp, nx, "r_dst")
     check(rs, r0, rp, nx, "r_src")
+
+
+def random_pitched_cases(count, seed):
+    """Shapes and pitches drawn at random: the FFT pitch 2*(nx/2+1) in most
+    cases, an arbitrary larger pitch in the rest."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for k in range(count):
+        nx = int(rng.integers(1, 40)) * 4 if k % 3 else int(rng.integers(1, 150))
+        shape = (nx, int(rng.integers(1, 60)), int(rng.integers(1, 90)))
+        pitch = 2 * (nx // 2 + 1) if k % 4 else nx + int(rng.integers(1, 9))
+        out.append((shape, pitch))
+    return out
+
+
+@pytest.mark.parametrize("shape,pitch", random_pitched_cases(8, 20261203))
+def test_random_pitched_shapes(T, shape, pitch):
+    nx, ny, nz = shape
+    seed = (nx * 131 + ny) * 197 + nz + pitch
+    rng = np.random.default_rng(seed)
+    nsteps = int(rng.integers(1, 10))
+    lam = float(rng.uniform(0.01, 0.2))
+    b = synth.random_case(shape, seed)
+    p0 = synth.random_dual(shape, seed + 1, scale=0.5)
+    r0 = synth.random_dual(shape, seed + 2, scale=0.7)
+    bp, pp, rp = pad(b, pitch, seed + 3), pad(p0, pitch, seed + 4), pad(r0, pitch, seed + 5)
+    zp = pad(np.zeros_like(b), pitch, seed + 6)
+    p, r, z = dev(pp), dev(rp), dev(zp)
+    with T.Tvfgp(nx, ny, nz, "auto", True, pitch=pitch) as h:
+        h.run(dev(bp), p, r, lam, nsteps, 1.0)
+        h.primal(dev(bp), p, lam, z=z)
+        assert h.last_variant == pitched_variant(T, nx, pitch, "auto", nsteps)
+        assert h.check() == 0
+    po, ro = p0.copy(), r0.copy()
+    oracle.fgp_run(b, po, ro, lam, nsteps, 1.0)
+    check(p, po, pp, nx, "p")
+    check(r, ro, rp, nx, "r")
+    check(z, oracle.primal(b, po, lam), zp, nx, "z")
