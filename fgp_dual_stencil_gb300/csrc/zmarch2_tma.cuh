@@ -50,6 +50,8 @@
 // drained, return).
 #pragma once
 
+#include <type_traits>
+
 #include "zmarch_tma.cuh"
 
 namespace tvfgp {
@@ -272,12 +274,14 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     // and rows 1..TY+1 (the tile, the ring's right column and its last row)
     const bool doC = doA && my_c >= 4 && my_row >= 1 && my_row <= Z2_TY + 1;
     // Step k's quads cover lx -4..TX+3, ly -1..TY.  When all of them lie
-    // inside the volume and none touches the upper x face, step k needs no
-    // per-voxel boundary test (most CTAs of a large volume).
+    // inside the volume and none touches the upper x face, neither step
+    // needs a per-voxel boundary test, nor a y or x face test (most CTAs of
+    // a large volume): the march below is compiled twice, with and without
+    // the tests, and each CTA runs one of the two.
 #if TVFGP_Z2_EDGE_SPLIT
-    const bool edge = !(x0 >= 4 && x0 + Z2_TX + 5 <= nx && y0 >= 1 && y0 + Z2_TY + 2 <= ny);
+    const bool edge_cta = !(x0 >= 4 && x0 + Z2_TX + 5 <= nx && y0 >= 1 && y0 + Z2_TY + 2 <= ny);
 #else
-    const bool edge = true;
+    const bool edge_cta = true;
 #endif
 
     // z^k of plane q for this thread's quad, from the staged plane st and the
@@ -341,139 +345,147 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     float4 Z1c = f4zero();                                    // z^{k+1} of plane q-1 (tile quads)
 
     int qlast = f - 1;                          // planes <= qlast+1 were waited for
-    for (int q = f; q <= ze && !aborted; ++q) {
-        qlast = q;
-        volatile int *flag = abort_flag + ((q - f + 1) & 1);
-        // ---- A: z^k of plane q+1 -------------------------------------------
-        float4 ZKn = f4zero(), Bn = f4zero();
-        if (q + 1 <= last) {
-            if (mbar_wait_tma(&bars[slot(q + 1)], parity(q + 1), polls(q + 1))) {
-                if (doA) ZKn = zk_quad(q + 1, stage(q + 1), F(stage(q), Z2_OFF_R2), Bn);
-            } else {
-                *flag = 1;
-            }
-        }
-        // ---- B: step k on plane q over the grown tile ----------------------
-        float4 nP0 = f4zero(), nP1 = f4zero(), nP2 = f4zero(), nR0 = f4zero(), nR1 = f4zero(), nR2 = f4zero();
-        if (q <= uk_last && doB) {
-            const unsigned char *st = stage(q);
-            const bool hasZ = q + 1 < nz;
-            const float *Zq = zkp(q);
-            const int c = my_c, row = my_row;                        // row = ly + 1
-            const int ly = row - 1, lx = c - 4;
-            const int x = x0 + lx, y = y0 + ly;
-            const int zo = row * Z2_PK + c;
-            const float4 zc = ZKc;
-            const float zx = c + 4 < Z2_PK ? Zq[zo + 4] : 0.0f;
-            const float4 zy = lds4(Zq + zo + Z2_PK);
-            const float4 zz = hasZ ? ZKn : f4zero();
-            const int ro = (row + 1) * Z2_BW + c, po = row * Z2_BW + c;
-            float4 R0 = lds4(F(st, Z2_OFF_R0) + ro), R1 = lds4(F(st, Z2_OFF_R1) + ro),
-                   R2 = lds4(F(st, Z2_OFF_R2) + ro);
-            float4 P0 = lds4(F(st, Z2_OFF_P0) + po), P1 = lds4(F(st, Z2_OFF_P1) + po),
-                   P2 = lds4(F(st, Z2_OFF_P2) + po);
-            const bool gy = y < ny - 1;
-            float4 G0 = make_float4(__fsub_rn(zc.x, zc.y), __fsub_rn(zc.y, zc.z), __fsub_rn(zc.z, zc.w),
-                                    __fsub_rn(zc.w, zx));
-            const float4 G1 = gy ? sub4_rn(zc, zy) : f4zero();
-            const float4 G2 = hasZ ? sub4_rn(zc, zz) : f4zero();
-            if (edge) {
-                float *g0 = &G0.x;
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (!(x + e < nx - 1)) g0[e] = 0.0f;
-            }
-            dual_update4(R0, R1, R2, G0, G1, G2, P0, P1, P2, s, m0, nzero);
-            // voxels of the ring outside the volume: r^{k+1} = 0, the r(-1) = 0
-            // boundary of step k+1 (their p is never used)
-            if (edge) {
-                const bool yin = y >= 0 && y < ny;
-                float *r0 = &R0.x, *r1 = &R1.x, *r2 = &R2.x;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int xe = x + e;
-                    if (!(yin && xe >= 0 && xe < nx)) r0[e] = r1[e] = r2[e] = 0.0f;
+    auto march = [&](auto edge_tag) {
+        constexpr bool edge = decltype(edge_tag)::value;
+        for (int q = f; q <= ze && !aborted; ++q) {
+            qlast = q;
+            volatile int *flag = abort_flag + ((q - f + 1) & 1);
+            // ---- A: z^k of plane q+1 -------------------------------------------
+            float4 ZKn = f4zero(), Bn = f4zero();
+            if (q + 1 <= last) {
+                if (mbar_wait_tma(&bars[slot(q + 1)], parity(q + 1), polls(q + 1))) {
+                    if (doA) ZKn = zk_quad(q + 1, stage(q + 1), F(stage(q), Z2_OFF_R2), Bn);
+                } else {
+                    *flag = 1;
                 }
             }
-            const int mo = row * Z2_PK + c;
-            *reinterpret_cast<float4 *>(mrp(q, 0) + mo) = R0;
-            *reinterpret_cast<float4 *>(mrp(q, 1) + mo) = R1;
-            *reinterpret_cast<float4 *>(mrp(q, 2) + mo) = R2;
-            nP0 = P0;
-            nP1 = P1;
-            nP2 = P2;
-            nR0 = R0;
-            nR1 = R1;
-            nR2 = R2;
-        }
-        ZKc = ZKn;
-        __syncthreads();
-        if (*flag) {
-            aborted = true;
-            break;
-        }
-        // every read of plane q's stage is done (phase C takes b from
-        // registers): the slot takes the next plane
-        if (tid == Z2_PRODUCER && next_issue <= last && q <= uk_last) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue(next_issue++);
-        }
-
-        // ---- C: z^{k+1} of plane q on the tile, its x+1 column and y+1 row ---
-        // (each quad by the thread that computed z^k there, which holds its b)
-        float4 Z1n = f4zero();
-        if (q >= z0 && q <= uk_last && doC) {
-            const float4 Z = z1_quad(q, my_c - 4, my_row - 1, Bc);
-            if (my_tile) Z1n = Z;
-        }
-        Bc = Bn;
-        // ---- D: step k+1 on plane q-1 over the tile -> p^{k+2}, r^{k+2} -----
-        const int qd = q - 1;
-        if (my_tile && qd >= z0 && qd < ze) {
-            const int c = my_c - 4, ly = my_row - 1;
-            const int x = x0 + c, y = y0 + ly;
-            if (x < nx && y < ny) {
-                const bool hasZ = qd + 1 < nz;
-                const float *Zd = z1p(qd);
-                const int zo = ly * Z2_P1 + c;
-                const float4 zc = Z1c;
-                const float zx = Zd[zo + 4];
-                const float4 zy = lds4(Zd + zo + Z2_P1);
-                const float4 zz = hasZ ? Z1n : f4zero();
-                float4 R0 = cR0, R1 = cR1, R2 = cR2;
-                float4 P0 = cP0, P1 = cP1, P2 = cP2;
-                const bool gy = y < ny - 1;
+            // ---- B: step k on plane q over the grown tile ----------------------
+            float4 nP0 = f4zero(), nP1 = f4zero(), nP2 = f4zero(), nR0 = f4zero(), nR1 = f4zero(), nR2 = f4zero();
+            if (q <= uk_last && doB) {
+                const unsigned char *st = stage(q);
+                const bool hasZ = q + 1 < nz;
+                const float *Zq = zkp(q);
+                const int c = my_c, row = my_row;                        // row = ly + 1
+                const int ly = row - 1, lx = c - 4;
+                const int x = x0 + lx, y = y0 + ly;
+                const int zo = row * Z2_PK + c;
+                const float4 zc = ZKc;
+                const float zx = c + 4 < Z2_PK ? Zq[zo + 4] : 0.0f;
+                const float4 zy = lds4(Zq + zo + Z2_PK);
+                const float4 zz = hasZ ? ZKn : f4zero();
+                const int ro = (row + 1) * Z2_BW + c, po = row * Z2_BW + c;
+                float4 R0 = lds4(F(st, Z2_OFF_R0) + ro), R1 = lds4(F(st, Z2_OFF_R1) + ro),
+                       R2 = lds4(F(st, Z2_OFF_R2) + ro);
+                float4 P0 = lds4(F(st, Z2_OFF_P0) + po), P1 = lds4(F(st, Z2_OFF_P1) + po),
+                       P2 = lds4(F(st, Z2_OFF_P2) + po);
+                const bool gy = !edge || y < ny - 1;
+                float4 G0 = make_float4(__fsub_rn(zc.x, zc.y), __fsub_rn(zc.y, zc.z), __fsub_rn(zc.z, zc.w),
+                                        __fsub_rn(zc.w, zx));
                 const float4 G1 = gy ? sub4_rn(zc, zy) : f4zero();
                 const float4 G2 = hasZ ? sub4_rn(zc, zz) : f4zero();
-                const float gx3 = (x + 3 < nx - 1) ? __fsub_rn(zc.w, zx) : 0.0f;
-                const float4 G0 = make_float4(__fsub_rn(zc.x, zc.y), __fsub_rn(zc.y, zc.z), __fsub_rn(zc.z, zc.w), gx3);
-                dual_update4(R0, R1, R2, G0, G1, G2, P0, P1, P2, s, m1, nzero);
-                const long long i = x + (long long)opx * (y + (long long)ny * qd);
-                if (!PADDED_OUT) {
-                    st4(p0d + i, P0);
-                    st4(p1d + i, P1);
-                    st4(p2d + i, P2);
-                    st4(r0d + i, R0);
-                    st4(r1d + i, R1);
-                    st4(r2d + i, R2);
-                } else {
-                    stq<2>(p0d + i, P0);
-                    stq<2>(p1d + i, P1);
-                    stq<2>(p2d + i, P2);
-                    stq<2>(r0d + i, R0);
-                    stq<2>(r1d + i, R1);
-                    stq<2>(r2d + i, R2);
+                if (edge) {
+                    float *g0 = &G0.x;
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (!(x + e < nx - 1)) g0[e] = 0.0f;
+                }
+                dual_update4(R0, R1, R2, G0, G1, G2, P0, P1, P2, s, m0, nzero);
+                // voxels of the ring outside the volume: r^{k+1} = 0, the r(-1) = 0
+                // boundary of step k+1 (their p is never used)
+                if (edge) {
+                    const bool yin = y >= 0 && y < ny;
+                    float *r0 = &R0.x, *r1 = &R1.x, *r2 = &R2.x;
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int xe = x + e;
+                        if (!(yin && xe >= 0 && xe < nx)) r0[e] = r1[e] = r2[e] = 0.0f;
+                    }
+                }
+                const int mo = row * Z2_PK + c;
+                *reinterpret_cast<float4 *>(mrp(q, 0) + mo) = R0;
+                *reinterpret_cast<float4 *>(mrp(q, 1) + mo) = R1;
+                *reinterpret_cast<float4 *>(mrp(q, 2) + mo) = R2;
+                nP0 = P0;
+                nP1 = P1;
+                nP2 = P2;
+                nR0 = R0;
+                nR1 = R1;
+                nR2 = R2;
+            }
+            ZKc = ZKn;
+            __syncthreads();
+            if (*flag) {
+                aborted = true;
+                break;
+            }
+            // every read of plane q's stage is done (phase C takes b from
+            // registers): the slot takes the next plane
+            if (tid == Z2_PRODUCER && next_issue <= last && q <= uk_last) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(next_issue++);
+            }
+
+            // ---- C: z^{k+1} of plane q on the tile, its x+1 column and y+1 row ---
+            // (each quad by the thread that computed z^k there, which holds its b)
+            float4 Z1n = f4zero();
+            if (q >= z0 && q <= uk_last && doC) {
+                const float4 Z = z1_quad(q, my_c - 4, my_row - 1, Bc);
+                if (my_tile) Z1n = Z;
+            }
+            Bc = Bn;
+            // ---- D: step k+1 on plane q-1 over the tile -> p^{k+2}, r^{k+2} -----
+            const int qd = q - 1;
+            if (my_tile && qd >= z0 && qd < ze) {
+                const int c = my_c - 4, ly = my_row - 1;
+                const int x = x0 + c, y = y0 + ly;
+                if (!edge || (x < nx && y < ny)) {
+                    const bool hasZ = qd + 1 < nz;
+                    const float *Zd = z1p(qd);
+                    const int zo = ly * Z2_P1 + c;
+                    const float4 zc = Z1c;
+                    const float zx = Zd[zo + 4];
+                    const float4 zy = lds4(Zd + zo + Z2_P1);
+                    const float4 zz = hasZ ? Z1n : f4zero();
+                    float4 R0 = cR0, R1 = cR1, R2 = cR2;
+                    float4 P0 = cP0, P1 = cP1, P2 = cP2;
+                    const bool gy = !edge || y < ny - 1;
+                    const float4 G1 = gy ? sub4_rn(zc, zy) : f4zero();
+                    const float4 G2 = hasZ ? sub4_rn(zc, zz) : f4zero();
+                    const float gx3 = (!edge || x + 3 < nx - 1) ? __fsub_rn(zc.w, zx) : 0.0f;
+                    const float4 G0 =
+                        make_float4(__fsub_rn(zc.x, zc.y), __fsub_rn(zc.y, zc.z), __fsub_rn(zc.z, zc.w), gx3);
+                    dual_update4(R0, R1, R2, G0, G1, G2, P0, P1, P2, s, m1, nzero);
+                    const long long i = x + (long long)opx * (y + (long long)ny * qd);
+                    if (!PADDED_OUT) {
+                        st4(p0d + i, P0);
+                        st4(p1d + i, P1);
+                        st4(p2d + i, P2);
+                        st4(r0d + i, R0);
+                        st4(r1d + i, R1);
+                        st4(r2d + i, R2);
+                    } else {
+                        stq<2>(p0d + i, P0);
+                        stq<2>(p1d + i, P1);
+                        stq<2>(p2d + i, P2);
+                        stq<2>(r0d + i, R0);
+                        stq<2>(r1d + i, R1);
+                        stq<2>(r2d + i, R2);
+                    }
                 }
             }
+            Z1c = Z1n;
+            cP0 = nP0;
+            cP1 = nP1;
+            cP2 = nP2;
+            cR0 = nR0;
+            cR1 = nR1;
+            cR2 = nR2;
         }
-        Z1c = Z1n;
-        cP0 = nP0;
-        cP1 = nP1;
-        cP2 = nP2;
-        cR0 = nR0;
-        cR1 = nR1;
-        cR2 = nR2;
-    }
+    };
+    if (edge_cta)
+        march(std::true_type{});
+    else
+        march(std::false_type{});
 
     if (aborted) {
         // A wait gave up.  Record it, then drain (bounded) every copy this
