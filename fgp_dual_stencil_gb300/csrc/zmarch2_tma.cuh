@@ -69,9 +69,9 @@ namespace tvfgp {
 #define TVFGP_Z2_CTAS 3           // CTAs per SM the shared memory is sized for
 #endif
 // The minimum CTAs per SM given to the compiler: 2 leaves it up to 204
-// registers a thread, and it then takes 118, for a schedule measured 0.4%
-// faster than the one it builds in the 136 that 3 CTAs allow (113
-// registers).  Three CTAs still fit: 3 x 160 x 118 registers <= 65536.
+// registers a thread, and it then takes 114, for a schedule measured 0.5%
+// faster than the one it builds in the 136 that 3 CTAs allow (110
+// registers).  Three CTAs still fit: 3 x 160 x 114 registers <= 65536.
 #ifndef TVFGP_Z2_MINB
 #define TVFGP_Z2_MINB 2
 #endif
