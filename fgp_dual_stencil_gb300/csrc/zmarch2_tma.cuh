@@ -345,6 +345,8 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     float4 Z1c = f4zero();                                    // z^{k+1} of plane q-1 (tile quads)
 
     int qlast = f - 1;                          // planes <= qlast+1 were waited for
+    // The march over the CTA's planes, instantiated for edge = true (every
+    // boundary test) and edge = false (none; interior CTAs only).
     auto march = [&](auto edge_tag) {
         constexpr bool edge = decltype(edge_tag)::value;
         for (int q = f; q <= ze && !aborted; ++q) {
