@@ -28,8 +28,9 @@
 // own r^{k+1} and p^{k+1} from the registers of the thread that made them
 // (one plane earlier), C reads r^{k+1} of plane q and r_z^{k+1} of plane q-1,
 // and B of plane q+1 writes r^{k+1} into a third slot for r_z (two for
-// r_x, r_y).  The z rings, the stages and the abort flags are written only
-// at points that one barrier already separates from their readers.
+// r_x, r_y).  The z rings and the stages are written only at points that
+// one barrier already separates from their readers; a wait that gives up is
+// reported through that barrier (its OR over the threads).
 //
 // Each thread owns one quad (four x voxels) and runs A and B, and C and D,
 // on it: the voxel's own z^k, z^{k+1}, p^{k+1} and r^{k+1} stay in its
@@ -161,8 +162,7 @@ constexpr int Z2_OFF_Z1 = zm_round128(Z2_OFF_MR + Z2_MR_SLOTS * Z2_MR_COMP * 4);
 // z^{k+1} ring is first written, so it shares that ring's memory
 constexpr int Z2_OFF_PREV = Z2_OFF_Z1;
 constexpr int Z2_OFF_BAR = zm_round128(Z2_OFF_Z1 + 2 * Z2_RING_Z1 * 4);
-constexpr int Z2_OFF_FLAG = Z2_OFF_BAR + 8 * (Z2_STAGES + 1);   // two abort flags (plane parity)
-constexpr int Z2_SMEM = Z2_OFF_FLAG + 16 + 128;
+constexpr int Z2_SMEM = Z2_OFF_BAR + 8 * (Z2_STAGES + 1) + 128;
 
 static_assert(Z2_TX % 4 == 0 && Z2_BW <= 256 && Z2_HR <= 256, "TMA box limits");
 static_assert(Z2_STAGES >= 2, "two stages at least");
@@ -194,10 +194,6 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     extern __shared__ unsigned char z2_raw[];
     unsigned char *smem = z2_raw + ((128 - (smem_addr(z2_raw) & 127)) & 127);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Z2_OFF_BAR);   // [STAGES] + prev
-    // abort flags: the prologue and the planes of even count from f use [0],
-    // the others [1], so that a thread setting the flag of plane q+1 never
-    // changes the one another thread still reads after plane q's barrier
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Z2_OFF_FLAG);
     float *ZK = reinterpret_cast<float *>(smem + Z2_OFF_ZK);
     float *MR = reinterpret_cast<float *>(smem + Z2_OFF_MR);
     float *Z1 = reinterpret_cast<float *>(smem + Z2_OFF_Z1);
@@ -217,7 +213,6 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
 
     if (tid == 0) {
         for (int k = 0; k <= Z2_STAGES; ++k) mbar_init(&bars[k], 1);
-        abort_flag[0] = abort_flag[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -320,21 +315,15 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
 
     float4 ZKc = f4zero();                      // z^k of this quad, current plane
     float4 Bc = f4zero();                       // b of this quad, current plane
-    // prologue: z^k of plane f
-    {
-        bool ok = true;
-        if (f > 0) ok = mbar_wait_tma(&bars[Z2_STAGES], 0, polls(f));
-        ok = ok && mbar_wait_tma(&bars[slot(f)], parity(f), polls(f));
-        if (ok) {
-            if (doA)
-                ZKc = zk_quad(f, stage(f), f > 0 ? reinterpret_cast<const float *>(smem + Z2_OFF_PREV) : nullptr,
-                              Bc);
-        } else {
-            abort_flag[0] = 1;
-        }
-    }
-    __syncthreads();
-    bool aborted = abort_flag[0] != 0;
+    // prologue: z^k of plane f.  A wait that gives up is reported through
+    // the barrier itself (its OR over the threads), so every thread takes
+    // the same decision with no flag in shared memory.
+    bool ok = true;
+    if (f > 0) ok = mbar_wait_tma(&bars[Z2_STAGES], 0, polls(f));
+    ok = ok && mbar_wait_tma(&bars[slot(f)], parity(f), polls(f));
+    if (ok && doA)
+        ZKc = zk_quad(f, stage(f), f > 0 ? reinterpret_cast<const float *>(smem + Z2_OFF_PREV) : nullptr, Bc);
+    bool aborted = __syncthreads_or(!ok) != 0;
 
     const long long No = PADDED_OUT ? za.No : za.N;
     const int opx = PADDED_OUT ? za.opx : nx;
@@ -351,14 +340,14 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
         constexpr bool edge = decltype(edge_tag)::value;
         for (int q = f; q <= ze && !aborted; ++q) {
             qlast = q;
-            volatile int *flag = abort_flag + ((q - f + 1) & 1);
+            bool failed = false;
             // ---- A: z^k of plane q+1 -------------------------------------------
             float4 ZKn = f4zero(), Bn = f4zero();
             if (q + 1 <= last) {
                 if (mbar_wait_tma(&bars[slot(q + 1)], parity(q + 1), polls(q + 1))) {
                     if (doA) ZKn = zk_quad(q + 1, stage(q + 1), F(stage(q), Z2_OFF_R2), Bn);
                 } else {
-                    *flag = 1;
+                    failed = true;
                 }
             }
             // ---- B: step k on plane q over the grown tile ----------------------
@@ -415,8 +404,7 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
                 nR2 = R2;
             }
             ZKc = ZKn;
-            __syncthreads();
-            if (*flag) {
+            if (__syncthreads_or(failed)) {
                 aborted = true;
                 break;
             }
