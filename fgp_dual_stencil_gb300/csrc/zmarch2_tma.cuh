@@ -70,9 +70,10 @@ namespace tvfgp {
 #define TVFGP_Z2_CTAS 3           // CTAs per SM the shared memory is sized for
 #endif
 // The minimum CTAs per SM given to the compiler: 2 leaves it up to 204
-// registers a thread, and it then takes 114, for a schedule measured 0.5%
-// faster than the one it builds in the 136 that 3 CTAs allow (110
-// registers).  Three CTAs still fit: 3 x 160 x 114 registers <= 65536.
+// registers a thread; it takes 113 to 118 (by version of the kernel), for
+// a schedule measured 0.4-0.5% faster than the one it builds within the
+// 136 that 3 CTAs allow.  Three CTAs still fit while it takes at most 136
+// (3 x 160 x 136 <= 65536); the build log shows the count.
 #ifndef TVFGP_Z2_MINB
 #define TVFGP_Z2_MINB 2
 #endif
