@@ -296,11 +296,14 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
     };
     // z^{k+1} of plane q for the quad at (c = lx, ly) whose b is Bq,
     // stored and returned
-    auto z1_quad = [&](int q, int c, int ly, float4 Bq) {
-        const float *M0 = mrp(q, 0), *M1 = mrp(q, 1), *M2 = mrp(q, 2);
+    // (the quad's own r^{k+1} of plane q, R0..R2, and r_z^{k+1} of plane q-1,
+    // R2lo, come from the registers of this thread, which made them in step
+    // k; only the x-1 and y-1 neighbours are read from the ring)
+    auto z1_quad = [&](int q, int c, int ly, float4 Bq, float4 R0, float4 R1, float4 R2, float4 R2lo) {
+        const float *M0 = mrp(q, 0), *M1 = mrp(q, 1);
         const int mo = (ly + 1) * Z2_PK + c + 4;                     // r^{k+1} at (lx = c, ly)
-        const float4 Z = zquad(Bq, lds4(M0 + mo), lds4(M1 + mo), lds4(M2 + mo), M0[mo - 1],
-                               lds4(M1 + mo - Z2_PK), q > 0 ? lds4(mrp(q - 1, 2) + mo) : f4zero(), lam, nzero);
+        const float4 Z = zquad(Bq, R0, R1, R2, M0[mo - 1], lds4(M1 + mo - Z2_PK), q > 0 ? R2lo : f4zero(), lam,
+                               nzero);
         *reinterpret_cast<float4 *>(z1p(q) + ly * Z2_P1 + c) = Z;
         return Z;
     };
@@ -420,7 +423,7 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
             // (each quad by the thread that computed z^k there, which holds its b)
             float4 Z1n = f4zero();
             if (q >= z0 && q <= uk_last && doC) {
-                const float4 Z = z1_quad(q, my_c - 4, my_row - 1, Bc);
+                const float4 Z = z1_quad(q, my_c - 4, my_row - 1, Bc, nR0, nR1, nR2, cR2);
                 if (my_tile) Z1n = Z;
             }
             Bc = Bn;
