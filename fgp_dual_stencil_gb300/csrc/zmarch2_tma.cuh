@@ -16,27 +16,29 @@
 //
 //   at iteration q:
 //     A  z^k     of plane q+1 on x0-1..x0+TX+1, y0-1..y0+TY+1   (staged b, r^k)
-//     B  step k  of plane q   on x0-1..x0+TX,   y0-1..y0+TY     (-> r^{k+1} shared, p^{k+1} registers)
+//     B  step k  of plane q   on x0-1..x0+TX,   y0-1..y0+TY     (-> r_x, r_y^{k+1} shared, all in registers)
 //     -- barrier
-//     C  z^{k+1} of plane q   on x0..x0+TX,     y0..y0+TY       (b in registers, r^{k+1})
+//     C  z^{k+1} of plane q   on x0..x0+TX,     y0..y0+TY       (b, own r^{k+1} in registers)
 //     D  step k+1 of plane q-1 on the tile                      (-> p^{k+2}, r^{k+2} in HBM)
 //
 // One barrier per plane suffices.  Across it every phase reads what the
 // phases before it wrote.  Without a second one, a thread may already run
 // A and B of plane q+1 while another still runs C and D of plane q, so what
-// the latter read must not be overwritten by the former: step k+1 takes its
-// own r^{k+1} and p^{k+1} from the registers of the thread that made them
-// (one plane earlier), C reads r^{k+1} of plane q and r_z^{k+1} of plane q-1,
-// and B of plane q+1 writes r^{k+1} into a third slot for r_z (two for
-// r_x, r_y).  The z rings and the stages are written only at points that
-// one barrier already separates from their readers; a wait that gives up is
-// reported through that barrier (its OR over the threads).
+// the latter read must not be overwritten by the former: C and step k+1
+// take the quad's own r^{k+1} (and step k+1 its p^{k+1}) from the registers
+// of the thread that made them, and C reads from shared memory only r_x of
+// plane q at x-1 and r_y at y-1, which B of plane q+1 writes into the other
+// of two slots.  r_z^{k+1} is needed only at the quad's own column, so it
+// never goes through shared memory.  The z rings and the stages are written
+// only at points that one barrier already separates from their readers; a
+// wait that gives up is reported through that barrier (its OR over the
+// threads).
 //
 // Each thread owns one quad (four x voxels) and runs A and B, and C and D,
 // on it: the voxel's own z^k, z^{k+1}, p^{k+1} and r^{k+1} stay in its
 // registers from the phase that makes them to the phase that uses them, and
 // only the x+1 / y+1 neighbours' z and the r^{k+1} halo go through shared
-// memory (rings of two or three planes).  Voxels of the ring that
+// memory (rings of two planes).  Voxels of the ring that
 // lie outside the volume get r^{k+1} = 0: that is the r(-1) = 0 boundary step
 // k+1 sees.
 // Every value is computed by the same expressions, in the same order, as in
@@ -148,13 +150,13 @@ constexpr int Z2_RING_B = Z2_TASKS_B - Z2_TASKS_D;        // 2 QA + 2 TY
 static_assert(Z2_RING_B == 2 * Z2_QA + 2 * Z2_TY && Z2_TASKS_A - Z2_TASKS_B == Z2_QA, "thread roles");
 static_assert(Z2_TASKS_B <= Z2_THREADS && Z2_TASKS_A <= Z2_THREADS, "thread roles");
 
-// shared rings (z^k, z^{k+1}: two slots; r^{k+1}: two slots for r_x, r_y and
-// three for r_z, see above); pitches in floats
+// shared rings (z^k, z^{k+1}, and r_x, r_y of r^{k+1}: two slots each, see
+// above); pitches in floats
 constexpr int Z2_PK = Z2_BW;                              // z^k and r^{k+1}: columns lx+4
 constexpr int Z2_P1 = Z2_TX + 4;                          // z^{k+1}: columns lx
 constexpr int Z2_RING_ZK = (Z2_TY + 3) * Z2_PK;           // floats per slot
 constexpr int Z2_MR_COMP = (Z2_TY + 2) * Z2_PK;
-constexpr int Z2_MR_SLOTS = 2 + 2 + 3;                    // r_x, r_y: 2 slots each; r_z: 3
+constexpr int Z2_MR_SLOTS = 2 + 2;                        // r_x, r_y: 2 slots each
 constexpr int Z2_RING_Z1 = (Z2_TY + 1) * Z2_P1;
 constexpr int Z2_OFF_ZK = Z2_STAGES * Z2_STAGE_STRIDE;
 constexpr int Z2_OFF_MR = zm_round128(Z2_OFF_ZK + 2 * Z2_RING_ZK * 4);
@@ -241,9 +243,7 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
 
     auto F = [](const unsigned char *st, int off) { return reinterpret_cast<const float *>(st + off); };
     auto zkp = [&](int q) { return ZK + (q & 1) * Z2_RING_ZK; };
-    auto mrp = [&](int q, int a) {
-        return MR + (a < 2 ? (q & 1) * 2 + a : 4 + q % 3) * Z2_MR_COMP;
-    };
+    auto mrp = [&](int q, int a) { return MR + ((q & 1) * 2 + a) * Z2_MR_COMP; };   // a = 0 (x), 1 (y)
     auto z1p = [&](int q) { return Z1 + (q & 1) * Z2_RING_Z1; };
 
     // this thread's quad in the z^k / step-k grid (c = lx + 4, row = ly + 1)
@@ -399,7 +399,6 @@ fgp_step2_zmarch_tma(const __grid_constant__ Zmarch2Args za)
                 const int mo = row * Z2_PK + c;
                 *reinterpret_cast<float4 *>(mrp(q, 0) + mo) = R0;
                 *reinterpret_cast<float4 *>(mrp(q, 1) + mo) = R1;
-                *reinterpret_cast<float4 *>(mrp(q, 2) + mo) = R2;
                 nP0 = P0;
                 nP1 = P1;
                 nP2 = P2;
