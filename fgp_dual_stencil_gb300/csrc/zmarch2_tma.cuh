@@ -72,7 +72,7 @@ namespace tvfgp {
 #define TVFGP_Z2_CTAS 3           // CTAs per SM the shared memory is sized for
 #endif
 // The minimum CTAs per SM given to the compiler: 2 leaves it up to 204
-// registers a thread; it takes 113 to 118 (by version of the kernel), for
+// registers a thread; it takes 110 to 118 (by version of the kernel), for
 // a schedule measured 0.4-0.5% faster than the one it builds within the
 // 136 that 3 CTAs allow.  Three CTAs still fit while it takes at most 136
 // (3 x 160 x 136 <= 65536); the build log shows the count.
